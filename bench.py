@@ -1,0 +1,417 @@
+"""Benchmark of the fused NHWC convolution layer on GB300.
+
+One step = one pass of every layer of the batch-8 bf16 throughput sweep
+(3x3 64->128 @160x160, 3x3 256->256 @80x80, 3x3 512->1024 @40x40,
+1x1 1024->512 @20x20, depthwise 3x3 512 @40x40; Mish epilogue), inputs
+resident in HBM, through the library's C ABI.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+Timing: W untimed warm-up steps, then K timed steps.  Before every step the
+L2 is flushed (a write of a buffer twice the L2 size) outside the step's
+CUDA-event pair; each layer is also bracketed by events on the launching
+stream, which gives the per-layer durations and the dominant kernel's
+roofline.  `value` = algorithmic FLOPs (2 * MACs) of all layers of all ranks
+/ the slowest rank's summed step time.  `e2e` times the same step through
+the same API from pinned host buffers (host->device copies of x, w, b and
+device->host copy of y inside the timed region).  `cpu_baseline` times the
+CPU oracle on a bounded random sample of output points of the same layers.
+`--impl reference` times that oracle alone on the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused conv TFLOP/s (bf16) & TOPS (int8) per layer shape; % of GB300 roofline"
+DEFAULT_WORKLOAD = "sweep_b8_bf16"
+# Fallback peaks (one earlier GB300 measurement) when MEASURED_PEAKS.json is absent.
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+def flops_of(spec):
+    from conv_workloads import macs
+    return 2.0 * macs(spec)
+
+
+def layer_bound(spec, peaks):
+    """Which roof binds a layer: compare its arithmetic intensity with the
+    ridge (bf16 peak / HBM bandwidth)."""
+    from conv_workloads import alg_bytes
+    ai = flops_of(spec) / alg_bytes(spec)
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    return ("tensor" if ai >= ridge else "hbm"), ai
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples nvidia-smi clocks / throttle reasons every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index=0):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, device):
+    import torch
+
+    import convolution_nhwc_implicit_gb300 as cl
+    from conv_workloads import CONFIGS, alg_bytes, generate, macs, output_hw
+
+    peaks, peaks_src = load_peaks()
+    torch.cuda.set_device(device)
+    dev = torch.device("cuda", device)
+    layers = generate(args.workload)
+    plans, X, Wt, B, Y = [], [], [], [], []
+    for d in layers:
+        s = d.spec
+        quant = (s.in_scale, s.out_scale, d.w_scales.tolist()) if s.dtype == "i8" else None
+        p = cl.Plan(s.n, s.h, s.w, s.cin, s.cout, s.kh, s.kw, s.stride, s.pad_h, s.pad_w, s.groups,
+                    s.dtype, s.act, quant)
+        plans.append(p)
+        X.append(d.x.to(dev))
+        Wt.append(d.w.to(dev))
+        B.append(None if d.b is None else d.b.to(dev))
+        Y.append(torch.empty(p.output_shape, dtype=d.x.dtype, device=dev))
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    nl = len(layers)
+
+    def step(ev=None):
+        for i in range(nl):
+            if ev is not None:
+                ev[i].record(stream)
+            plans[i].run(X[i], Wt[i], B[i], Y[i], stream)
+        if ev is not None:
+            ev[nl].record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(args.steps)]
+    clocks = ClockSampler(device)
+    clocks.start()
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        step(events[k])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+    for p in plans:
+        p.check_device_status()
+
+    per_layer = np.zeros((args.steps, nl))
+    step_ms = np.zeros(args.steps)
+    for k in range(args.steps):
+        for i in range(nl):
+            per_layer[k, i] = events[k][i].elapsed_time(events[k][i + 1])
+        step_ms[k] = events[k][0].elapsed_time(events[k][nl])
+    my_ms = float(step_ms.sum())
+    if world > 1:
+        t = torch.tensor([my_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        my_ms = float(t.item())
+    total_flops = sum(flops_of(d.spec) for d in layers)
+    ms_per_step = my_ms / args.steps
+    value = total_flops * world * args.steps / (my_ms * 1e-3) / 1e12
+
+    # ---- per-layer figures and the dominant kernel's roofline
+    layer_rows = []
+    for i, d in enumerate(layers):
+        s = d.spec
+        us = float(per_layer[:, i].mean() * 1e3)
+        bound, ai = layer_bound(s, peaks)
+        fl = flops_of(s)
+        by = alg_bytes(s)
+        if bound == "tensor":
+            ach, pk, unit = fl / (us * 1e-6) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+        else:
+            ach, pk, unit = by / (us * 1e-6) / 1e9, peaks["hbm_gbs"], "GB/s"
+        layer_rows.append({
+            "layer": s.name, "kernel": plans[i].describe(), "us": round(us, 2),
+            "tflops": round(fl / (us * 1e-6) / 1e12, 1), "gbs": round(by / (us * 1e-6) / 1e9, 1),
+            "ai_flop_per_byte": round(ai, 1), "bound": bound,
+            "achieved": round(ach, 1), "peak": pk, "unit": unit, "frac": round(ach / pk, 4),
+        })
+    dom = max(range(nl), key=lambda i: per_layer[:, i].mean())
+    dr = layer_rows[dom]
+    traffic = _traffic_for(layers[dom].spec.name, plans[dom].describe())
+    roofline = {"bound": dr["bound"], "achieved": dr["achieved"], "peak": dr["peak"], "unit": dr["unit"],
+                "frac": dr["frac"], "traffic": traffic, "kernel": layers[dom].spec.name,
+                "peak_source": f"{peaks_src} ({'bf16 burst' if dr['bound'] == 'tensor' else 'HBM copy'})"}
+
+    # ---- end to end through the same API, from pinned host memory
+    e2e = run_e2e(args, layers, plans, dev, stream, total_flops, world)
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "layers": len(layers),
+                   "batch_per_gpu": layers[0].spec.n, "l2": "flushed before every step (outside the events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roofline, "layers": layer_rows, "e2e": e2e,
+        "gpu_launches": nl * args.steps, "clocks": clk, "wall_s_timed_region": round(wall, 4),
+    }
+    return out
+
+
+def run_e2e(args, layers, plans, dev, stream, total_flops, world):
+    """Same step, but inputs start in pinned host memory and y returns to it."""
+    import torch
+    hx = [d.x.pin_memory() for d in layers]
+    hw = [d.w.pin_memory() for d in layers]
+    hb = [None if d.b is None else d.b.pin_memory() for d in layers]
+    hy = [torch.empty(p.output_shape, dtype=d.x.dtype).pin_memory() for p, d in zip(plans, layers)]
+    dx = [torch.empty_like(t, device=dev) for t in hx]
+    dw = [torch.empty_like(t, device=dev) for t in hw]
+    db = [None if t is None else torch.empty_like(t, device=dev) for t in hb]
+    dy = [torch.empty(t.shape, dtype=t.dtype, device=dev) for t in hy]
+    h2d = sum(t.numel() * t.element_size() for t in hx + hw + [t for t in hb if t is not None])
+    d2h = sum(t.numel() * t.element_size() for t in hy)
+
+    def step():
+        for i, p in enumerate(plans):
+            dx[i].copy_(hx[i], non_blocking=True)
+            dw[i].copy_(hw[i], non_blocking=True)
+            if hb[i] is not None:
+                db[i].copy_(hb[i], non_blocking=True)
+            p.run(dx[i], dw[i], db[i], dy[i], stream)
+            hy[i].copy_(dy[i], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    k = max(1, args.steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(k):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": round(total_flops * world * k / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(ms / k, 4)}
+
+
+def _traffic_for(layer_name, kernel_desc):
+    """DRAM bytes per launch of this kernel from the committed ncu summary
+    (profiles/dram_traffic.json), if it was captured for this exact kernel."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(layer_name)
+    if not e or e.get("kernel") != kernel_desc:
+        return None
+    return e.get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_sample(layers, budget_s, seed=0):
+    """Times the oracle on a bounded random sample of output points of every
+    layer, sized from a short calibration so the whole sample takes about
+    budget_s seconds.  Returns (flops_done, seconds, points, threads)."""
+    import oracle
+    from conv_workloads import macs, output_hw
+    prepared = []
+    for d in layers:
+        s = d.spec
+        if s.dtype == "i8":
+            raise NotImplementedError("bench workloads are float")
+        prepared.append((s, d.x.double().numpy(), d.w.double().numpy(),
+                         None if d.b is None else d.b.double().numpy()))
+    rng = np.random.default_rng(seed)
+
+    def pts_for(s, count):
+        oh, ow = output_hw(s)
+        return np.stack([rng.integers(0, s.n, count), rng.integers(0, oh, count), rng.integers(0, ow, count),
+                         rng.integers(0, s.cout, count)], axis=1).astype(np.int32)
+
+    def run(frac):
+        fl, secs, npts = 0.0, 0.0, 0
+        for s, x, w, b in prepared:
+            oh, ow = output_hw(s)
+            total = s.n * oh * ow * s.cout
+            count = max(16, int(total * frac))
+            pts = pts_for(s, count)
+            t0 = time.perf_counter()
+            oracle.conv_f64_points(x, w, b, pts, s.stride, s.pad_h, s.pad_w, s.groups, s.act)
+            secs += time.perf_counter() - t0
+            fl += 2.0 * macs(s) * count / total
+            npts += count
+        return fl, secs, npts
+
+    frac = 2e-5
+    fl, secs, npts = run(frac)
+    scale = max(1.0, budget_s / max(secs, 1e-3))
+    fl, secs, npts = run(min(1.0, frac * scale))
+    return fl, secs, npts, oracle.max_threads(0)
+
+
+def cpu_baseline(layers, budget_s=12.0):
+    fl, secs, npts, thr = oracle_sample(layers, budget_s)
+    return {"value": round(fl / secs / 1e12, 6), "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+            "sample": f"{npts} random output points across the {len(layers)} layers "
+                      f"({fl / 1e9:.2f} GFLOP, {secs:.1f} s, fp64 nested loops, OpenMP)"}
+
+
+def run_reference(args):
+    from conv_workloads import generate
+    layers = generate(args.workload)
+    per_step_budget = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(layers, per_step_budget / 4, seed=1)
+    fl_tot, s_tot, pts_tot, thr = 0.0, 0.0, 0, 1
+    for k in range(args.steps):
+        fl, secs, npts, thr = oracle_sample(layers, per_step_budget, seed=100 + k)
+        fl_tot += fl
+        s_tot += secs
+        pts_tot += npts
+    value = fl_tot / s_tot / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s_tot / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "layers": len(layers), "batch_per_gpu": layers[0].spec.n,
+                   "note": "CPU oracle on a bounded random sample of output points per step"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                         "sample": f"{pts_tot} output points over {args.steps} steps "
+                                   f"({fl_tot / 1e9:.2f} GFLOP in {s_tot:.1f} s)"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ---------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import __graft_entry__
+    __graft_entry__.build()
+    out = run_ours(args, rank, world, local)
+    if rank == 0 and not args.no_cpu_baseline:
+        from conv_workloads import generate
+        out["cpu_baseline"] = cpu_baseline(generate(args.workload))
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,247 @@
+// C ABI of the fused NHWC convolution library (declared in conv_nhwc.h):
+// argument validation, plan construction, kernel-family selection and the
+// stream-ordered run entry point.
+//
+// Validation happens at plan creation, before any CUDA call, so that an
+// invalid or unsupported layer is a named failure at preparation time
+// ("nanoinfer", "Pooling read int8 tensors through a float*": unsupported
+// op / dtype pairs become a named load failure instead of quiet garbage).
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "conv_internal.h"
+
+namespace {
+
+// floor((in + 2 * pad - k) / stride) + 1, or -1 when no output fits.
+long long out_dim(long long in, long long k, long long pad, long long stride) {
+    const long long span = in + 2 * pad - k;
+    if (span < 0) return -1;
+    return span / stride + 1;
+}
+
+int validate(const conv_shape_t *s, int stride, int pad_h, int pad_w, int groups, conv_dtype_t dtype,
+             conv_act_t act, const conv_quant_t *quant, int *oh, int *ow) {
+    if (s->n < 0 || s->h < 1 || s->w < 1 || s->c_in < 1 || s->c_out < 1 || s->k_h < 1 || s->k_w < 1)
+        return CONV_ERR_INVALID_SHAPE;
+    if (stride < 1 || pad_h < 0 || pad_w < 0 || groups < 1) return CONV_ERR_INVALID_SHAPE;
+    if (s->c_in % groups != 0 || s->c_out % groups != 0) return CONV_ERR_INVALID_SHAPE;
+    if ((int)dtype < CONV_F32 || (int)dtype > CONV_I8) return CONV_ERR_INVALID_ARG;
+    if ((int)act < CONV_ACT_NONE || (int)act > CONV_ACT_MISH) return CONV_ERR_INVALID_ARG;
+    const long long OH = out_dim(s->h, s->k_h, pad_h, stride);
+    const long long OW = out_dim(s->w, s->k_w, pad_w, stride);
+    if (OH < 1 || OW < 1) return CONV_ERR_INVALID_SHAPE;
+    // Size limits of the kernels' index arithmetic.
+    const long long cpg = s->c_in / groups;
+    const long long x_elems = (long long)s->n * s->h * s->w * s->c_in;
+    const long long y_elems = (long long)s->n * OH * OW * s->c_out;
+    const long long w_elems = (long long)s->c_out * s->k_h * s->k_w * cpg;
+    const long long lim = 1ll << 40;
+    if (x_elems >= lim || y_elems >= lim || w_elems >= lim) return CONV_ERR_UNSUPPORTED;
+    if ((long long)s->n * OH * OW >= (1ll << 31) || (long long)s->n * s->h * s->w >= (1ll << 32))
+        return CONV_ERR_UNSUPPORTED;
+    if (dtype == CONV_I8) {
+        if (!quant || !quant->w_scales) return CONV_ERR_NULL_ARG;
+        if (!(quant->in_scale > 0.0f) || !(quant->out_scale > 0.0f) || !isfinite(quant->in_scale) ||
+            !isfinite(quant->out_scale))
+            return CONV_ERR_INVALID_ARG;
+        for (int co = 0; co < s->c_out; ++co)
+            if (!(quant->w_scales[co] > 0.0f) || !isfinite(quant->w_scales[co])) return CONV_ERR_INVALID_ARG;
+        // An int8 MAC is < 2^14 in magnitude: the int32 accumulator of a
+        // dot product of length K is exact while K * 2^14 < 2^31.
+        if ((long long)s->k_h * s->k_w * cpg >= (1ll << 17)) return CONV_ERR_UNSUPPORTED;
+        // Mish of a requantised value is not bit-reproducible across
+        // implementations of expf; the int8 path offers NONE and RELU.
+        if (act == CONV_ACT_MISH) return CONV_ERR_UNSUPPORTED;
+    } else if (quant) {
+        return CONV_ERR_INVALID_ARG;
+    }
+    *oh = (int)OH;
+    *ow = (int)OW;
+    return CONV_OK;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int conv_abi_version(void) { return CONV_NHWC_ABI_VERSION; }
+
+const char *conv_status_str(int status) {
+    switch (status) {
+    case CONV_OK: return "CONV_OK";
+    case CONV_ERR_NULL_ARG: return "CONV_ERR_NULL_ARG";
+    case CONV_ERR_INVALID_SHAPE: return "CONV_ERR_INVALID_SHAPE";
+    case CONV_ERR_UNSUPPORTED: return "CONV_ERR_UNSUPPORTED";
+    case CONV_ERR_MISALIGNED: return "CONV_ERR_MISALIGNED";
+    case CONV_ERR_ALIASING: return "CONV_ERR_ALIASING";
+    case CONV_ERR_CUDA: return "CONV_ERR_CUDA";
+    case CONV_ERR_DEVICE_TIMEOUT: return "CONV_ERR_DEVICE_TIMEOUT";
+    case CONV_ERR_OOM: return "CONV_ERR_OOM";
+    case CONV_ERR_INVALID_ARG: return "CONV_ERR_INVALID_ARG";
+    default: return "CONV_ERR_UNKNOWN";
+    }
+}
+
+int conv_plan_create_ex(const conv_shape_t *shape, int stride, int pad_h, int pad_w, int groups,
+                        conv_dtype_t dtype, conv_act_t act, const conv_quant_t *quant, conv_algo_t algo,
+                        conv_plan_t **out_plan) {
+    if (!out_plan) return CONV_ERR_NULL_ARG;
+    *out_plan = nullptr;
+    if (!shape) return CONV_ERR_NULL_ARG;
+    if ((int)algo < CONV_ALGO_AUTO || (int)algo > CONV_ALGO_IGEMM) return CONV_ERR_INVALID_ARG;
+    int oh = 0, ow = 0;
+    int rc = validate(shape, stride, pad_h, pad_w, groups, dtype, act, quant, &oh, &ow);
+    if (rc != CONV_OK) return rc;
+
+    conv_plan *p = new (std::nothrow) conv_plan();
+    if (!p) return CONV_ERR_OOM;
+    p->s = *shape;
+    p->stride = stride; p->pad_h = pad_h; p->pad_w = pad_w; p->groups = groups;
+    p->dtype = dtype; p->act = act; p->oh = oh; p->ow = ow;
+
+    // Device properties.  The kernels are built for sm_103a only.
+    cudaDeviceProp prop;
+    if (cudaGetDevice(&p->device) != cudaSuccess ||
+        cudaGetDeviceProperties(&prop, p->device) != cudaSuccess) {
+        delete p;
+        return CONV_ERR_CUDA;
+    }
+    if (prop.major != 10 || prop.minor != 3) {
+        delete p;
+        return CONV_ERR_UNSUPPORTED;
+    }
+    p->num_sms = prop.multiProcessorCount;
+
+    // Kernel family.
+    const bool can_ig = igemm_supported(p), can_dw = dw3x3_supported(p), can_direct = direct_supported(p);
+    int chosen = -1;
+    if (algo == CONV_ALGO_AUTO)
+        chosen = can_ig ? CONV_ALGO_IGEMM : (can_dw ? CONV_ALGO_DEPTHWISE : (can_direct ? CONV_ALGO_DIRECT : -1));
+    else if (algo == CONV_ALGO_IGEMM && can_ig) chosen = CONV_ALGO_IGEMM;
+    else if (algo == CONV_ALGO_DEPTHWISE && can_dw) chosen = CONV_ALGO_DEPTHWISE;
+    else if (algo == CONV_ALGO_DIRECT && can_direct) chosen = CONV_ALGO_DIRECT;
+    if (chosen < 0) {
+        delete p;
+        return CONV_ERR_UNSUPPORTED;
+    }
+    p->algo = chosen;
+
+    // Device-side state: status word and (int8) requantisation multipliers.
+    if (cudaMalloc(&p->d_status, sizeof(int)) != cudaSuccess) {
+        delete p;
+        return CONV_ERR_OOM;
+    }
+    if (cudaMemset(p->d_status, 0, sizeof(int)) != cudaSuccess) {
+        conv_plan_destroy(p);
+        return CONV_ERR_CUDA;
+    }
+    if (dtype == CONV_I8) {
+        float *hm = (float *)malloc(sizeof(float) * shape->c_out);
+        if (!hm) { conv_plan_destroy(p); return CONV_ERR_OOM; }
+        // M[co] = s_x * s_w[co] / s_y, formed in double and rounded once.
+        for (int co = 0; co < shape->c_out; ++co)
+            hm[co] = (float)((double)quant->in_scale * (double)quant->w_scales[co] / (double)quant->out_scale);
+        if (cudaMalloc(&p->d_mult, sizeof(float) * shape->c_out) != cudaSuccess) {
+            free(hm);
+            conv_plan_destroy(p);
+            return CONV_ERR_OOM;
+        }
+        const cudaError_t e = cudaMemcpy(p->d_mult, hm, sizeof(float) * shape->c_out, cudaMemcpyHostToDevice);
+        free(hm);
+        if (e != cudaSuccess) { conv_plan_destroy(p); return CONV_ERR_CUDA; }
+    }
+
+    if (chosen == CONV_ALGO_IGEMM) {
+        rc = igemm_configure(p);
+        if (rc != CONV_OK) { conv_plan_destroy(p); return rc; }
+    } else if (chosen == CONV_ALGO_DEPTHWISE) {
+        dw3x3_configure(p);
+        snprintf(p->desc, sizeof(p->desc), "dw3x3 %s rows/thread=%d threads=%lld",
+                 dtype == CONV_F32 ? "f32" : (dtype == CONV_BF16 ? "bf16" : "i8"), p->dw.th, p->dw.items);
+    } else {
+        snprintf(p->desc, sizeof(p->desc), "direct %s",
+                 dtype == CONV_F32 ? "f32-ffma" : (dtype == CONV_BF16 ? "bf16-ffma" : "i8-dp4a"));
+    }
+    *out_plan = p;
+    return CONV_OK;
+}
+
+int conv_plan_create(const conv_shape_t *shape, int stride, int pad_h, int pad_w, int groups,
+                     conv_dtype_t dtype, conv_act_t act, const conv_quant_t *quant, conv_plan_t **out_plan) {
+    return conv_plan_create_ex(shape, stride, pad_h, pad_w, groups, dtype, act, quant, CONV_ALGO_AUTO,
+                               out_plan);
+}
+
+void conv_plan_destroy(conv_plan_t *plan) {
+    if (!plan) return;
+    if (plan->d_status) cudaFree(plan->d_status);
+    if (plan->d_mult) cudaFree(plan->d_mult);
+    delete plan;
+}
+
+int conv_plan_output_shape(const conv_plan_t *plan, int *oh, int *ow) {
+    if (!plan || !oh || !ow) return CONV_ERR_NULL_ARG;
+    *oh = plan->oh;
+    *ow = plan->ow;
+    return CONV_OK;
+}
+
+int conv_plan_algo(const conv_plan_t *plan) {
+    if (!plan) return CONV_ERR_NULL_ARG;
+    return plan->algo;
+}
+
+const char *conv_plan_describe(const conv_plan_t *plan) { return plan ? plan->desc : ""; }
+
+int conv_run(const conv_plan_t *plan, const void *x, const void *w, const void *bias, void *y, void *stream) {
+    if (!plan) return CONV_ERR_NULL_ARG;
+    const conv_plan *p = plan;
+    if (p->s.n == 0) return CONV_OK;  // empty batch: nothing to compute
+    if (!x || !w || !y) return CONV_ERR_NULL_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias))) return CONV_ERR_MISALIGNED;
+    const size_t es = (size_t)conv_esize(p->dtype);
+    const size_t xb = (size_t)p->s.n * p->s.h * p->s.w * p->s.c_in * es;
+    const size_t wb = (size_t)p->s.c_out * p->s.k_h * p->s.k_w * (p->s.c_in / p->groups) * es;
+    const size_t bb = bias ? (size_t)p->s.c_out * 4 : 0;
+    const size_t yb = (size_t)p->s.n * p->oh * p->ow * p->s.c_out * es;
+    if (overlaps(y, yb, x, xb) || overlaps(y, yb, w, wb) || overlaps(y, yb, bias, bb)) return CONV_ERR_ALIASING;
+
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e;
+    switch (p->algo) {
+    case CONV_ALGO_IGEMM: return launch_igemm(p, x, w, bias, y, st);
+    case CONV_ALGO_DEPTHWISE: e = launch_dw3x3(p, x, w, bias, y, st); break;
+    default: e = launch_direct(p, x, w, bias, y, st); break;
+    }
+    return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+}
+
+int conv_plan_check_device_status(conv_plan_t *plan, void *stream) {
+    if (!plan) return CONV_ERR_NULL_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    int h = 0;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return CONV_ERR_CUDA;
+    if (cudaMemcpy(&h, plan->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return CONV_ERR_CUDA;
+    if (h != 0) {
+        if (cudaMemset(plan->d_status, 0, sizeof(int)) != cudaSuccess) return CONV_ERR_CUDA;
+        return CONV_ERR_DEVICE_TIMEOUT;
+    }
+    return CONV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,76 @@
+// Internal declarations of the fused NHWC convolution library: the plan
+// structure and the launchers of the three kernel families.  Not part of the
+// public ABI (include/conv_nhwc.h is).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "conv_nhwc.h"
+
+// Status word codes written by kernels (device side) into the plan's status
+// word; conv_plan_check_device_status maps any nonzero value to
+// CONV_ERR_DEVICE_TIMEOUT.
+enum {
+    KSTATUS_OK = 0,
+    KSTATUS_TIMEOUT_PRODUCER = 1,  // TMA warp gave up waiting for a free stage
+    KSTATUS_TIMEOUT_MMA = 2,       // MMA warp gave up waiting for data / TMEM
+    KSTATUS_TIMEOUT_EPILOGUE = 3,  // epilogue gave up waiting for an accumulator
+};
+
+// Geometry of the tcgen05 implicit-GEMM launch chosen at plan time.
+struct IgemmGeom {
+    int bn;        // output channels per tile (UMMA N): 64, 128 or 256
+    int bk;        // input channels per K block: 64, 32 or 16 (128/64/32-byte rows)
+    int flat;      // 1: 1x1 / stride 1 / pad 0, A is x viewed as [N*H*W, Cin]
+    int bw, bh;    // spatial mode: an M tile is a bh x bw rectangle of output pixels
+    int tiles_w, tiles_h, tiles_m, tiles_n, num_tiles;
+    int cblocks;   // Cin / bk
+    int kblocks;   // k_h * k_w * cblocks: K blocks per tile
+    int stages;    // shared-memory pipeline depth
+    int grid;      // persistent CTAs
+    int smem;      // dynamic shared memory bytes
+    int in_i8;     // operands are int8 (converted to bf16 on chip)
+};
+
+struct DwGeom {
+    int th;        // output rows per thread (register sliding window)
+    int nstrips;   // ceil(OH / th)
+    long long items;
+};
+
+struct conv_plan {
+    conv_shape_t s;
+    int stride, pad_h, pad_w, groups;
+    conv_dtype_t dtype;
+    conv_act_t act;
+    int oh, ow;
+    int algo;          // conv_algo_t actually used
+    int device;
+    int num_sms;
+    float *d_mult;     // int8: requantisation multipliers M[co] (device)
+    int *d_status;     // device status word (bounded-wait timeouts)
+    IgemmGeom ig;
+    DwGeom dw;
+    char desc[192];
+};
+
+// Element size of a conv_dtype_t.
+static inline int conv_esize(conv_dtype_t t) { return t == CONV_F32 ? 4 : (t == CONV_BF16 ? 2 : 1); }
+
+// Launchers (stream-ordered, no allocation, no synchronisation).
+cudaError_t launch_direct(const conv_plan *p, const void *x, const void *w, const void *bias,
+                          void *y, cudaStream_t st);
+cudaError_t launch_dw3x3(const conv_plan *p, const void *x, const void *w, const void *bias,
+                         void *y, cudaStream_t st);
+// Returns a CONV_* status (tensor-map encoding can fail on the host).
+int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *bias, void *y,
+                 cudaStream_t st);
+
+// Plan-time helpers of each family.
+bool direct_supported(const conv_plan *p);
+bool dw3x3_supported(const conv_plan *p);
+void dw3x3_configure(conv_plan *p);
+bool igemm_supported(const conv_plan *p);
+int igemm_configure(conv_plan *p);  // fills p->ig, sets kernel attributes; CONV_* status

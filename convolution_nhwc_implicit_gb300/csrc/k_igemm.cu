@@ -1,0 +1,479 @@
+// Implicit-GEMM convolution on the 5th-generation tensor cores (tcgen05),
+// bf16 operands with fp32 accumulation in TMEM, for dense k x k and 1x1
+// layers.  im2col is never materialised ("nanoinfer", "1x1 convolutions are
+// already a GEMM": the patch matrix of a 1x1 stride-1 unpadded layer is the
+// input itself; for k x k layers each tap's patch rows are fetched straight
+// from the NHWC input by TMA).
+//
+// GEMM view: M = output pixels, N = Cout, K = k_h * k_w * Cin ordered
+// (r, s, ci).  NHWC activations and OHWI weights are then both K-contiguous
+// ("nanoinfer", cuBLAS layout comparison: both operands K-contiguous is the
+// fast layout for tensor cores), so the weight tensor is, as stored, the
+// K-major B operand [Cout][K].
+//
+// Tiles.  An M tile is 128 output pixels.  For a 1x1, stride-1, unpadded
+// layer ("flat" mode) it is 128 consecutive pixels of x viewed as
+// [N*H*W, Cin].  Otherwise it is a bh x bw rectangle of output pixels of one
+// image (bh * bw <= 128; rows past bh * bw are computed from stale shared
+// memory and never stored).  For tap (r, s) and channel block cb, the A tile
+// is one 4-D TMA box of the NHWC input starting at
+// (cb * BK, ow0 * S - pad_w + s, oh0 * S - pad_h + r, n) with element strides
+// (1, S, S, 1): TMA fills out-of-image coordinates with zeros, which is the
+// zero padding, and the element strides are the convolution stride.  The B
+// tile is the [BN x BK] block of the weights at K offset (r, s, cb).
+//
+// Warp roles (192 threads, one CTA per SM, persistent over tiles):
+//   warp 0      TMA producer: fills a ring of `stages` shared-memory stages
+//   warp 1      MMA issuer: tcgen05.mma M=128 x N=BN x K=16 per instruction,
+//               accumulating a tile in one of two TMEM buffers
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one pixel row per
+//               thread), + bias, ReLU / Mish, round to bf16, 16-byte stores.
+// Two TMEM accumulators let the epilogue of tile i overlap the MMAs of tile
+// i + 1.  Every wait on an mbarrier is bounded; a wait that runs out sets the
+// plan's status word and the CTA unwinds (frees its TMEM and returns).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include <mutex>
+
+#include "conv_internal.h"
+#include "epilogue.cuh"
+#include "tc_ptx.cuh"
+
+using namespace convk;
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kBM = 128;
+
+struct IgArgs {
+    int H, W, Cin, Cout, KH, KW, stride, pad_h, pad_w, OH, OW;
+    int bw, bh, tiles_w, tiles_h, tiles_n, num_tiles, cblocks, kblocks, stages;
+    long long M;         // flat mode: rows of x viewed as [N*H*W, Cin]
+    uint32_t a_bytes;    // bytes TMA writes per A box
+    int act;
+    const float *bias;
+    __nv_bfloat16 *y;
+    int *status;
+};
+
+// Waits for phase `parity` of `bar`, giving up after kWaitBudgetNs or when
+// another role of the CTA has given up.  Returns false on give-up.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                             int *status, int code) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (tc::mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0u) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+                *abort_flag = 1;
+                atomicExch(status, code);
+                return false;
+            }
+        }
+    }
+}
+
+template <int BN, int BK, bool FLAT>
+__global__ void __launch_bounds__(kThreads, 1)
+igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const IgArgs a) {
+    constexpr uint32_t kRowBytes = BK * 2;
+    constexpr uint32_t kAStage = kBM * BK * 2;
+    constexpr uint32_t kBStage = BN * BK * 2;
+    constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators of BN fp32 columns
+    constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kBM, BN);
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = tc::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms need 1024-byte alignment
+    uint8_t *gbase = smem_raw + (base - raw);
+    const int stages = a.stages;
+    const uint32_t sA = base;
+    const uint32_t sB = base + stages * kAStage;
+    const uint32_t sBar = sB + stages * kBStage;
+    auto full_bar = [&](int s) { return sBar + 8u * s; };
+    auto empty_bar = [&](int s) { return sBar + 8u * (stages + s); };
+    auto tfull_bar = [&](int b) { return sBar + 8u * (2 * stages + b); };
+    auto tempty_bar = [&](int b) { return sBar + 8u * (2 * stages + 2 + b); };
+    uint8_t *gmisc = gbase + (sBar - base) + 8u * (2 * stages + 4);
+    volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(gmisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gmisc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            tc::mbar_init(full_bar(s), 1);
+            tc::mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(tfull_bar(b), 1);
+            tc::mbar_init(tempty_bar(b), 128);
+        }
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+        tc::tma_prefetch_desc(&tmA);
+        tc::tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tc::smem_u32((const void *)tmem_holder), kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
+                const int nb = tile % a.tiles_n;
+                const int mt = tile / a.tiles_n;
+                int n = 0, oh0 = 0, ow0 = 0;
+                int m0 = 0;
+                if (FLAT) {
+                    m0 = mt * kBM;
+                } else {
+                    const int tw = mt % a.tiles_w;
+                    const int t2 = mt / a.tiles_w;
+                    oh0 = (t2 % a.tiles_h) * a.bh;
+                    n = t2 / a.tiles_h;
+                    ow0 = tw * a.bw;
+                }
+                int r = 0, s = 0, cb = 0;
+                for (int kb = 0; kb < a.kblocks; ++kb) {
+                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, a.status,
+                                      KSTATUS_TIMEOUT_PRODUCER)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::mbar_arrive_expect_tx(full_bar(stage), a.a_bytes + kBStage);
+                    const uint32_t dA = sA + stage * kAStage;
+                    const uint32_t dB = sB + stage * kBStage;
+                    if (FLAT)
+                        tc::tma_load_2d(dA, &tmA, full_bar(stage), cb * BK, m0);
+                    else
+                        tc::tma_load_4d(dA, &tmA, full_bar(stage), cb * BK,
+                                        ow0 * a.stride - a.pad_w + s, oh0 * a.stride - a.pad_h + r, n);
+                    tc::tma_load_2d(dB, &tmB, full_bar(stage), (r * a.KW + s) * a.Cin + cb * BK, nb * BN);
+                    if (++stage == stages) { stage = 0; phase ^= 1u; }
+                    if (++cb == a.cblocks) {
+                        cb = 0;
+                        if (++s == a.KW) { s = 0; ++r; }
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int lt = 0;
+            for (int tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x, ++lt) {
+                const int buf = lt & 1;
+                const uint32_t use = (uint32_t)(lt >> 1);
+                if (!wait_bounded(tempty_bar(buf), (use & 1u) ^ 1u, abort_flag, a.status,
+                                  KSTATUS_TIMEOUT_MMA))
+                    break;
+                tc::fence_after_sync();
+                const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+                for (int kb = 0; kb < a.kblocks; ++kb) {
+                    if (!wait_bounded(full_bar(stage), phase, abort_flag, a.status, KSTATUS_TIMEOUT_MMA)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const uint32_t aS = sA + stage * kAStage;
+                    const uint32_t bS = sB + stage * kBStage;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        const uint64_t ad = tc::smem_desc_kmajor(aS + 32u * k, kRowBytes);
+                        const uint64_t bd = tc::smem_desc_kmajor(bS + 32u * k, kRowBytes);
+                        tc::mma_bf16(d, ad, bd, kIdesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    tc::mma_commit(empty_bar(stage));  // stage free once these MMAs complete
+                    if (++stage == stages) { stage = 0; phase ^= 1u; }
+                }
+                if (ok) tc::mma_commit(tfull_bar(buf));  // accumulator ready
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 2..5)
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int row = q * 32 + lane;
+        int lt = 0;
+        for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x, ++lt) {
+            const int buf = lt & 1;
+            const uint32_t use = (uint32_t)(lt >> 1);
+            const bool got = wait_bounded(tfull_bar(buf), use & 1u, abort_flag, a.status,
+                                          KSTATUS_TIMEOUT_EPILOGUE);
+            __syncwarp();  // tcgen05.ld below is warp-collective (.sync.aligned)
+            if (!__all_sync(0xffffffffu, got)) break;
+            tc::fence_after_sync();
+            const int nb = tile % a.tiles_n;
+            const int mt = tile / a.tiles_n;
+            bool valid;
+            long long pix;
+            if (FLAT) {
+                pix = (long long)mt * kBM + row;
+                valid = pix < a.M;
+            } else {
+                const int tw = mt % a.tiles_w;
+                const int t2 = mt / a.tiles_w;
+                const int th = t2 % a.tiles_h;
+                const int n = t2 / a.tiles_h;
+                const int dh = row / a.bw;
+                const int oh = th * a.bh + dh;
+                const int ow = tw * a.bw + (row - dh * a.bw);
+                valid = row < a.bw * a.bh && oh < a.OH && ow < a.OW;
+                pix = ((long long)n * a.OH + oh) * a.OW + ow;
+            }
+            __nv_bfloat16 *yrow = a.y + pix * a.Cout;
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t acc[32];
+                tc::tmem_ld_32x32(tbase + (uint32_t)c, acc);
+                tc::tmem_ld_wait();
+                const int co = nb * BN + c;
+                if (valid) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int cj = co + 8 * j;
+                        if (cj < a.Cout) {
+                            float bv[8];
+                            if (a.bias) {
+                                const float4 b0 = __ldg(reinterpret_cast<const float4 *>(a.bias + cj));
+                                const float4 b1 = __ldg(reinterpret_cast<const float4 *>(a.bias + cj) + 1);
+                                bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w;
+                                bv[4] = b1.x; bv[5] = b1.y; bv[6] = b1.z; bv[7] = b1.w;
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) bv[e] = 0.0f;
+                            }
+                            uint32_t packed[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float lo = activate(__uint_as_float(acc[8 * j + 2 * e]) + bv[2 * e], a.act);
+                                const float hi =
+                                    activate(__uint_as_float(acc[8 * j + 2 * e + 1]) + bv[2 * e + 1], a.act);
+                                __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
+                                packed[e] = *reinterpret_cast<uint32_t *>(&h2);
+                            }
+                            *reinterpret_cast<uint4 *>(yrow + cj) =
+                                make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                        }
+                    }
+                }
+            }
+            tc::fence_before_sync();
+            tc::mbar_arrive(tempty_bar(buf));
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+CUtensorMapSwizzle swizzle_for(int bk) {
+    return bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : (bk == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
+template <int BN, int BK, bool FLAT>
+void *kernel_ptr() {
+    return reinterpret_cast<void *>(&igemm_bf16_kernel<BN, BK, FLAT>);
+}
+
+template <int BN, int BK>
+void *kernel_ptr_flat(bool flat) {
+    return flat ? kernel_ptr<BN, BK, true>() : kernel_ptr<BN, BK, false>();
+}
+
+template <int BN>
+void *kernel_ptr_bk(int bk, bool flat) {
+    switch (bk) {
+    case 64: return kernel_ptr_flat<BN, 64>(flat);
+    case 32: return kernel_ptr_flat<BN, 32>(flat);
+    default: return kernel_ptr_flat<BN, 16>(flat);
+    }
+}
+
+void *select_kernel(int bn, int bk, bool flat) {
+    switch (bn) {
+    case 256: return kernel_ptr_bk<256>(bk, flat);
+    case 128: return kernel_ptr_bk<128>(bk, flat);
+    default: return kernel_ptr_bk<64>(bk, flat);
+    }
+}
+
+}  // namespace
+
+bool igemm_supported(const conv_plan *p) {
+    if (p->dtype != CONV_BF16 || p->groups != 1) return false;
+    if (p->s.c_in % 16 != 0 || p->s.c_out % 8 != 0) return false;
+    if (p->stride > 8) return false;  // TMA element strides are at most 8
+    const long long pixels_in = (long long)p->s.n * p->s.h * p->s.w;
+    if (pixels_in > 0xFFFFFFFFll) return false;  // TMA dimension limit
+    if ((long long)p->s.n * p->oh * p->ow > 0x7FFFFFFFll) return false;
+    return true;
+}
+
+int igemm_configure(conv_plan *p) {
+    IgemmGeom &g = p->ig;
+    const int S = p->stride;
+    g.in_i8 = 0;
+    g.flat = (p->s.k_h == 1 && p->s.k_w == 1 && S == 1 && p->pad_h == 0 && p->pad_w == 0) ? 1 : 0;
+    g.bk = p->s.c_in % 64 == 0 ? 64 : (p->s.c_in % 32 == 0 ? 32 : 16);
+    g.cblocks = p->s.c_in / g.bk;
+    g.kblocks = p->s.k_h * p->s.k_w * g.cblocks;
+
+    // M tiling.
+    if (g.flat) {
+        const long long M = (long long)p->s.n * p->s.h * p->s.w;
+        g.bw = kBM; g.bh = 1;
+        g.tiles_w = 1; g.tiles_h = 1;
+        g.tiles_m = (int)((M + kBM - 1) / kBM);
+    } else {
+        // Smallest number of bh x bw rectangles covering the output; among
+        // equal counts, the widest (longest contiguous NHWC runs).
+        long long best = -1;
+        for (int bw = 1; bw <= kBM && bw <= p->ow * 2; ++bw) {
+            if (bw * S > 256) break;
+            int bh = kBM / bw;
+            if (bh > p->oh) bh = p->oh;
+            while (bh * S > 256) --bh;
+            if (bh < 1) continue;
+            const long long tw = (p->ow + bw - 1) / bw, th = (p->oh + bh - 1) / bh;
+            const long long tiles = tw * th * p->s.n;
+            if (best < 0 || tiles < best || (tiles == best && bw > g.bw)) {
+                best = tiles; g.bw = bw; g.bh = bh; g.tiles_w = (int)tw; g.tiles_h = (int)th;
+            }
+            if (bw >= p->ow) break;
+        }
+        g.tiles_m = g.tiles_w * g.tiles_h * p->s.n;
+    }
+
+    // N tile: estimated time ~ waves x (BN + fixed per-tile cost).
+    long long best_cost = -1;
+    for (int bn : {256, 128, 64}) {
+        const long long tn = (p->s.c_out + bn - 1) / bn;
+        const long long tiles = tn * g.tiles_m;
+        const long long waves = (tiles + p->num_sms - 1) / p->num_sms;
+        const long long cost = waves * (bn + 48);
+        if (best_cost < 0 || cost < best_cost) { best_cost = cost; g.bn = bn; g.tiles_n = (int)tn; }
+    }
+    g.num_tiles = g.tiles_n * g.tiles_m;
+
+    const int stage_bytes = (kBM + g.bn) * g.bk * 2;
+    const int budget = 227 * 1024 - 1024 - 256;
+    g.stages = budget / stage_bytes;
+    if (g.stages > 8) g.stages = 8;
+    if (g.stages < 2) return CONV_ERR_UNSUPPORTED;
+    g.smem = 1024 + g.stages * stage_bytes + 8 * (2 * g.stages + 4) + 16;
+    // Ask for more than half of an SM's shared memory so that no two CTAs of
+    // this persistent kernel share an SM: each CTA then owns its TMEM
+    // columns (2 * BN <= 512) without waiting for another to free them.
+    if (g.smem < 116 * 1024) g.smem = 116 * 1024;
+    g.grid = g.num_tiles < p->num_sms ? g.num_tiles : p->num_sms;
+
+    if (!tensor_map_encoder()) return CONV_ERR_CUDA;
+    void *k = select_kernel(g.bn, g.bk, g.flat != 0);
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem) != cudaSuccess)
+        return CONV_ERR_CUDA;
+    snprintf(p->desc, sizeof(p->desc),
+             "igemm_bf16_tcgen05 %s BM=128 BN=%d BK=%d tile=%dx%d stages=%d tiles=%d grid=%d",
+             g.flat ? "flat" : "spatial", g.bn, g.bk, g.bh, g.bw, g.stages, g.num_tiles, g.grid);
+    return CONV_OK;
+}
+
+int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *bias, void *y,
+                 cudaStream_t st) {
+    const IgemmGeom &g = p->ig;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return CONV_ERR_CUDA;
+    const int S = p->stride;
+    alignas(64) CUtensorMap tmA, tmB;
+    const cuuint32_t ones[4] = {1, 1, 1, 1};
+    CUresult rc;
+    if (g.flat) {
+        const cuuint64_t dims[2] = {(cuuint64_t)p->s.c_in, (cuuint64_t)p->s.n * p->s.h * p->s.w};
+        const cuuint64_t strides[1] = {(cuuint64_t)p->s.c_in * 2};
+        const cuuint32_t box[2] = {(cuuint32_t)g.bk, (cuuint32_t)kBM};
+        rc = encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims, strides, box, ones,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(g.bk), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        const cuuint64_t dims[4] = {(cuuint64_t)p->s.c_in, (cuuint64_t)p->s.w, (cuuint64_t)p->s.h,
+                                    (cuuint64_t)p->s.n};
+        const cuuint64_t strides[3] = {(cuuint64_t)p->s.c_in * 2, (cuuint64_t)p->s.w * p->s.c_in * 2,
+                                       (cuuint64_t)p->s.h * p->s.w * p->s.c_in * 2};
+        const cuuint32_t box[4] = {(cuuint32_t)g.bk, (cuuint32_t)(g.bw * S), (cuuint32_t)(g.bh * S), 1};
+        const cuuint32_t estr[4] = {1, (cuuint32_t)S, (cuuint32_t)S, 1};
+        rc = encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(x), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(g.bk), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (rc != CUDA_SUCCESS) return CONV_ERR_CUDA;
+    {
+        const cuuint64_t K = (cuuint64_t)p->s.k_h * p->s.k_w * p->s.c_in;
+        const cuuint64_t dims[2] = {K, (cuuint64_t)p->s.c_out};
+        const cuuint64_t strides[1] = {K * 2};
+        const cuuint32_t box[2] = {(cuuint32_t)g.bk, (cuuint32_t)g.bn};
+        rc = encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(w), dims, strides, box, ones,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(g.bk), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (rc != CUDA_SUCCESS) return CONV_ERR_CUDA;
+    }
+
+    IgArgs a;
+    a.H = p->s.h; a.W = p->s.w; a.Cin = p->s.c_in; a.Cout = p->s.c_out; a.KH = p->s.k_h; a.KW = p->s.k_w;
+    a.stride = S; a.pad_h = p->pad_h; a.pad_w = p->pad_w; a.OH = p->oh; a.OW = p->ow;
+    a.bw = g.bw; a.bh = g.bh; a.tiles_w = g.tiles_w; a.tiles_h = g.tiles_h; a.tiles_n = g.tiles_n;
+    a.num_tiles = g.num_tiles; a.cblocks = g.cblocks; a.kblocks = g.kblocks; a.stages = g.stages;
+    a.M = (long long)p->s.n * p->s.h * p->s.w;
+    a.a_bytes = (uint32_t)((g.flat ? kBM : g.bw * g.bh) * g.bk * 2);
+    a.act = (int)p->act;
+    a.bias = (const float *)bias;
+    a.y = (__nv_bfloat16 *)y;
+    a.status = p->d_status;
+
+    void *k = select_kernel(g.bn, g.bk, g.flat != 0);
+    void *args[] = {&tmA, &tmB, &a};
+    cudaError_t e = cudaLaunchKernel(k, dim3(g.grid), dim3(kThreads), args, (size_t)g.smem, st);
+    return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+}

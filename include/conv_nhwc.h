@@ -1,0 +1,167 @@
+/*
+ * conv_nhwc.h -- C ABI of the fused NHWC 2-D convolution layer for GB300
+ * (sm_103a): y = epilogue(conv(x, w) + bias).
+ *
+ * The operation.  A 2-D cross-correlation over NHWC activations with OHWI
+ * weights, zero padding, one stride for both axes and one pad per axis
+ * applied on both sides, followed by a fused epilogue: bias, then ReLU or
+ * Mish, then (int8 layers) per-output-channel requantisation.
+ *
+ *   OH = floor((H + 2*pad_h - k_h) / stride) + 1   (likewise OW)
+ *   y[n,oh,ow,co] = act( b[co] + sum_{r<k_h, s<k_w, j<Cin/groups}
+ *                        x[n, oh*stride-pad_h+r, ow*stride-pad_w+s, g0+j]
+ *                        * w[co, r, s, j] ),    g0 = (co / (Cout/groups)) * (Cin/groups)
+ *
+ *   - layer types: dense k x k (any k_h, k_w, including asymmetric kernels
+ *     such as the 10x4 keyword-spotting stem with padding (5, 1) of the
+ *     "nanoinfer" page, section "Asymmetric padding collapsed to one axis"),
+ *     1x1 pointwise ("nanoinfer", "1x1 convolutions are already a GEMM"),
+ *     depthwise (groups == Cin == Cout) and grouped;
+ *   - Mish(v) = v * tanh(ln(1 + e^v)) ("YOLOv4, optimized for Wormhole",
+ *     section 7, the Mish / HardMish table), computed in fp32;
+ *   - int8 requantisation with symmetric scales and no zero point
+ *     ("nanoinfer", post-training quantization: symmetric per-output-channel
+ *     weight scales, calibrated activation range):
+ *       M[co] = float(double(s_x) * double(s_w[co]) / double(s_y))  (at plan time)
+ *       q = saturate_[-128,127]( round_half_even( float(acc + b[co]) * M[co] ) )
+ *     every float operation rounded to nearest-even in single precision;
+ *     ReLU, if asked for, is max(q, 0).
+ *
+ * Data types.  x, w and y share one type: CONV_F32 (fp32 arithmetic on FFMA,
+ * never TF32), CONV_BF16 (bf16 operands, fp32 accumulation, output rounded to
+ * nearest-even bf16) or CONV_I8 (int8 operands, exact int32 accumulation).
+ * The bias is float32 for CONV_F32 / CONV_BF16 and int32 for CONV_I8.
+ *
+ * Layouts (all dense, row-major, no padding between rows):
+ *   x    [N][H][W][Cin]                 (NHWC)
+ *   w    [Cout][k_h][k_w][Cin/groups]   (OHWI)
+ *   bias [Cout]                          (may be NULL: no bias)
+ *   y    [N][OH][OW][Cout]              (NHWC)
+ *
+ * Ownership.  The caller owns x, w, bias, y (device pointers) and the
+ * stream.  The plan owns its host structure and the small device buffers it
+ * allocates at creation (requantisation multipliers, a status word); they are
+ * freed by conv_plan_destroy.  conv_run never allocates and never
+ * synchronises: it enqueues kernels on the caller's stream and returns.
+ *
+ * Errors.  Every entry point returns CONV_OK (0) or a negative CONV_ERR_*
+ * code; conv_status_str names it.  Invalid shapes and unsupported
+ * combinations are rejected at plan creation, pointer problems at run time.
+ * There is no CPU fallback: a plan either runs on the GPU or fails.
+ */
+#ifndef CONV_NHWC_H
+#define CONV_NHWC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CONV_NHWC_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define CONV_API __attribute__((visibility("default")))
+#else
+#define CONV_API
+#endif
+
+typedef struct {
+    int32_t n, h, w;      /* batch, input height, input width (n may be 0) */
+    int32_t c_in, c_out;  /* input / output channels */
+    int32_t k_h, k_w;     /* kernel height, width */
+} conv_shape_t;
+
+typedef enum { CONV_F32 = 0, CONV_BF16 = 1, CONV_I8 = 2 } conv_dtype_t;
+
+typedef enum { CONV_ACT_NONE = 0, CONV_ACT_RELU = 1, CONV_ACT_MISH = 2 } conv_act_t;
+
+/* int8 quantisation parameters: activation scale s_x, output scale s_y and
+ * c_out per-output-channel weight scales s_w (a HOST array, read and copied
+ * during conv_plan_create; the caller may free it afterwards).  All > 0. */
+typedef struct {
+    float in_scale;
+    float out_scale;
+    const float *w_scales;
+} conv_quant_t;
+
+/* Kernel family a plan runs.  AUTO picks one from the shape; the others force
+ * a family (for tests), failing with CONV_ERR_UNSUPPORTED where it cannot
+ * run the layer. */
+typedef enum {
+    CONV_ALGO_AUTO = 0,
+    CONV_ALGO_DIRECT = 1,     /* CUDA-core direct convolution, any shape  */
+    CONV_ALGO_DEPTHWISE = 2,  /* depthwise 3x3 register/L1 stencil        */
+    CONV_ALGO_IGEMM = 3,      /* tcgen05 implicit GEMM (TMA, TMEM)        */
+} conv_algo_t;
+
+enum {
+    CONV_OK = 0,
+    CONV_ERR_NULL_ARG = -1,        /* a required pointer is NULL            */
+    CONV_ERR_INVALID_SHAPE = -2,   /* sizes, stride, pads or groups invalid */
+    CONV_ERR_UNSUPPORTED = -3,     /* valid but not implemented (e.g. I8+Mish) */
+    CONV_ERR_MISALIGNED = -4,      /* x, w, bias or y not 16-byte aligned   */
+    CONV_ERR_ALIASING = -5,        /* y overlaps x, w or bias               */
+    CONV_ERR_CUDA = -6,            /* a CUDA runtime/driver call failed     */
+    CONV_ERR_DEVICE_TIMEOUT = -7,  /* a kernel gave up waiting on a barrier */
+    CONV_ERR_OOM = -8,             /* host or device allocation failed      */
+    CONV_ERR_INVALID_ARG = -9,     /* bad enum value or quantisation params */
+};
+
+typedef struct conv_plan conv_plan_t; /* opaque */
+
+/* Validates the layer and builds a plan for the current CUDA device.
+ *   shape   : sizes (n >= 0; h, w, c_in, c_out, k_h, k_w >= 1)
+ *   stride  : >= 1, both axes
+ *   pad_h/w : >= 0, applied on both sides of the axis
+ *   groups  : >= 1, dividing c_in and c_out
+ *   quant   : required for CONV_I8, must be NULL otherwise
+ * CONV_I8 with CONV_ACT_MISH is CONV_ERR_UNSUPPORTED (not bit-reproducible).
+ * On success *out_plan receives the plan; on failure it is set to NULL. */
+CONV_API int conv_plan_create(const conv_shape_t *shape, int stride, int pad_h, int pad_w,
+                     int groups, conv_dtype_t dtype, conv_act_t act,
+                     const conv_quant_t *quant, conv_plan_t **out_plan);
+
+/* As conv_plan_create, forcing a kernel family (CONV_ALGO_AUTO = choose). */
+CONV_API int conv_plan_create_ex(const conv_shape_t *shape, int stride, int pad_h, int pad_w,
+                        int groups, conv_dtype_t dtype, conv_act_t act,
+                        const conv_quant_t *quant, conv_algo_t algo,
+                        conv_plan_t **out_plan);
+
+/* Enqueues the layer on `stream` (a cudaStream_t; NULL = legacy default
+ * stream).  x, w, y are device pointers, bias a device pointer or NULL; all
+ * 16-byte aligned.  y must not overlap x, w or bias.  Asynchronous: errors
+ * of the kernel itself surface through conv_plan_check_device_status. */
+CONV_API int conv_run(const conv_plan_t *plan, const void *x, const void *w, const void *bias,
+             void *y, void *stream);
+
+/* Frees the plan and its device buffers.  NULL-safe.  The caller must make
+ * sure no conv_run of this plan is still executing on the GPU. */
+CONV_API void conv_plan_destroy(conv_plan_t *plan);
+
+/* Output height and width of the plan's layer. */
+CONV_API int conv_plan_output_shape(const conv_plan_t *plan, int *oh, int *ow);
+
+/* The kernel family (conv_algo_t) the plan runs, or a negative error. */
+CONV_API int conv_plan_algo(const conv_plan_t *plan);
+
+/* A short human-readable description of the kernel and tiling chosen. */
+CONV_API const char *conv_plan_describe(const conv_plan_t *plan);
+
+/* Synchronises `stream`, reads and clears the plan's device status word.
+ * Returns CONV_OK, or CONV_ERR_DEVICE_TIMEOUT if a kernel of this plan gave
+ * up on a barrier wait since the last check, or CONV_ERR_CUDA. */
+CONV_API int conv_plan_check_device_status(conv_plan_t *plan, void *stream);
+
+/* The name of a status code ("CONV_OK", "CONV_ERR_MISALIGNED", ...). */
+CONV_API const char *conv_status_str(int status);
+
+/* CONV_NHWC_ABI_VERSION of the library. */
+CONV_API int conv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONV_NHWC_H */

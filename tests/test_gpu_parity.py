@@ -1,0 +1,246 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on
+the same seeded inputs, element by element, for every kernel family and
+dtype, at sizes spanning several tiles with ragged tails; then the five layer
+sets at full size (whole outputs where the oracle is quick, sampled outputs
+otherwise); then the boundary's run-time checks."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+from conv_workloads import CONFIGS, LayerSpec, generate, make_layer, output_hw
+from parity_util import (assert_close, make_plan, run_gpu, run_oracle, run_oracle_points,
+                         sample_points)
+
+pytestmark = pytest.mark.gpu
+
+_I8 = dict(dtype="i8", act="none", x_dist=("int", -128, 127), w_dist=("int", -127, 127),
+           b_dist=("int", -1000, 1000))
+
+
+def L(name, n, h, w, cin, cout, kh, kw, s=1, ph=0, pw=0, groups=1, dtype="bf16", act="mish", **extra):
+    base = dict(x_dist=("uniform", -1.0, 1.0), w_dist=("he",), b_dist=("normal", 0.5))
+    if dtype == "i8":
+        base = dict(x_dist=_I8["x_dist"], w_dist=_I8["w_dist"], b_dist=_I8["b_dist"])
+    base.update(extra)
+    return LayerSpec(name, n, h, w, cin, cout, kh, kw, s, ph, pw, groups, dtype, act, **base)
+
+
+def check(spec, algo="auto", expect_algo=None, seed=0):
+    g = torch.Generator("cpu").manual_seed(seed)
+    d = make_layer(spec, g)
+    y, plan = run_gpu(spec, d, algo)
+    if expect_algo:
+        assert plan.algo == expect_algo, plan.describe()
+    ref = run_oracle(spec, d)
+    assert_close(spec, y, ref, f"{spec.name} [{plan.describe()}]")
+    return plan
+
+
+# ------------------------------------------------ tcgen05 implicit GEMM (bf16)
+
+IGEMM = [
+    L("3x3_s1_ragged", 2, 19, 21, 64, 80, 3, 3, 1, 1, 1),
+    L("3x3_s2_bk32", 1, 23, 17, 32, 64, 3, 3, 2, 1, 1, act="relu"),
+    L("3x3_bk16_cout24", 1, 13, 9, 16, 24, 3, 3, 1, 1, 1, act="none"),
+    L("5x5_p2", 1, 12, 12, 64, 128, 5, 5, 1, 2, 2),
+    L("1x3_asym_pad", 1, 9, 14, 64, 64, 1, 3, 1, 0, 1),
+    L("3x3_overpad", 1, 7, 7, 64, 64, 3, 3, 1, 2, 2),
+    L("3x3_s3_p0", 1, 20, 20, 64, 64, 3, 3, 3, 0, 0),
+    L("3x3_many_kblocks", 1, 10, 10, 256, 256, 3, 3, 1, 1, 1),
+    L("3x3_wide_rows", 2, 6, 150, 64, 64, 3, 3, 1, 1, 1),
+    L("1x1_flat_ragged", 2, 15, 15, 128, 192, 1, 1),
+    L("1x1_flat_bn256", 1, 10, 10, 64, 512, 1, 1, act="relu"),
+    L("1x1_stride2", 1, 17, 17, 64, 64, 1, 1, 2, 0, 0),
+    L("1x1_cout8", 1, 9, 9, 32, 8, 1, 1, act="none"),
+    L("3x3_no_bias", 1, 11, 11, 64, 64, 3, 3, 1, 1, 1, b_dist=None),
+    L("7x7_s2_p3", 1, 30, 30, 32, 64, 7, 7, 2, 3, 3),
+    L("3x3_single_pixel", 1, 1, 1, 64, 64, 3, 3, 1, 1, 1),
+]
+
+
+@pytest.mark.parametrize("spec", IGEMM, ids=lambda s: s.name)
+def test_igemm_bf16(spec):
+    check(spec, "igemm", "igemm")
+
+
+# ------------------------------------------------ depthwise 3x3
+
+DW = []
+for dt, C in (("f32", 12), ("bf16", 24), ("i8", 48)):
+    for s, p in ((1, 1), (2, 1), (1, 0), (2, 2), (3, 1)):
+        act = "relu" if dt != "bf16" else "mish"
+        DW.append(L(f"dw_{dt}_s{s}_p{p}", 2, 13, 11, C, C, 3, 3, s, p, p, groups=C, dtype=dt, act=act))
+DW.append(L("dw_i8_relu_sat", 1, 9, 9, 32, 32, 3, 3, 1, 1, 1, groups=32, dtype="i8", act="relu",
+            b_dist=("int", -200000, 200000)))
+
+
+@pytest.mark.parametrize("spec", DW, ids=lambda s: s.name)
+def test_depthwise(spec):
+    check(spec, "depthwise", "depthwise")
+
+
+# ------------------------------------------------ direct (CUDA cores)
+
+DIRECT = [
+    L("f32_3x3", 1, 28, 28, 8, 16, 3, 3, 1, 1, 1, dtype="f32", act="relu"),
+    L("f32_stem_10x4", 1, 49, 10, 1, 64, 10, 4, 2, 5, 1, dtype="f32", act="relu"),
+    L("f32_grouped", 2, 9, 8, 8, 12, 3, 3, 1, 1, 1, groups=4, dtype="f32", act="mish"),
+    L("f32_1x1", 1, 25, 5, 64, 64, 1, 1, dtype="f32", act="relu"),
+    L("bf16_stem_cin3", 1, 33, 35, 3, 32, 3, 3, 1, 1, 1),
+    L("bf16_grouped", 1, 10, 10, 16, 32, 3, 3, 2, 1, 1, groups=2),
+    L("i8_3x3_dp4a", 1, 17, 19, 64, 40, 3, 3, 1, 1, 1, dtype="i8"),
+    L("i8_1x1", 1, 12, 12, 32, 64, 1, 1, dtype="i8", act="relu"),
+    L("i8_cin3_scalar", 1, 11, 9, 3, 16, 3, 3, 2, 1, 1, dtype="i8"),
+    L("i8_grouped", 1, 8, 8, 16, 16, 3, 3, 1, 1, 1, groups=4, dtype="i8"),
+]
+
+
+@pytest.mark.parametrize("spec", DIRECT, ids=lambda s: s.name)
+def test_direct(spec):
+    check(spec, "direct", "direct")
+
+
+def test_pointwise_paths_agree():
+    """A 1x1 layer through the tcgen05 GEMM and through the direct kernel."""
+    spec = L("pw_both", 1, 20, 20, 128, 64, 1, 1)
+    g = torch.Generator("cpu").manual_seed(5)
+    d = make_layer(spec, g)
+    y_ig, p1 = run_gpu(spec, d, "igemm")
+    y_di, p2 = run_gpu(spec, d, "direct")
+    assert p1.algo == "igemm" and p2.algo == "direct"
+    ref = run_oracle(spec, d)
+    assert_close(spec, y_ig, ref, "igemm")
+    assert_close(spec, y_di, ref, "direct")
+
+
+def test_int8_depthwise_equals_direct_bitwise():
+    spec = L("dw_i8_both", 1, 21, 19, 32, 32, 3, 3, 1, 1, 1, groups=32, dtype="i8")
+    g = torch.Generator("cpu").manual_seed(6)
+    d = make_layer(spec, g)
+    y1, _ = run_gpu(spec, d, "depthwise")
+    y2, _ = run_gpu(spec, d, "direct")
+    assert torch.equal(y1, y2)
+
+
+# ------------------------------------------------ the five layer sets, full size
+
+def _check_full(cfg, name, full=True, npoints=3000):
+    (d,) = generate(cfg, [name])
+    spec = d.spec
+    y, plan = run_gpu(spec, d)
+    if full:
+        ref = run_oracle(spec, d)
+        assert_close(spec, y, ref, f"{cfg}/{name} [{plan.describe()}]")
+    else:
+        pts = sample_points(spec, npoints, seed=zlib.crc32(name.encode()))
+        ref = run_oracle_points(spec, d, pts)
+        got = y[pts[:, 0], pts[:, 1], pts[:, 2], pts[:, 3]]
+        assert_close(spec, got, ref, f"{cfg}/{name} sampled [{plan.describe()}]")
+    return plan
+
+
+SMALL_CFGS = [(c, s.name) for c in ("mnist_conv3x3_f32", "kws_dscnn_f32", "vww_int8") for s in CONFIGS[c]]
+
+
+@pytest.mark.parametrize("cfg,name", SMALL_CFGS, ids=[n for _, n in SMALL_CFGS])
+def test_layer_sets_small_full_output(cfg, name):
+    _check_full(cfg, name, full=True)
+
+
+BIG_CFGS = [(c, s.name) for c in ("yolov4_m640_bf16", "sweep_b8_bf16") for s in CONFIGS[c]]
+
+
+@pytest.mark.parametrize("cfg,name", BIG_CFGS, ids=[n for _, n in BIG_CFGS])
+def test_layer_sets_large_sampled(cfg, name):
+    plan = _check_full(cfg, name, full=False)
+    spec = next(s for s in CONFIGS[cfg] if s.name == name)
+    if spec.groups == 1 and spec.cin % 16 == 0:
+        assert plan.algo == "igemm"
+
+
+def test_yolov4_stem_full_output():
+    _check_full("yolov4_m640_bf16", "stem3x3_3to32_640", full=True)
+
+
+def test_kws_chain_fp32():
+    """Stem -> 4 x (dw, pw), each layer fed the previous GPU output; the
+    oracle runs the same chain on its own outputs."""
+    layers = generate("kws_dscnn_f32")
+    x_gpu = layers[0].x
+    x_ref = layers[0].x.double().numpy()
+    for d in layers:
+        d.x = x_gpu
+        y, _ = run_gpu(d.spec, d)
+        import oracle
+        ref = oracle.conv_f64(x_ref, d.w.double().numpy(), d.b.double().numpy(), d.spec.stride,
+                              d.spec.pad_h, d.spec.pad_w, d.spec.groups, d.spec.act)
+        assert_close(d.spec, y, ref, f"chain {d.spec.name}")
+        x_gpu, x_ref = y, ref
+
+
+def test_vww_chain_int8_exact():
+    layers = generate("vww_int8")
+    x = layers[0].x
+    for d in layers:
+        d.x = x
+        y, _ = run_gpu(d.spec, d)
+        assert_close(d.spec, y, run_oracle(d.spec, d), f"chain {d.spec.name}")
+        x = y
+
+
+# ------------------------------------------------ boundary checks at run time
+
+def _small_plan():
+    spec = L("edge", 1, 8, 8, 64, 64, 3, 3, 1, 1, 1)
+    d = make_layer(spec, torch.Generator("cpu").manual_seed(1))
+    return spec, d, make_plan(spec, d)
+
+
+def test_empty_batch_is_a_no_op():
+    import convolution_nhwc_implicit_gb300 as cl
+    for dtype, cin in (("bf16", 64), ("f32", 8), ("i8", 32)):
+        quant = (0.05, 0.05, [0.01] * 16) if dtype == "i8" else None
+        p = cl.Plan(0, 8, 8, cin, 16, 3, 3, 1, 1, 1, 1, dtype, "relu" if dtype == "i8" else "mish", quant)
+        assert p.output_shape == (0, 8, 8, 16)
+        p.run(None, None, None, None)
+        p.check_device_status()
+
+
+def test_misaligned_aliasing_null():
+    import convolution_nhwc_implicit_gb300 as cl
+    spec, d, plan = _small_plan()
+    dev = torch.device("cuda:0")
+    x, w, b = d.x.to(dev), d.w.to(dev), d.b.to(dev)
+    y = torch.empty(plan.output_shape, dtype=torch.bfloat16, device=dev)
+    big = torch.empty(x.numel() + 8, dtype=torch.bfloat16, device=dev)
+    xm = big[1:1 + x.numel()].view_as(x)  # 2-byte offset
+    with pytest.raises(cl.ConvError) as e:
+        plan.run(xm, w, b, y)
+    assert e.value.code == -4
+    with pytest.raises(cl.ConvError) as e:
+        plan.run(x, w, b, x)  # y aliases x
+    assert e.value.code == -5
+    with pytest.raises(cl.ConvError) as e:
+        plan.run(None, w, b, y)
+    assert e.value.code == -1
+    plan.run(x, w, b, y)
+    plan.check_device_status()
+
+
+def test_bias_optional_everywhere():
+    for algo, spec in (("igemm", L("nb_ig", 1, 9, 9, 64, 64, 3, 3, 1, 1, 1, b_dist=None)),
+                       ("depthwise", L("nb_dw", 1, 9, 9, 64, 64, 3, 3, 1, 1, 1, groups=64, b_dist=None)),
+                       ("direct", L("nb_di", 1, 9, 9, 8, 8, 3, 3, 1, 1, 1, dtype="f32", b_dist=None))):
+        check(spec, algo, algo)
+
+
+def test_repeated_runs_are_deterministic():
+    spec = L("det", 2, 16, 16, 64, 128, 3, 3, 1, 1, 1)
+    g = torch.Generator("cpu").manual_seed(9)
+    d = make_layer(spec, g)
+    plan = make_plan(spec, d)
+    y1, _ = run_gpu(spec, d, plan=plan)
+    y2, _ = run_gpu(spec, d, plan=plan)
+    assert torch.equal(y1, y2)
