@@ -70,7 +70,7 @@ def layer_bound(spec, peaks):
 class ClockSampler:
     """Samples nvidia-smi clocks / throttle reasons every 200 ms while running."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -84,7 +84,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -94,7 +94,10 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
 
     def stop(self):
         if not self.proc:
@@ -108,7 +111,14 @@ class ClockSampler:
             self.t.join(timeout=2)
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        # samples that arrived inside the timed region (+ one sampling period)
+        t0, t1 = getattr(self, "t_start", 0.0), getattr(self, "t_end", 1e30) + 0.06
+        inside = [ln for ts, ln in self.lines if t0 <= ts <= t1]
+        where = "timed region"
+        if not inside and self.lines:
+            inside = [ln for _, ln in self.lines]
+            where = "whole run (timed region shorter than the sampling period)"
+        for ln in inside:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -123,7 +133,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window": where}
 
 
 # ---------------------------------------------------------------- our arm
@@ -162,6 +172,8 @@ def run_ours(args, rank, world, device):
         if ev is not None:
             ev[nl].record(stream)
 
+    clocks = ClockSampler(device)
+    clocks.start()
     for _ in range(args.warmup):
         flush.fill_(1)
         step()
@@ -171,14 +183,14 @@ def run_ours(args, rank, world, device):
     torch.cuda.synchronize()
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(args.steps)]
-    clocks = ClockSampler(device)
-    clocks.start()
+    clocks.mark("t_start")
     t0 = time.perf_counter()
     for k in range(args.steps):
         flush.fill_(k & 0xFF)
         step(events[k])
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
+    clocks.mark("t_end")
     clk = clocks.stop()
     for p in plans:
         p.check_device_status()
@@ -379,7 +391,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)

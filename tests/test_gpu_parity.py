@@ -19,7 +19,9 @@ _I8 = dict(dtype="i8", act="none", x_dist=("int", -128, 127), w_dist=("int", -12
            b_dist=("int", -1000, 1000))
 
 
-def L(name, n, h, w, cin, cout, kh, kw, s=1, ph=0, pw=0, groups=1, dtype="bf16", act="mish", **extra):
+def L(name, n, h, w, cin, cout, kh, kw, s=1, ph=0, pw=0, groups=1, dtype="bf16", act=None, **extra):
+    if act is None:
+        act = "none" if dtype == "i8" else "mish"
     base = dict(x_dist=("uniform", -1.0, 1.0), w_dist=("he",), b_dist=("normal", 0.5))
     if dtype == "i8":
         base = dict(x_dist=_I8["x_dist"], w_dist=_I8["w_dist"], b_dist=_I8["b_dist"])
