@@ -18,7 +18,11 @@ import ctypes
 import os
 
 __all__ = ["Plan", "ConvError", "conv2d_nhwc", "library_path", "load_library", "DTYPES", "ACTS",
-           "ALGOS", "status_str", "abi_version"]
+           "ALGOS", "status_str", "abi_version", "run_i8_noalloc", "NOALLOC_MAX_COUT"]
+
+# Largest c_out conv_run_i8_noalloc accepts (its fixed scratch array holds
+# that many requantisation multipliers).
+NOALLOC_MAX_COUT = 4096
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libconv_nhwc.so")
@@ -84,6 +88,10 @@ def load_library():
     lib.conv_status_str.restype = ctypes.c_char_p
     lib.conv_abi_version.argtypes = []
     lib.conv_abi_version.restype = c_int
+    lib.conv_run_i8_noalloc.argtypes = [ctypes.POINTER(_Shape), c_int, c_int, c_int, c_int, c_int,
+                                        ctypes.POINTER(_Quant), c_void_p, c_void_p, c_void_p, c_void_p,
+                                        c_void_p]
+    lib.conv_run_i8_noalloc.restype = c_int
     _lib = lib
     return lib
 
@@ -196,3 +204,24 @@ def conv2d_nhwc(x, w, b=None, stride=1, pad=(0, 0), groups=1, act="none", quant=
         out = torch.empty(plan.output_shape, dtype=x.dtype, device=x.device)
     plan.run(x, w, b, out)
     return out
+
+
+def run_i8_noalloc(x, w, b, y, stride=1, pad=(0, 0), groups=1, act="none", quant=None, stream=None):
+    """An int8 layer through conv_run_i8_noalloc: no plan and no device
+    allocation, for callers that must not allocate device memory at run time
+    (their buffers come from a pre-reserved pool).  The library keeps the
+    requantisation table in one fixed device array shared by all calls, so
+    calls that may overlap on the GPU must be serialised.  x NHWC, w OHWI,
+    b int32 [Cout] or None, y preallocated NHWC int8; quant = (s_x, s_y, s_w)."""
+    lib = load_library()
+    n, h, wd, c_in = x.shape
+    c_out, k_h, k_w, _ = w.shape
+    in_scale, out_scale, w_scales = quant
+    ws = (ctypes.c_float * c_out)(*[float(v) for v in w_scales])
+    q = _Quant(float(in_scale), float(out_scale), ctypes.cast(ws, ctypes.POINTER(ctypes.c_float)))
+    shape = _Shape(n, h, wd, c_in, c_out, k_h, k_w)
+    rc = lib.conv_run_i8_noalloc(ctypes.byref(shape), stride, pad[0], pad[1], groups, ACTS[act],
+                                 ctypes.byref(q), _ptr(x), _ptr(w), _ptr(b), _ptr(y), _stream_handle(stream))
+    if rc != 0:
+        raise ConvError("conv_run_i8_noalloc", rc)
+    return y

@@ -77,6 +77,25 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 }  // namespace
 
+// Shared with the other entry points of the library (conv_internal.h).
+int conv_validate_layer(const conv_shape_t *s, int stride, int pad_h, int pad_w, int groups,
+                        conv_dtype_t dtype, conv_act_t act, const conv_quant_t *quant, int *oh, int *ow) {
+    return validate(s, stride, pad_h, pad_w, groups, dtype, act, quant, oh, ow);
+}
+
+int conv_check_run_pointers(conv_dtype_t dtype, const conv_shape_t *s, int groups, int oh, int ow,
+                            const void *x, const void *w, const void *bias, const void *y) {
+    if (!x || !w || !y) return CONV_ERR_NULL_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias))) return CONV_ERR_MISALIGNED;
+    const size_t es = (size_t)conv_esize(dtype);
+    const size_t xb = (size_t)s->n * s->h * s->w * s->c_in * es;
+    const size_t wb = (size_t)s->c_out * s->k_h * s->k_w * (s->c_in / groups) * es;
+    const size_t bb = bias ? (size_t)s->c_out * 4 : 0;
+    const size_t yb = (size_t)s->n * oh * ow * s->c_out * es;
+    if (overlaps(y, yb, x, xb) || overlaps(y, yb, w, wb) || overlaps(y, yb, bias, bb)) return CONV_ERR_ALIASING;
+    return CONV_OK;
+}
+
 extern "C" {
 
 int conv_abi_version(void) { return CONV_NHWC_ABI_VERSION; }
@@ -93,6 +112,7 @@ const char *conv_status_str(int status) {
     case CONV_ERR_DEVICE_TIMEOUT: return "CONV_ERR_DEVICE_TIMEOUT";
     case CONV_ERR_OOM: return "CONV_ERR_OOM";
     case CONV_ERR_INVALID_ARG: return "CONV_ERR_INVALID_ARG";
+    case CONV_ERR_SCRATCH_LIMIT: return "CONV_ERR_SCRATCH_LIMIT";
     default: return "CONV_ERR_UNKNOWN";
     }
 }

@@ -74,3 +74,9 @@ bool dw3x3_supported(const conv_plan *p);
 void dw3x3_configure(conv_plan *p);
 bool igemm_supported(const conv_plan *p);
 int igemm_configure(conv_plan *p);  // fills p->ig, sets kernel attributes; CONV_* status
+
+// Host-side argument checks shared by the entry points (api.cu).
+int conv_validate_layer(const conv_shape_t *s, int stride, int pad_h, int pad_w, int groups,
+                        conv_dtype_t dtype, conv_act_t act, const conv_quant_t *quant, int *oh, int *ow);
+int conv_check_run_pointers(conv_dtype_t dtype, const conv_shape_t *s, int groups, int oh, int ow,
+                            const void *x, const void *w, const void *bias, const void *y);

@@ -107,6 +107,7 @@ enum {
     CONV_ERR_DEVICE_TIMEOUT = -7,  /* a kernel gave up waiting on a barrier */
     CONV_ERR_OOM = -8,             /* host or device allocation failed      */
     CONV_ERR_INVALID_ARG = -9,     /* bad enum value or quantisation params */
+    CONV_ERR_SCRATCH_LIMIT = -10,  /* layer needs more than a fixed scratch area holds */
 };
 
 typedef struct conv_plan conv_plan_t; /* opaque */
@@ -159,6 +160,42 @@ CONV_API const char *conv_status_str(int status);
 
 /* CONV_NHWC_ABI_VERSION of the library. */
 CONV_API int conv_abi_version(void);
+
+/* ---------------------------------------------------------------------------
+ * An int8 layer run that allocates nothing.  (The pages describe no such
+ * entry point; it exists for callers of this library, not for the method.)
+ *
+ * Who needs it: code that may not call cudaMalloc at run time -- an engine
+ * that reserves all device memory up front in its own arena, a process
+ * working under a fixed memory budget, or a caller holding a lock in which an
+ * allocation could block or fail.  conv_plan_create allocates the int8
+ * requantisation table on the device; this entry point does not.
+ *
+ * What it computes: exactly what conv_plan_create(..., CONV_I8, act, quant)
+ * followed by conv_run computes (same validation, same bit-exact results),
+ * on the CUDA-core direct kernel.  x, w, bias, y and `stream` are as for
+ * conv_run.  quant->w_scales is a HOST array of shape->c_out floats.
+ *
+ * Scratch: the per-channel multipliers M[co] are written into one fixed
+ * device array inside the library, CONV_NOALLOC_MAX_COUT floats (16 KiB),
+ * which every GPU that loads the library holds until the process exits.
+ * Layers with c_out > CONV_NOALLOC_MAX_COUT return CONV_ERR_SCRATCH_LIMIT.
+ * Every call rewrites the whole part of the array it uses, before its kernel
+ * reads it, in stream order.  All calls share that one array, so two calls
+ * that can overlap on the GPU (different streams, or different host
+ * threads) race and may read each other's multipliers: serialise them.
+ *
+ * Set-up: the first call on a device looks up the array's device address on
+ * that device (cudaGetSymbolAddress, with that device current) and caches it;
+ * make that first call before any stream capture begins.
+ *
+ * Returns CONV_OK or a CONV_ERR_* code, like conv_plan_create and conv_run
+ * together.  Asynchronous: returns once the work is enqueued. */
+#define CONV_NOALLOC_MAX_COUT 4096
+CONV_API int conv_run_i8_noalloc(const conv_shape_t *shape, int stride, int pad_h, int pad_w,
+                                 int groups, conv_act_t act, const conv_quant_t *quant,
+                                 const void *x, const void *w, const void *bias, void *y,
+                                 void *stream);
 
 #ifdef __cplusplus
 }
