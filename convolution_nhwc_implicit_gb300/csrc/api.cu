@@ -96,6 +96,19 @@ int conv_check_run_pointers(conv_dtype_t dtype, const conv_shape_t *s, int group
     return CONV_OK;
 }
 
+int conv_grant_smem(const void *k, int device, int need) {
+    int optin = 0;
+    cudaFuncAttributes fa;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa, k) != cudaSuccess)
+        return CONV_ERR_CUDA;
+    const int avail = optin - (int)fa.sharedSizeBytes;
+    if (need > avail) return CONV_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, avail) != cudaSuccess)
+        return CONV_ERR_CUDA;
+    return CONV_OK;
+}
+
 extern "C" {
 
 int conv_abi_version(void) { return CONV_NHWC_ABI_VERSION; }
@@ -190,9 +203,11 @@ int conv_plan_create_ex(const conv_shape_t *shape, int stride, int pad_h, int pa
         rc = igemm_configure(p);
         if (rc != CONV_OK) { conv_plan_destroy(p); return rc; }
     } else if (chosen == CONV_ALGO_DEPTHWISE) {
-        dw3x3_configure(p);
-        snprintf(p->desc, sizeof(p->desc), "dw3x3 %s rows/thread=%d threads=%lld",
-                 dtype == CONV_F32 ? "f32" : (dtype == CONV_BF16 ? "bf16" : "i8"), p->dw.th, p->dw.items);
+        rc = dw3x3_configure(p);
+        if (rc != CONV_OK) { conv_plan_destroy(p); return rc; }
+        snprintf(p->desc, sizeof(p->desc), "dw3x3 %s tile=%dx%dx%dch halo=%dx%d threads=%d blocks=%lld",
+                 dtype == CONV_F32 ? "f32" : (dtype == CONV_BF16 ? "bf16" : "i8"), p->dw.th, p->dw.tw,
+                 p->dw.cbv * 16 / conv_esize(dtype), p->dw.hin, p->dw.win, p->dw.threads, p->dw.blocks);
     } else {
         snprintf(p->desc, sizeof(p->desc), "direct %s",
                  dtype == CONV_F32 ? "f32-ffma" : (dtype == CONV_BF16 ? "bf16-ffma" : "i8-dp4a"));

@@ -35,9 +35,13 @@ struct IgemmGeom {
 };
 
 struct DwGeom {
-    int th;        // output rows per thread (register sliding window)
-    int nstrips;   // ceil(OH / th)
-    long long items;
+    int th, tw;    // output rows / columns of one CTA tile
+    int cbv;       // 16-byte channel vectors per tile
+    int hin, win;  // input halo rows / columns (one TMA box)
+    int tiles_w, tiles_h, tiles_c;
+    int smem;      // dynamic shared memory bytes (the halo)
+    int threads;   // threads per CTA
+    long long blocks;
 };
 
 struct conv_plan {
@@ -71,7 +75,7 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
 // Plan-time helpers of each family.
 bool direct_supported(const conv_plan *p);
 bool dw3x3_supported(const conv_plan *p);
-void dw3x3_configure(conv_plan *p);
+int dw3x3_configure(conv_plan *p);  // CONV_* status
 bool igemm_supported(const conv_plan *p);
 int igemm_configure(conv_plan *p);  // fills p->ig, sets kernel attributes; CONV_* status
 
@@ -80,3 +84,9 @@ int conv_validate_layer(const conv_shape_t *s, int stride, int pad_h, int pad_w,
                         conv_dtype_t dtype, conv_act_t act, const conv_quant_t *quant, int *oh, int *ow);
 int conv_check_run_pointers(conv_dtype_t dtype, const conv_shape_t *s, int groups, int oh, int ow,
                             const void *x, const void *w, const void *bias, const void *y);
+
+// Grants kernel `k` the device's whole opt-in dynamic shared memory (minus its
+// static shared memory) and checks that `need` bytes fit.  The attribute is a
+// per-kernel permission shared by all plans, so it is never lowered to one
+// plan's size.  Returns a CONV_* status.
+int conv_grant_smem(const void *k, int device, int need);

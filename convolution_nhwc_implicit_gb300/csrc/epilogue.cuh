@@ -24,6 +24,23 @@ __device__ __forceinline__ float mish_f32(float v) {
     return v * (t / (t + 2.0f));
 }
 
+// The same Mish with the hardware exp2 and reciprocal approximations
+// (__expf, __fdividef): relative error ~1e-6, far below the bf16 rounding
+// (2^-9) of the outputs it feeds.  t + 2 stays below 2^126 because v <= 20.
+__device__ __forceinline__ float mish_fast(float v) {
+    if (v > 20.0f) return v;
+    const float n = __expf(v);
+    const float t = n * (n + 2.0f);
+    return v * __fdividef(t, t + 2.0f);
+}
+
+// Activation for bf16 outputs.
+__device__ __forceinline__ float activate_fast(float v, int act) {
+    if (act == ACT_RELU) return fmaxf(v, 0.0f);
+    if (act == ACT_MISH) return mish_fast(v);
+    return v;
+}
+
 __device__ __forceinline__ float activate(float v, int act) {
     if (act == ACT_RELU) return fmaxf(v, 0.0f);
     if (act == ACT_MISH) return mish_f32(v);

@@ -22,14 +22,16 @@
 // zero padding, and the element strides are the convolution stride.  The B
 // tile is the [BN x BK] block of the weights at K offset (r, s, cb).
 //
-// Warp roles (192 threads, one CTA per SM, persistent over tiles):
+// Warp roles (320 or 576 threads, one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer: fills a ring of `stages` shared-memory stages
 //   warp 1      MMA issuer: tcgen05.mma M=128 x N=BN x K=16 per instruction,
 //               accumulating a tile in one of two TMEM buffers
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one pixel row per
-//               thread), + bias, ReLU / Mish, round to bf16, 16-byte stores.
+//   warps 2..    epilogue: 2 or 4 warpgroups, each draining a slice of the
+//               tile's columns (tcgen05.ld, one pixel row per thread), then
+//               + bias, ReLU / Mish, round to bf16, 16-byte stores.
 // Two TMEM accumulators let the epilogue of tile i overlap the MMAs of tile
-// i + 1.  Every wait on an mbarrier is bounded; a wait that runs out sets the
+// i + 1; an epilogue thread returns its TMEM slice as soon as the values are
+// in registers.  Every wait on an mbarrier is bounded; a wait that runs out sets the
 // plan's status word and the CTA unwinds (frees its TMEM and returns).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -47,8 +49,12 @@ using namespace convk;
 
 namespace {
 
-constexpr int kThreads = 192;
 constexpr int kBM = 128;
+
+// Epilogue warpgroups per CTA: each takes BN / groups columns of every tile.
+__host__ __device__ constexpr int epi_groups(int bn) { return bn >= 128 ? 4 : 2; }
+// Threads per CTA: the TMA warp, the MMA warp and the epilogue warpgroups.
+__host__ __device__ constexpr int cta_threads(int bn) { return 64 + 128 * epi_groups(bn); }
 
 struct IgArgs {
     int H, W, Cin, Cout, KH, KW, stride, pad_h, pad_w, OH, OW;
@@ -81,7 +87,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
 }
 
 template <int BN, int BK, bool FLAT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(cta_threads(BN), 1)
 igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const IgArgs a) {
     constexpr uint32_t kRowBytes = BK * 2;
@@ -89,6 +95,9 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     constexpr uint32_t kBStage = BN * BK * 2;
     constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators of BN fp32 columns
     constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kBM, BN);
+    constexpr int kGroups = epi_groups(BN);
+    constexpr int kCols = BN / kGroups;  // accumulator columns per epilogue thread (32 or 64)
+    static_assert(kCols % 32 == 0, "epilogue reads TMEM 32 columns at a time");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
@@ -116,7 +125,7 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(tfull_bar(b), 1);
-            tc::mbar_init(tempty_bar(b), 128);
+            tc::mbar_init(tempty_bar(b), 128 * kGroups);
         }
         *abort_flag = 0;
         tc::fence_mbar_init();
@@ -212,9 +221,14 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             }
         }
     } else {
-        // ------------------------------------------------ epilogue (warps 2..5)
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        // ------------------------------------------------ epilogue (warps 2 ..)
+        // tcgen05.ld lets warp w reach TMEM lanes 32 * (w % 4) .. + 31, so every
+        // run of four consecutive warps covers the 128 accumulator rows; warp
+        // group g (warps 2 + 4g .. 5 + 4g) drains columns [g * kCols, (g+1) * kCols).
+        const int q = warp & 3;
+        const int grp = (warp - 2) >> 2;
         const int row = q * 32 + lane;
+        const int c_base = grp * kCols;
         int lt = 0;
         for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x, ++lt) {
             const int buf = lt & 1;
@@ -224,6 +238,17 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             __syncwarp();  // tcgen05.ld below is warp-collective (.sync.aligned)
             if (!__all_sync(0xffffffffu, got)) break;
             tc::fence_after_sync();
+            // Move this thread's slice of the accumulator into registers, then
+            // hand the TMEM buffer back to the MMA warp before doing the math.
+            uint32_t acc[kCols];
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c_base);
+#pragma unroll
+            for (int c = 0; c < kCols; c += 32)
+                tc::tmem_ld_32x32(tbase + (uint32_t)c, *reinterpret_cast<uint32_t(*)[32]>(acc + c));
+            tc::tmem_ld_wait();
+            tc::fence_before_sync();
+            tc::mbar_arrive(tempty_bar(buf));
+
             const int nb = tile % a.tiles_n;
             const int mt = tile / a.tiles_n;
             bool valid;
@@ -242,46 +267,31 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 valid = row < a.bw * a.bh && oh < a.OH && ow < a.OW;
                 pix = ((long long)n * a.OH + oh) * a.OW + ow;
             }
+            if (!valid) continue;
             __nv_bfloat16 *yrow = a.y + pix * a.Cout;
-            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
-#pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
-                uint32_t acc[32];
-                tc::tmem_ld_32x32(tbase + (uint32_t)c, acc);
-                tc::tmem_ld_wait();
-                const int co = nb * BN + c;
-                if (valid) {
+            const int co0 = nb * BN + c_base;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int cj = co + 8 * j;
-                        if (cj < a.Cout) {
-                            float bv[8];
-                            if (a.bias) {
-                                const float4 b0 = __ldg(reinterpret_cast<const float4 *>(a.bias + cj));
-                                const float4 b1 = __ldg(reinterpret_cast<const float4 *>(a.bias + cj) + 1);
-                                bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w;
-                                bv[4] = b1.x; bv[5] = b1.y; bv[6] = b1.z; bv[7] = b1.w;
-                            } else {
+            for (int j = 0; j < kCols / 8; ++j) {
+                const int cj = co0 + 8 * j;
+                if (cj >= a.Cout) break;
+                float v[8];
 #pragma unroll
-                                for (int e = 0; e < 8; ++e) bv[e] = 0.0f;
-                            }
-                            uint32_t packed[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float lo = activate(__uint_as_float(acc[8 * j + 2 * e]) + bv[2 * e], a.act);
-                                const float hi =
-                                    activate(__uint_as_float(acc[8 * j + 2 * e + 1]) + bv[2 * e + 1], a.act);
-                                __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
-                                packed[e] = *reinterpret_cast<uint32_t *>(&h2);
-                            }
-                            *reinterpret_cast<uint4 *>(yrow + cj) =
-                                make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                        }
-                    }
+                for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(acc[8 * j + e]);
+                if (a.bias) {
+                    const float4 b0 = __ldg(reinterpret_cast<const float4 *>(a.bias + cj));
+                    const float4 b1 = __ldg(reinterpret_cast<const float4 *>(a.bias + cj) + 1);
+                    v[0] += b0.x; v[1] += b0.y; v[2] += b0.z; v[3] += b0.w;
+                    v[4] += b1.x; v[5] += b1.y; v[6] += b1.z; v[7] += b1.w;
                 }
+                uint32_t packed[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    __nv_bfloat162 h2 = __floats2bfloat162_rn(activate_fast(v[2 * e], a.act),
+                                                              activate_fast(v[2 * e + 1], a.act));
+                    packed[e] = *reinterpret_cast<uint32_t *>(&h2);
+                }
+                *reinterpret_cast<uint4 *>(yrow + cj) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
             }
-            tc::fence_before_sync();
-            tc::mbar_arrive(tempty_bar(buf));
         }
     }
 
@@ -412,9 +422,8 @@ int igemm_configure(conv_plan *p) {
     g.grid = g.num_tiles < p->num_sms ? g.num_tiles : p->num_sms;
 
     if (!tensor_map_encoder()) return CONV_ERR_CUDA;
-    void *k = select_kernel(g.bn, g.bk, g.flat != 0);
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem) != cudaSuccess)
-        return CONV_ERR_CUDA;
+    const int rc = conv_grant_smem(select_kernel(g.bn, g.bk, g.flat != 0), p->device, g.smem);
+    if (rc != CONV_OK) return rc;
     snprintf(p->desc, sizeof(p->desc),
              "igemm_bf16_tcgen05 %s BM=128 BN=%d BK=%d tile=%dx%d stages=%d tiles=%d grid=%d",
              g.flat ? "flat" : "spatial", g.bn, g.bk, g.bh, g.bw, g.stages, g.num_tiles, g.grid);
@@ -474,6 +483,6 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
 
     void *k = select_kernel(g.bn, g.bk, g.flat != 0);
     void *args[] = {&tmA, &tmB, &a};
-    cudaError_t e = cudaLaunchKernel(k, dim3(g.grid), dim3(kThreads), args, (size_t)g.smem, st);
+    cudaError_t e = cudaLaunchKernel(k, dim3(g.grid), dim3(cta_threads(g.bn)), args, (size_t)g.smem, st);
     return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
