@@ -50,202 +50,242 @@ struct DwArgs {
 };
 
 template <typename T> struct DwT;
+// fp32: a thread owns 4 channels (one 16-byte vector).
 template <> struct DwT<float> {
     static constexpr int V = 4;
+    using Vec = uint4;
     static constexpr CUtensorMapDataType tma = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    __device__ static __forceinline__ void to_f(const Vec &u, float (&o)[4]) {
+        o[0] = __uint_as_float(u.x); o[1] = __uint_as_float(u.y);
+        o[2] = __uint_as_float(u.z); o[3] = __uint_as_float(u.w);
+    }
 };
+// bf16: a thread owns 4 channels (one 8-byte vector); widening a bf16 to
+// fp32 is a 16-bit shift of its bits, exact.
 template <> struct DwT<__nv_bfloat16> {
-    static constexpr int V = 8;
+    static constexpr int V = 4;
+    using Vec = uint2;
     static constexpr CUtensorMapDataType tma = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    __device__ static __forceinline__ void to_f(const Vec &u, float (&o)[4]) {
+        o[0] = __uint_as_float(u.x << 16); o[1] = __uint_as_float(u.x & 0xffff0000u);
+        o[2] = __uint_as_float(u.y << 16); o[3] = __uint_as_float(u.y & 0xffff0000u);
+    }
 };
+// int8: a thread owns 16 channels (one 16-byte vector), kept packed.
 template <> struct DwT<int8_t> {
     static constexpr int V = 16;
+    using Vec = uint4;
     static constexpr CUtensorMapDataType tma = CU_TENSOR_MAP_DATA_TYPE_UINT8;
 };
-
-// acc += x * w for one 16-byte input vector and the matching 16 bytes of one
-// tap's weights (V channels).
-__device__ __forceinline__ void fma_vec(float (&acc)[4], const uint4 &x, const float (&w)[4]) {
-    acc[0] = __fmaf_rn(__uint_as_float(x.x), w[0], acc[0]);
-    acc[1] = __fmaf_rn(__uint_as_float(x.y), w[1], acc[1]);
-    acc[2] = __fmaf_rn(__uint_as_float(x.z), w[2], acc[2]);
-    acc[3] = __fmaf_rn(__uint_as_float(x.w), w[3], acc[3]);
-}
-
-// bf16: both operands are bf16 halves of 32-bit words; fp32 accumulation.
-__device__ __forceinline__ float fma_bf16(uint32_t xw, int xh, uint32_t ww, int wh, float c) {
-    float d;
-    if (xh == 0 && wh == 0)
-        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
-            "fma.rn.f32.bf16 %0, a0, b0, %3;\n\t}" : "=f"(d) : "r"(xw), "r"(ww), "f"(c));
-    else if (xh == 0 && wh == 1)
-        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
-            "fma.rn.f32.bf16 %0, a0, b1, %3;\n\t}" : "=f"(d) : "r"(xw), "r"(ww), "f"(c));
-    else if (xh == 1 && wh == 0)
-        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
-            "fma.rn.f32.bf16 %0, a1, b0, %3;\n\t}" : "=f"(d) : "r"(xw), "r"(ww), "f"(c));
-    else
-        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
-            "fma.rn.f32.bf16 %0, a1, b1, %3;\n\t}" : "=f"(d) : "r"(xw), "r"(ww), "f"(c));
-    return d;
-}
 
 __device__ __forceinline__ uint32_t word(const uint4 &u, int i) {
     return i == 0 ? u.x : (i == 1 ? u.y : (i == 2 ? u.z : u.w));
 }
 
-template <typename T, int S>
-__global__ void __launch_bounds__(256, 2)
-dw3x3_kernel(const __grid_constant__ CUtensorMap tmX, const T *__restrict__ w, const DwArgs a) {
-    constexpr int V = DwT<T>::V;
-    extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(8) uint64_t bar;
-    const int stride = S ? S : a.stride;
+// Bounded wait for the halo; false if it ran out (status word set).
+__device__ __forceinline__ bool wait_halo(uint32_t sbar, int *status) {
+    if (tc::mbar_try_wait(sbar, 0)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (tc::mbar_try_wait(sbar, 0)) return true;
+        if ((i & 63u) == 0u && globaltimer_ns() - t0 > kWaitBudgetNs) {
+            if (threadIdx.x == 0) atomicExch(status, KSTATUS_TIMEOUT_EPILOGUE);
+            return false;
+        }
+    }
+}
 
-    // tile coordinates: channel block fastest, then columns, rows, image
-    int t = blockIdx.x;
-    const int tc_ = t % a.tiles_c; t /= a.tiles_c;
-    const int tw_ = t % a.tiles_w; t /= a.tiles_w;
-    const int th_ = t % a.tiles_h;
-    const int n = t / a.tiles_h;
-    const int oh0 = th_ * a.th, ow0 = tw_ * a.tw;
-    const int cv = threadIdx.x % a.cbv;
-    const int col = threadIdx.x / a.cbv;
-    const int c0 = (tc_ * a.cbv + cv) * V;  // first channel of this thread's vector
-    const int cbytes = a.cbv * 16;           // bytes of one halo pixel
+// Issues the halo TMA (thread 0); returns the tile's coordinates.
+struct DwTile {
+    int n, oh0, ow0, cv, col, c0;
+};
 
-    const uint32_t sbar = tc::smem_u32(&bar);
+template <int V>
+__device__ __forceinline__ DwTile dw_tile_start(const CUtensorMap *tmX, const DwArgs &a, uint8_t *smem,
+                                                uint32_t sbar, int stride, int vbytes) {
+    DwTile t;
+    int b = blockIdx.x;
+    const int tc_ = b % a.tiles_c; b /= a.tiles_c;
+    const int tw_ = b % a.tiles_w; b /= a.tiles_w;
+    const int th_ = b % a.tiles_h;
+    t.n = b / a.tiles_h;
+    t.oh0 = th_ * a.th;
+    t.ow0 = tw_ * a.tw;
+    t.cv = threadIdx.x % a.cbv;
+    t.col = threadIdx.x / a.cbv;
+    t.c0 = (tc_ * a.cbv + t.cv) * V;
     if (threadIdx.x == 0) {
         tc::mbar_init(sbar, 1);
         tc::fence_mbar_init();
-        tc::mbar_arrive_expect_tx(sbar, (uint32_t)(a.hin * a.win * cbytes));
-        tc::tma_load_4d(tc::smem_u32(smem), &tmX, sbar, tc_ * a.cbv * V, ow0 * stride - a.pad_w,
-                        oh0 * stride - a.pad_h, n);
+        tc::mbar_arrive_expect_tx(sbar, (uint32_t)(a.hin * a.win * a.cbv * vbytes));
+        tc::tma_load_4d(tc::smem_u32(smem), tmX, sbar, tc_ * a.cbv * V, t.ow0 * stride - a.pad_w,
+                        t.oh0 * stride - a.pad_h, t.n);
     }
+    return t;
+}
 
-    // Weights and bias while the halo is in flight.
-    const bool active = col < a.tw && c0 < a.C;
-    uint4 wv[9];
+// fp32 and bf16: fp32 window and weights in registers, FFMA.
+template <typename T, int S>
+__global__ void __launch_bounds__(256, 2)
+dw3x3_float_kernel(const __grid_constant__ CUtensorMap tmX, const T *__restrict__ w, const DwArgs a) {
+    using Tr = DwT<T>;
+    using Vec = typename Tr::Vec;
+    constexpr int VB = sizeof(Vec);
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t bar;
+    const int stride = S ? S : a.stride;
+    const uint32_t sbar = tc::smem_u32(&bar);
+    const DwTile t = dw_tile_start<4>(&tmX, a, smem, sbar, stride, VB);
+
+    // Weights (OHWI [C][3][3]: a channel's nine taps are contiguous, so the
+    // thread's 4 x 9 weights are nine vectors) and bias, while the halo flies.
+    const bool active = t.col < a.tw && t.c0 < a.C;
+    float wt[9][4];
+    float bv[4] = {0.f, 0.f, 0.f, 0.f};
     if (active) {
-        const uint4 *wp = reinterpret_cast<const uint4 *>(w + (long long)c0 * 9);
+        const Vec *wp = reinterpret_cast<const Vec *>(w + (long long)t.c0 * 9);
+        float raw[36];
 #pragma unroll
-        for (int k = 0; k < 9; ++k) wv[k] = __ldg(wp + k);
+        for (int k = 0; k < 9; ++k) {
+            float f[4];
+            Tr::to_f(__ldg(wp + k), f);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) raw[4 * k + e] = f[e];
+        }
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+#pragma unroll
+            for (int k = 0; k < 9; ++k) wt[k][v] = raw[v * 9 + k];
+        const float *b = reinterpret_cast<const float *>(a.bias);
+        if (b) {
+            const float4 b4 = __ldg(reinterpret_cast<const float4 *>(b + t.c0));
+            bv[0] = b4.x; bv[1] = b4.y; bv[2] = b4.z; bv[3] = b4.w;
+        }
     }
+    __syncwarp();     // thread 0 took a branch of its own: reconverge warp 0
     __syncthreads();  // barrier initialised before anyone waits on it
+    if (!wait_halo(sbar, a.status) || !active) return;
+    const int ow = t.ow0 + t.col;
+    if (ow >= a.OW) return;
 
-    // Bounded wait for the halo (every thread polls the mbarrier).
-    bool ok = tc::mbar_try_wait(sbar, 0);
-    if (!ok) {
-        const unsigned long long t0 = globaltimer_ns();
-        for (uint32_t i = 1; !ok; ++i) {
-            ok = tc::mbar_try_wait(sbar, 0);
-            if (!ok && (i & 63u) == 0u && globaltimer_ns() - t0 > kWaitBudgetNs) {
-                if (threadIdx.x == 0) atomicExch(a.status, KSTATUS_TIMEOUT_EPILOGUE);
-                break;
+    const int pix_bytes = a.cbv * VB;
+    const uint8_t *hp = smem + t.cv * VB;
+    const int cw = t.col * stride;
+    auto load = [&](float (&o)[4], int r, int c) {
+        Tr::to_f(*reinterpret_cast<const Vec *>(hp + (r * a.win + c) * pix_bytes), o);
+    };
+    float win[3][3][4];
+#pragma unroll
+    for (int r = 0; r < 3; ++r)
+#pragma unroll
+        for (int s = 0; s < 3; ++s) load(win[r][s], r, cw + s);
+
+    const int rows = min(a.th, a.OH - t.oh0);
+    T *yp = reinterpret_cast<T *>(a.y) + (((long long)t.n * a.OH + t.oh0) * a.OW + ow) * a.C + t.c0;
+    const long long ystep = (long long)a.OW * a.C;
+    for (int i = 0; i < rows; ++i, yp += ystep) {
+        float acc[4] = {bv[0], bv[1], bv[2], bv[3]};
+#pragma unroll
+        for (int r = 0; r < 3; ++r)
+#pragma unroll
+            for (int s = 0; s < 3; ++s)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) acc[v] = __fmaf_rn(win[r][s][v], wt[r * 3 + s][v], acc[v]);
+        if constexpr (std::is_same<T, float>::value) {
+            *reinterpret_cast<uint4 *>(yp) =
+                make_uint4(__float_as_uint(activate(acc[0], a.act)), __float_as_uint(activate(acc[1], a.act)),
+                           __float_as_uint(activate(acc[2], a.act)), __float_as_uint(activate(acc[3], a.act)));
+        } else {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(activate_fast(acc[0], a.act), activate_fast(acc[1], a.act));
+            __nv_bfloat162 hi = __floats2bfloat162_rn(activate_fast(acc[2], a.act), activate_fast(acc[3], a.act));
+            *reinterpret_cast<uint2 *>(yp) =
+                make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+        }
+        if (i + 1 < rows) {
+            const int r0 = (i + 1) * stride;  // halo row of the next window's top tap
+            if (S == 1) {
+#pragma unroll
+                for (int s = 0; s < 3; ++s)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) { win[0][s][v] = win[1][s][v]; win[1][s][v] = win[2][s][v]; }
+#pragma unroll
+                for (int s = 0; s < 3; ++s) load(win[2][s], r0 + 2, cw + s);
+            } else if (S == 2) {
+#pragma unroll
+                for (int s = 0; s < 3; ++s)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) win[0][s][v] = win[2][s][v];
+#pragma unroll
+                for (int s = 0; s < 3; ++s) { load(win[1][s], r0 + 1, cw + s); load(win[2][s], r0 + 2, cw + s); }
+            } else {
+#pragma unroll
+                for (int r = 0; r < 3; ++r)
+#pragma unroll
+                    for (int s = 0; s < 3; ++s) load(win[r][s], r0 + r, cw + s);
             }
         }
     }
-    if (!ok || !active) return;
-    const int ow = ow0 + col;
+}
+
+// int8: 16 channels per thread, packed window and weights, exact int32.
+template <int S>
+__global__ void __launch_bounds__(256, 2)
+dw3x3_i8_kernel(const __grid_constant__ CUtensorMap tmX, const int8_t *__restrict__ w, const DwArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t bar;
+    const int stride = S ? S : a.stride;
+    const uint32_t sbar = tc::smem_u32(&bar);
+    const DwTile t = dw_tile_start<16>(&tmX, a, smem, sbar, stride, 16);
+    const bool active = t.col < a.tw && t.c0 < a.C;
+    uint4 wv[9];
+    if (active) {
+        const uint4 *wp = reinterpret_cast<const uint4 *>(w + (long long)t.c0 * 9);
+#pragma unroll
+        for (int k = 0; k < 9; ++k) wv[k] = __ldg(wp + k);
+    }
+    __syncwarp();
+    __syncthreads();
+    if (!wait_halo(sbar, a.status) || !active) return;
+    const int ow = t.ow0 + t.col;
     if (ow >= a.OW) return;
 
-    const uint8_t *hp = smem + cv * 16;
-    auto halo = [&](int r, int c) {
-        return *reinterpret_cast<const uint4 *>(hp + (r * a.win + c) * cbytes);
-    };
-    const int cw = col * stride;  // halo column of the window's left tap
+    const int pix_bytes = a.cbv * 16;
+    const uint8_t *hp = smem + t.cv * 16;
+    auto halo = [&](int r, int c) { return *reinterpret_cast<const uint4 *>(hp + (r * a.win + c) * pix_bytes); };
+    const int cw = t.col * stride;
     uint4 win[3][3];
 #pragma unroll
     for (int r = 0; r < 3; ++r)
 #pragma unroll
         for (int s = 0; s < 3; ++s) win[r][s] = halo(r, cw + s);
-
-    const int rows = min(a.th, a.OH - oh0);
+    const int32_t *b = reinterpret_cast<const int32_t *>(a.bias);
+    const int rows = min(a.th, a.OH - t.oh0);
     for (int i = 0; i < rows; ++i) {
-        uint4 out;
-        if constexpr (std::is_same<T, float>::value) {
-            float acc[4];
-            const float *b = reinterpret_cast<const float *>(a.bias);
+        int acc[16];
 #pragma unroll
-            for (int v = 0; v < 4; ++v) acc[v] = b ? __ldg(b + c0 + v) : 0.0f;
+        for (int v = 0; v < 16; ++v) acc[v] = 0;
 #pragma unroll
-            for (int r = 0; r < 3; ++r)
+        for (int r = 0; r < 3; ++r)
 #pragma unroll
-                for (int s = 0; s < 3; ++s) {
-                    // weights of tap k for channels c0..c0+3: element v*9+k of wv
-                    float wt[4];
+            for (int s = 0; s < 3; ++s)
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const int e = v * 9 + r * 3 + s;
-                        wt[v] = __uint_as_float(word(wv[e / 4], e % 4));
-                    }
-                    fma_vec(acc, win[r][s], wt);
+                for (int v = 0; v < 16; ++v) {
+                    const int e = v * 9 + r * 3 + s;
+                    const int xv = (int)(int8_t)(word(win[r][s], v >> 2) >> (8 * (v & 3)));
+                    const int wq = (int)(int8_t)(word(wv[e >> 4], (e >> 2) & 3) >> (8 * (e & 3)));
+                    acc[v] += xv * wq;
                 }
-            float o[4];
+        uint32_t wd[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-            for (int v = 0; v < 4; ++v) o[v] = activate(acc[v], a.act);
-            out = make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]),
-                             __float_as_uint(o[3]));
-        } else if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-            float acc[8];
-            const float *b = reinterpret_cast<const float *>(a.bias);
-            if (b) {
-                const float4 b0 = __ldg(reinterpret_cast<const float4 *>(b + c0));
-                const float4 b1 = __ldg(reinterpret_cast<const float4 *>(b + c0) + 1);
-                acc[0] = b0.x; acc[1] = b0.y; acc[2] = b0.z; acc[3] = b0.w;
-                acc[4] = b1.x; acc[5] = b1.y; acc[6] = b1.z; acc[7] = b1.w;
-            } else {
-#pragma unroll
-                for (int v = 0; v < 8; ++v) acc[v] = 0.0f;
-            }
-#pragma unroll
-            for (int r = 0; r < 3; ++r)
-#pragma unroll
-                for (int s = 0; s < 3; ++s)
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        const int e = v * 9 + r * 3 + s;  // weight element (bf16 index)
-                        acc[v] = fma_bf16(word(win[r][s], v >> 1), v & 1, word(wv[e >> 3], (e >> 1) & 3), e & 1,
-                                          acc[v]);
-                    }
-            uint32_t wd[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                __nv_bfloat162 h2 =
-                    __floats2bfloat162_rn(activate_fast(acc[2 * k], a.act), activate_fast(acc[2 * k + 1], a.act));
-                wd[k] = *reinterpret_cast<uint32_t *>(&h2);
-            }
-            out = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-        } else {
-            int acc[16];
-            const int32_t *b = reinterpret_cast<const int32_t *>(a.bias);
-#pragma unroll
-            for (int v = 0; v < 16; ++v) acc[v] = 0;
-#pragma unroll
-            for (int r = 0; r < 3; ++r)
-#pragma unroll
-                for (int s = 0; s < 3; ++s)
-#pragma unroll
-                    for (int v = 0; v < 16; ++v) {
-                        const int e = v * 9 + r * 3 + s;
-                        const int xv = (int)(int8_t)(word(win[r][s], v >> 2) >> (8 * (v & 3)));
-                        const int wt = (int)(int8_t)(word(wv[e >> 4], (e >> 2) & 3) >> (8 * (e & 3)));
-                        acc[v] += xv * wt;
-                    }
-            uint32_t wd[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-            for (int v = 0; v < 16; ++v) {
-                const long long val = (long long)acc[v] + (b ? (long long)__ldg(b + c0 + v) : 0ll);
-                const int q = requant_i8(val, __ldg(a.mult + c0 + v), a.act);
-                wd[v >> 2] |= ((uint32_t)(q & 0xff)) << (8 * (v & 3));
-            }
-            out = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        for (int v = 0; v < 16; ++v) {
+            const long long val = (long long)acc[v] + (b ? (long long)__ldg(b + t.c0 + v) : 0ll);
+            const int q = requant_i8(val, __ldg(a.mult + t.c0 + v), a.act);
+            wd[v >> 2] |= ((uint32_t)(q & 0xff)) << (8 * (v & 3));
         }
-        T *yp = reinterpret_cast<T *>(a.y) + (((long long)n * a.OH + oh0 + i) * a.OW + ow) * a.C + c0;
-        *reinterpret_cast<uint4 *>(yp) = out;
-
+        int8_t *yp = reinterpret_cast<int8_t *>(a.y) + (((long long)t.n * a.OH + t.oh0 + i) * a.OW + ow) * a.C + t.c0;
+        *reinterpret_cast<uint4 *>(yp) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
         if (i + 1 < rows) {
-            const int r0 = (i + 1) * stride;  // halo row of the next window's top tap
+            const int r0 = (i + 1) * stride;
             if (S == 1) {
 #pragma unroll
                 for (int s = 0; s < 3; ++s) { win[0][s] = win[1][s]; win[1][s] = win[2][s]; win[2][s] = halo(r0 + 2, cw + s); }
@@ -280,18 +320,25 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 
 template <typename T>
 void *kernel_for(int stride) {
-    if (stride == 1) return reinterpret_cast<void *>(&dw3x3_kernel<T, 1>);
-    if (stride == 2) return reinterpret_cast<void *>(&dw3x3_kernel<T, 2>);
-    return reinterpret_cast<void *>(&dw3x3_kernel<T, 0>);
+    if (stride == 1) return reinterpret_cast<void *>(&dw3x3_float_kernel<T, 1>);
+    if (stride == 2) return reinterpret_cast<void *>(&dw3x3_float_kernel<T, 2>);
+    return reinterpret_cast<void *>(&dw3x3_float_kernel<T, 0>);
 }
 
 void *select(conv_dtype_t dt, int stride) {
     switch (dt) {
     case CONV_F32: return kernel_for<float>(stride);
     case CONV_BF16: return kernel_for<__nv_bfloat16>(stride);
-    default: return kernel_for<int8_t>(stride);
+    default:
+        if (stride == 1) return reinterpret_cast<void *>(&dw3x3_i8_kernel<1>);
+        if (stride == 2) return reinterpret_cast<void *>(&dw3x3_i8_kernel<2>);
+        return reinterpret_cast<void *>(&dw3x3_i8_kernel<0>);
     }
 }
+
+// Channels a thread owns and bytes of its vector.
+int dw_chans(conv_dtype_t dt) { return dt == CONV_I8 ? 16 : 4; }
+int dw_vbytes(conv_dtype_t dt) { return dt == CONV_BF16 ? 8 : 16; }
 
 CUtensorMapDataType tma_type(conv_dtype_t dt) {
     return dt == CONV_F32 ? DwT<float>::tma : (dt == CONV_BF16 ? DwT<__nv_bfloat16>::tma : DwT<int8_t>::tma);
@@ -301,7 +348,7 @@ CUtensorMapDataType tma_type(conv_dtype_t dt) {
 
 bool dw3x3_supported(const conv_plan *p) {
     const int C = p->s.c_in;
-    const int V = 16 / conv_esize(p->dtype);
+    const int V = dw_chans(p->dtype);
     if (!(p->groups == C && p->s.c_out == C && p->s.k_h == 3 && p->s.k_w == 3 && C % V == 0)) return false;
     if (p->stride > 64) return false;                        // halo box sides are at most 256
     if ((long long)p->s.n * p->s.h * p->s.w >= (1ll << 31)) return false;
@@ -310,15 +357,16 @@ bool dw3x3_supported(const conv_plan *p) {
 
 int dw3x3_configure(conv_plan *p) {
     const int S = p->stride;
-    const int V = 16 / conv_esize(p->dtype);
+    const int V = dw_chans(p->dtype);
     const int cvt = p->s.c_in / V;                 // channel vectors in a pixel
+    const int maxv = 256 / dw_vbytes(p->dtype);    // at most 256 bytes of channels per tile pixel
     // Channel vectors and output columns per tile: at most 256 threads, the
     // fewest halo columns loaded per output row (ragged tiles load wasted
     // columns too), then the most threads.
     int best_tw = 1, best_cbv = 1;
     long long best_cost = -1;
-    for (int cbv : {16, 8, 4, 2, 1}) {
-        if (cbv > cvt || cvt % cbv != 0) continue;
+    for (int cbv : {32, 16, 8, 4, 2, 1}) {
+        if (cbv > maxv || cbv > cvt || cvt % cbv != 0) continue;
         for (int tw = 1; tw * cbv <= 256 && (tw - 1) * S + 3 <= 256; ++tw) {
             const long long tiles = (p->ow + tw - 1) / tw;
             const long long cost = tiles * ((tw - 1) * S + 3) * (cvt / cbv);
@@ -341,7 +389,7 @@ int dw3x3_configure(conv_plan *p) {
     g.tiles_w = (p->ow + best_tw - 1) / best_tw;
     g.tiles_h = (p->oh + th - 1) / th;
     g.tiles_c = (cvt + cbv - 1) / cbv;
-    g.smem = g.hin * g.win * cbv * 16;
+    g.smem = g.hin * g.win * cbv * dw_vbytes(p->dtype);
     g.threads = ((best_tw * cbv + 31) / 32) * 32;
     g.blocks = (long long)g.tiles_c * g.tiles_w * g.tiles_h * p->s.n;
     return conv_grant_smem(select(p->dtype, S), p->device, g.smem);
@@ -353,7 +401,7 @@ cudaError_t launch_dw3x3(const conv_plan *p, const void *x, const void *w, const
     PFN_cuTensorMapEncodeTiled_v12000 encode = encoder();
     if (!encode) return cudaErrorNotSupported;
     const int es = conv_esize(p->dtype);
-    const int V = 16 / es;
+    const int V = dw_chans(p->dtype);
     alignas(64) CUtensorMap tm;
     const cuuint64_t dims[4] = {(cuuint64_t)p->s.c_in, (cuuint64_t)p->s.w, (cuuint64_t)p->s.h, (cuuint64_t)p->s.n};
     const cuuint64_t strides[3] = {(cuuint64_t)p->s.c_in * es, (cuuint64_t)p->s.w * p->s.c_in * es,

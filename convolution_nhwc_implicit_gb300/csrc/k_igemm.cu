@@ -136,6 +136,8 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         tc::tmem_alloc(tc::smem_u32((const void *)tmem_holder), kTmemCols);
         tc::tmem_relinquish();
     }
+    // __syncthreads is an aligned barrier: every warp must reach it converged.
+    __syncwarp();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -295,10 +297,13 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         }
     }
 
+    // Warps 0 and 1 ran their loops on lane 0 only: reconverge each warp
+    // before the block barrier, so that the barrier really waits for every
+    // role (TMEM is freed only after the epilogue's last tcgen05.ld).
+    __syncwarp();
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 1) {
-        __syncwarp();
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem_base, kTmemCols);
     }
