@@ -41,7 +41,8 @@ struct DwGeom {
     int tiles_w, tiles_h, tiles_c;
     int smem;      // dynamic shared memory bytes (the halo)
     int threads;   // threads per CTA
-    long long blocks;
+    long long tiles;   // output tiles
+    long long blocks;  // persistent CTAs
 };
 
 struct conv_plan {

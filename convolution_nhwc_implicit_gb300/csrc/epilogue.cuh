@@ -26,10 +26,12 @@ __device__ __forceinline__ float mish_f32(float v) {
 
 // The same Mish with the hardware exp2 and reciprocal approximations
 // (__expf, __fdividef): relative error ~1e-6, far below the bf16 rounding
-// (2^-9) of the outputs it feeds.  t + 2 stays below 2^126 because v <= 20.
+// (2^-9) of the outputs it feeds.  t + 2 stays below 2^126 (__fdividef's
+// range) because the exponent is clamped at 20.
 __device__ __forceinline__ float mish_fast(float v) {
-    if (v > 20.0f) return v;
-    const float n = __expf(v);
+    // Above v = 20, t / (t + 2) rounds to 1: clamping the exponent there
+    // gives v exactly, without a branch, and keeps t finite.
+    const float n = __expf(fminf(v, 20.0f));
     const float t = n * (n + 2.0f);
     return v * __fdividef(t, t + 2.0f);
 }

@@ -41,7 +41,7 @@ struct DwArgs {
     int H, W, C, OH, OW, stride, pad_h, pad_w;
     int th, tw, cbv;          // tile: output rows, output columns, 16-byte channel vectors
     int hin, win;             // halo rows / columns
-    int tiles_w, tiles_h, tiles_c;
+    int tiles_w, tiles_h, tiles_c, tiles_total;
     int act;
     const void *bias;
     const float *mult;
@@ -78,53 +78,70 @@ template <> struct DwT<int8_t> {
     static constexpr CUtensorMapDataType tma = CU_TENSOR_MAP_DATA_TYPE_UINT8;
 };
 
+template <typename T> __host__ __device__ constexpr int V_OF() { return DwT<T>::V; }
+
+// Two fp32 FMAs in one packed instruction (each lane rounded once, like
+// two __fmaf_rn): (d0, d1) = (a0 * b0 + c0, a1 * b1 + c1).
+__device__ __forceinline__ void ffma2(float &d0, float &d1, float a0, float a1, float b0, float b1, float c0,
+                                      float c1) {
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rc, ra, rb, rc;\n\tmov.b64 {%0, %1}, rc;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
 __device__ __forceinline__ uint32_t word(const uint4 &u, int i) {
     return i == 0 ? u.x : (i == 1 ? u.y : (i == 2 ? u.z : u.w));
 }
 
-// Bounded wait for the halo; false if it ran out (status word set).
-__device__ __forceinline__ bool wait_halo(uint32_t sbar, int *status) {
-    if (tc::mbar_try_wait(sbar, 0)) return true;
+// Output rows a thread walks per tile (the configured th is at most this).
+constexpr int kMaxTh = 8;
+
+// Bounded wait for a halo; false if it ran out (status word set).
+__device__ __forceinline__ bool wait_halo(uint32_t sbar, uint32_t parity, int *status) {
+    if (tc::mbar_try_wait(sbar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
-        if (tc::mbar_try_wait(sbar, 0)) return true;
+        if (tc::mbar_try_wait(sbar, parity)) return true;
         if ((i & 63u) == 0u && globaltimer_ns() - t0 > kWaitBudgetNs) {
-            if (threadIdx.x == 0) atomicExch(status, KSTATUS_TIMEOUT_EPILOGUE);
+            atomicExch(status, KSTATUS_TIMEOUT_EPILOGUE);
             return false;
         }
     }
 }
 
-// Issues the halo TMA (thread 0); returns the tile's coordinates.
+// Tile t -> (channel block, image, first output row / column); channel
+// block fastest.
 struct DwTile {
-    int n, oh0, ow0, cv, col, c0;
+    int tcb, n, oh0, ow0;
 };
-
-template <int V>
-__device__ __forceinline__ DwTile dw_tile_start(const CUtensorMap *tmX, const DwArgs &a, uint8_t *smem,
-                                                uint32_t sbar, int stride, int vbytes) {
-    DwTile t;
-    int b = blockIdx.x;
-    const int tc_ = b % a.tiles_c; b /= a.tiles_c;
-    const int tw_ = b % a.tiles_w; b /= a.tiles_w;
-    const int th_ = b % a.tiles_h;
-    t.n = b / a.tiles_h;
-    t.oh0 = th_ * a.th;
-    t.ow0 = tw_ * a.tw;
-    t.cv = threadIdx.x % a.cbv;
-    t.col = threadIdx.x / a.cbv;
-    t.c0 = (tc_ * a.cbv + t.cv) * V;
-    if (threadIdx.x == 0) {
-        tc::mbar_init(sbar, 1);
-        tc::fence_mbar_init();
-        tc::mbar_arrive_expect_tx(sbar, (uint32_t)(a.hin * a.win * a.cbv * vbytes));
-        tc::tma_load_4d(tc::smem_u32(smem), tmX, sbar, tc_ * a.cbv * V, t.ow0 * stride - a.pad_w,
-                        t.oh0 * stride - a.pad_h, t.n);
-    }
-    return t;
+__device__ __forceinline__ DwTile tile_of(const DwArgs &a, int t) {
+    DwTile d;
+    d.tcb = t % a.tiles_c; t /= a.tiles_c;
+    const int tw_ = t % a.tiles_w; t /= a.tiles_w;
+    d.oh0 = (t % a.tiles_h) * a.th;
+    d.n = t / a.tiles_h;
+    d.ow0 = tw_ * a.tw;
+    return d;
 }
 
-// fp32 and bf16: fp32 window and weights in registers, FFMA.
+// Thread 0: start the TMA of tile t's halo into `dst`, completing on `bar`.
+template <int V>
+__device__ __forceinline__ void issue_halo(const CUtensorMap *tm, const DwArgs &a, uint32_t dst, uint32_t bar,
+                                           int t, int stride, uint32_t bytes) {
+    const DwTile d = tile_of(a, t);
+    // The buffer was last read through ordinary shared-memory loads; order
+    // those before the asynchronous-proxy write that reuses it.
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc::mbar_arrive_expect_tx(bar, bytes);
+    tc::tma_load_4d(dst, tm, bar, d.tcb * a.cbv * V, d.ow0 * stride - a.pad_w, d.oh0 * stride - a.pad_h, d.n);
+}
+
+// Persistent CTAs: a CTA takes tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+// (gridDim.x is a multiple of tiles_c, so they all share one channel block
+// and the thread's weights load once).  Two halo buffers: the TMA of the next
+// tile runs while the current one is computed.
 template <typename T, int S>
 __global__ void __launch_bounds__(256, 2)
 dw3x3_float_kernel(const __grid_constant__ CUtensorMap tmX, const T *__restrict__ w, const DwArgs a) {
@@ -132,18 +149,34 @@ dw3x3_float_kernel(const __grid_constant__ CUtensorMap tmX, const T *__restrict_
     using Vec = typename Tr::Vec;
     constexpr int VB = sizeof(Vec);
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(8) uint64_t bar;
+    __shared__ __align__(8) uint64_t bars[2];
     const int stride = S ? S : a.stride;
-    const uint32_t sbar = tc::smem_u32(&bar);
-    const DwTile t = dw_tile_start<4>(&tmX, a, smem, sbar, stride, VB);
+    const uint32_t halo_bytes = (uint32_t)(a.hin * a.win * a.cbv * VB);
+    const uint32_t buf_stride = (halo_bytes + 127u) & ~127u;
+    const uint32_t sbase = tc::smem_u32(smem);
+    const uint32_t sbar0 = tc::smem_u32(&bars[0]);
+    if (threadIdx.x == 0) {
+        tc::mbar_init(sbar0, 1);
+        tc::mbar_init(sbar0 + 8, 1);
+        tc::fence_mbar_init();
+        if ((int)blockIdx.x < a.tiles_total)
+            issue_halo<4>(&tmX, a, sbase, sbar0, blockIdx.x, stride, halo_bytes);
+    }
+    __syncwarp();
+    __syncthreads();
+
+    const int cv = threadIdx.x % a.cbv;
+    const int col = threadIdx.x / a.cbv;
+    const int tcb = blockIdx.x % a.tiles_c;   // the same for all of this CTA's tiles
+    const int c0 = (tcb * a.cbv + cv) * V_OF<T>();
+    const bool active = col < a.tw && c0 < a.C;
 
     // Weights (OHWI [C][3][3]: a channel's nine taps are contiguous, so the
-    // thread's 4 x 9 weights are nine vectors) and bias, while the halo flies.
-    const bool active = t.col < a.tw && t.c0 < a.C;
+    // thread's 4 x 9 weights are nine vectors) and bias, loaded once.
     float wt[9][4];
     float bv[4] = {0.f, 0.f, 0.f, 0.f};
     if (active) {
-        const Vec *wp = reinterpret_cast<const Vec *>(w + (long long)t.c0 * 9);
+        const Vec *wp = reinterpret_cast<const Vec *>(w + (long long)c0 * 9);
         float raw[36];
 #pragma unroll
         for (int k = 0; k < 9; ++k) {
@@ -158,72 +191,99 @@ dw3x3_float_kernel(const __grid_constant__ CUtensorMap tmX, const T *__restrict_
             for (int k = 0; k < 9; ++k) wt[k][v] = raw[v * 9 + k];
         const float *b = reinterpret_cast<const float *>(a.bias);
         if (b) {
-            const float4 b4 = __ldg(reinterpret_cast<const float4 *>(b + t.c0));
+            const float4 b4 = __ldg(reinterpret_cast<const float4 *>(b + c0));
             bv[0] = b4.x; bv[1] = b4.y; bv[2] = b4.z; bv[3] = b4.w;
         }
     }
-    __syncwarp();     // thread 0 took a branch of its own: reconverge warp 0
-    __syncthreads();  // barrier initialised before anyone waits on it
-    if (!wait_halo(sbar, a.status) || !active) return;
-    const int ow = t.ow0 + t.col;
-    if (ow >= a.OW) return;
-
     const int pix_bytes = a.cbv * VB;
-    const uint8_t *hp = smem + t.cv * VB;
-    const int cw = t.col * stride;
-    auto load = [&](float (&o)[4], int r, int c) {
-        Tr::to_f(*reinterpret_cast<const Vec *>(hp + (r * a.win + c) * pix_bytes), o);
-    };
-    float win[3][3][4];
-#pragma unroll
-    for (int r = 0; r < 3; ++r)
-#pragma unroll
-        for (int s = 0; s < 3; ++s) load(win[r][s], r, cw + s);
+    const int cw = col * stride;
 
-    const int rows = min(a.th, a.OH - t.oh0);
-    T *yp = reinterpret_cast<T *>(a.y) + (((long long)t.n * a.OH + t.oh0) * a.OW + ow) * a.C + t.c0;
-    const long long ystep = (long long)a.OW * a.C;
-    for (int i = 0; i < rows; ++i, yp += ystep) {
-        float acc[4] = {bv[0], bv[1], bv[2], bv[3]};
+    int k = 0;
+    for (int t = blockIdx.x; t < a.tiles_total; t += gridDim.x, ++k) {
+        const int buf = k & 1;
+        if (threadIdx.x == 0 && t + (int)gridDim.x < a.tiles_total)
+            issue_halo<4>(&tmX, a, sbase + (buf ^ 1) * buf_stride, sbar0 + 8 * (buf ^ 1), t + gridDim.x, stride,
+                          halo_bytes);
+        const bool ok = wait_halo(sbar0 + 8 * buf, (uint32_t)(k >> 1) & 1u, a.status);
+        if (__syncthreads_or(!ok)) return;  // block-uniform give-up
+        const DwTile d = tile_of(a, t);
+        const int ow = d.ow0 + col;
+        if (active && ow < a.OW) {
+            const uint8_t *hp = smem + buf * buf_stride + cv * VB;
+            auto load = [&](float (&o)[4], int r, int c) {
+                Tr::to_f(*reinterpret_cast<const Vec *>(hp + (r * a.win + c) * pix_bytes), o);
+            };
+            float win[3][3][4];
 #pragma unroll
-        for (int r = 0; r < 3; ++r)
+            for (int r = 0; r < 3; ++r)
 #pragma unroll
-            for (int s = 0; s < 3; ++s)
+                for (int s = 0; s < 3; ++s) load(win[r][s], r, cw + s);
+            const int rows = min(a.th, a.OH - d.oh0);
+            T *yp = reinterpret_cast<T *>(a.y) + (((long long)d.n * a.OH + d.oh0) * a.OW + ow) * a.C + c0;
+            const long long ystep = (long long)a.OW * a.C;
+            // Fully unrolled walk down the tile (th <= kMaxTh): the window
+            // rotation is register renaming, not moves.
 #pragma unroll
-                for (int v = 0; v < 4; ++v) acc[v] = __fmaf_rn(win[r][s][v], wt[r * 3 + s][v], acc[v]);
-        if constexpr (std::is_same<T, float>::value) {
-            *reinterpret_cast<uint4 *>(yp) =
-                make_uint4(__float_as_uint(activate(acc[0], a.act)), __float_as_uint(activate(acc[1], a.act)),
-                           __float_as_uint(activate(acc[2], a.act)), __float_as_uint(activate(acc[3], a.act)));
-        } else {
-            __nv_bfloat162 lo = __floats2bfloat162_rn(activate_fast(acc[0], a.act), activate_fast(acc[1], a.act));
-            __nv_bfloat162 hi = __floats2bfloat162_rn(activate_fast(acc[2], a.act), activate_fast(acc[3], a.act));
-            *reinterpret_cast<uint2 *>(yp) =
-                make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
-        }
-        if (i + 1 < rows) {
-            const int r0 = (i + 1) * stride;  // halo row of the next window's top tap
-            if (S == 1) {
-#pragma unroll
-                for (int s = 0; s < 3; ++s)
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) { win[0][s][v] = win[1][s][v]; win[1][s][v] = win[2][s][v]; }
-#pragma unroll
-                for (int s = 0; s < 3; ++s) load(win[2][s], r0 + 2, cw + s);
-            } else if (S == 2) {
-#pragma unroll
-                for (int s = 0; s < 3; ++s)
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) win[0][s][v] = win[2][s][v];
-#pragma unroll
-                for (int s = 0; s < 3; ++s) { load(win[1][s], r0 + 1, cw + s); load(win[2][s], r0 + 2, cw + s); }
-            } else {
+            for (int i = 0; i < kMaxTh; ++i) {
+                if (i >= rows) break;
+                float acc[4];
 #pragma unroll
                 for (int r = 0; r < 3; ++r)
 #pragma unroll
-                    for (int s = 0; s < 3; ++s) load(win[r][s], r0 + r, cw + s);
+                    for (int s = 0; s < 3; ++s) {
+                        const int k = r * 3 + s;
+                        // the bias seeds the first tap's FMA
+                        const float c0_ = k == 0 ? bv[0] : acc[0], c1_ = k == 0 ? bv[1] : acc[1];
+                        const float c2_ = k == 0 ? bv[2] : acc[2], c3_ = k == 0 ? bv[3] : acc[3];
+                        ffma2(acc[0], acc[1], win[r][s][0], win[r][s][1], wt[k][0], wt[k][1], c0_, c1_);
+                        ffma2(acc[2], acc[3], win[r][s][2], win[r][s][3], wt[k][2], wt[k][3], c2_, c3_);
+                    }
+                if constexpr (std::is_same<T, float>::value) {
+                    *reinterpret_cast<uint4 *>(yp) = make_uint4(
+                        __float_as_uint(activate(acc[0], a.act)), __float_as_uint(activate(acc[1], a.act)),
+                        __float_as_uint(activate(acc[2], a.act)), __float_as_uint(activate(acc[3], a.act)));
+                } else {
+                    __nv_bfloat162 lo =
+                        __floats2bfloat162_rn(activate_fast(acc[0], a.act), activate_fast(acc[1], a.act));
+                    __nv_bfloat162 hi =
+                        __floats2bfloat162_rn(activate_fast(acc[2], a.act), activate_fast(acc[3], a.act));
+                    *reinterpret_cast<uint2 *>(yp) =
+                        make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+                }
+                yp += ystep;
+                if (i + 1 < rows) {
+                    const int r0 = (i + 1) * stride;  // halo row of the next window's top tap
+                    if (S == 1) {
+#pragma unroll
+                        for (int s = 0; s < 3; ++s)
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) {
+                                win[0][s][v] = win[1][s][v];
+                                win[1][s][v] = win[2][s][v];
+                            }
+#pragma unroll
+                        for (int s = 0; s < 3; ++s) load(win[2][s], r0 + 2, cw + s);
+                    } else if (S == 2) {
+#pragma unroll
+                        for (int s = 0; s < 3; ++s)
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) win[0][s][v] = win[2][s][v];
+#pragma unroll
+                        for (int s = 0; s < 3; ++s) {
+                            load(win[1][s], r0 + 1, cw + s);
+                            load(win[2][s], r0 + 2, cw + s);
+                        }
+                    } else {
+#pragma unroll
+                        for (int r = 0; r < 3; ++r)
+#pragma unroll
+                            for (int s = 0; s < 3; ++s) load(win[r][s], r0 + r, cw + s);
+                    }
+                }
             }
         }
+        __syncwarp();
+        __syncthreads();  // this buffer is free for the TMA two tiles ahead
     }
 }
 
@@ -232,75 +292,107 @@ template <int S>
 __global__ void __launch_bounds__(256, 2)
 dw3x3_i8_kernel(const __grid_constant__ CUtensorMap tmX, const int8_t *__restrict__ w, const DwArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(8) uint64_t bar;
+    __shared__ __align__(8) uint64_t bars[2];
     const int stride = S ? S : a.stride;
-    const uint32_t sbar = tc::smem_u32(&bar);
-    const DwTile t = dw_tile_start<16>(&tmX, a, smem, sbar, stride, 16);
-    const bool active = t.col < a.tw && t.c0 < a.C;
-    uint4 wv[9];
-    if (active) {
-        const uint4 *wp = reinterpret_cast<const uint4 *>(w + (long long)t.c0 * 9);
-#pragma unroll
-        for (int k = 0; k < 9; ++k) wv[k] = __ldg(wp + k);
+    const uint32_t halo_bytes = (uint32_t)(a.hin * a.win * a.cbv * 16);
+    const uint32_t buf_stride = (halo_bytes + 127u) & ~127u;
+    const uint32_t sbase = tc::smem_u32(smem);
+    const uint32_t sbar0 = tc::smem_u32(&bars[0]);
+    if (threadIdx.x == 0) {
+        tc::mbar_init(sbar0, 1);
+        tc::mbar_init(sbar0 + 8, 1);
+        tc::fence_mbar_init();
+        if ((int)blockIdx.x < a.tiles_total)
+            issue_halo<16>(&tmX, a, sbase, sbar0, blockIdx.x, stride, halo_bytes);
     }
     __syncwarp();
     __syncthreads();
-    if (!wait_halo(sbar, a.status) || !active) return;
-    const int ow = t.ow0 + t.col;
-    if (ow >= a.OW) return;
-
-    const int pix_bytes = a.cbv * 16;
-    const uint8_t *hp = smem + t.cv * 16;
-    auto halo = [&](int r, int c) { return *reinterpret_cast<const uint4 *>(hp + (r * a.win + c) * pix_bytes); };
-    const int cw = t.col * stride;
-    uint4 win[3][3];
+    const int cv = threadIdx.x % a.cbv;
+    const int col = threadIdx.x / a.cbv;
+    const int c0 = ((int)(blockIdx.x % a.tiles_c) * a.cbv + cv) * 16;
+    const bool active = col < a.tw && c0 < a.C;
+    uint4 wv[9];
+    if (active) {
+        const uint4 *wp = reinterpret_cast<const uint4 *>(w + (long long)c0 * 9);
 #pragma unroll
-    for (int r = 0; r < 3; ++r)
-#pragma unroll
-        for (int s = 0; s < 3; ++s) win[r][s] = halo(r, cw + s);
+        for (int k = 0; k < 9; ++k) wv[k] = __ldg(wp + k);
+    }
     const int32_t *b = reinterpret_cast<const int32_t *>(a.bias);
-    const int rows = min(a.th, a.OH - t.oh0);
-    for (int i = 0; i < rows; ++i) {
-        int acc[16];
+    const int pix_bytes = a.cbv * 16;
+    const int cw = col * stride;
+    int k = 0;
+    for (int t = blockIdx.x; t < a.tiles_total; t += gridDim.x, ++k) {
+        const int buf = k & 1;
+        if (threadIdx.x == 0 && t + (int)gridDim.x < a.tiles_total)
+            issue_halo<16>(&tmX, a, sbase + (buf ^ 1) * buf_stride, sbar0 + 8 * (buf ^ 1), t + gridDim.x, stride,
+                           halo_bytes);
+        const bool ok = wait_halo(sbar0 + 8 * buf, (uint32_t)(k >> 1) & 1u, a.status);
+        if (__syncthreads_or(!ok)) return;
+        const DwTile d = tile_of(a, t);
+        const int ow = d.ow0 + col;
+        if (active && ow < a.OW) {
+            const uint8_t *hp = smem + buf * buf_stride + cv * 16;
+            auto halo = [&](int r, int c) {
+                return *reinterpret_cast<const uint4 *>(hp + (r * a.win + c) * pix_bytes);
+            };
+            uint4 win[3][3];
 #pragma unroll
-        for (int v = 0; v < 16; ++v) acc[v] = 0;
+            for (int r = 0; r < 3; ++r)
 #pragma unroll
-        for (int r = 0; r < 3; ++r)
+                for (int s = 0; s < 3; ++s) win[r][s] = halo(r, cw + s);
+            const int rows = min(a.th, a.OH - d.oh0);
+            for (int i = 0; i < rows; ++i) {
+                int acc[16];
 #pragma unroll
-            for (int s = 0; s < 3; ++s)
-#pragma unroll
-                for (int v = 0; v < 16; ++v) {
-                    const int e = v * 9 + r * 3 + s;
-                    const int xv = (int)(int8_t)(word(win[r][s], v >> 2) >> (8 * (v & 3)));
-                    const int wq = (int)(int8_t)(word(wv[e >> 4], (e >> 2) & 3) >> (8 * (e & 3)));
-                    acc[v] += xv * wq;
-                }
-        uint32_t wd[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-        for (int v = 0; v < 16; ++v) {
-            const long long val = (long long)acc[v] + (b ? (long long)__ldg(b + t.c0 + v) : 0ll);
-            const int q = requant_i8(val, __ldg(a.mult + t.c0 + v), a.act);
-            wd[v >> 2] |= ((uint32_t)(q & 0xff)) << (8 * (v & 3));
-        }
-        int8_t *yp = reinterpret_cast<int8_t *>(a.y) + (((long long)t.n * a.OH + t.oh0 + i) * a.OW + ow) * a.C + t.c0;
-        *reinterpret_cast<uint4 *>(yp) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-        if (i + 1 < rows) {
-            const int r0 = (i + 1) * stride;
-            if (S == 1) {
-#pragma unroll
-                for (int s = 0; s < 3; ++s) { win[0][s] = win[1][s]; win[1][s] = win[2][s]; win[2][s] = halo(r0 + 2, cw + s); }
-            } else if (S == 2) {
-#pragma unroll
-                for (int s = 0; s < 3; ++s) {
-                    win[0][s] = win[2][s]; win[1][s] = halo(r0 + 1, cw + s); win[2][s] = halo(r0 + 2, cw + s);
-                }
-            } else {
+                for (int v = 0; v < 16; ++v) acc[v] = 0;
 #pragma unroll
                 for (int r = 0; r < 3; ++r)
 #pragma unroll
-                    for (int s = 0; s < 3; ++s) win[r][s] = halo(r0 + r, cw + s);
+                    for (int s = 0; s < 3; ++s)
+#pragma unroll
+                        for (int v = 0; v < 16; ++v) {
+                            const int e = v * 9 + r * 3 + s;
+                            const int xv = (int)(int8_t)(word(win[r][s], v >> 2) >> (8 * (v & 3)));
+                            const int wq = (int)(int8_t)(word(wv[e >> 4], (e >> 2) & 3) >> (8 * (e & 3)));
+                            acc[v] += xv * wq;
+                        }
+                uint32_t wd[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                for (int v = 0; v < 16; ++v) {
+                    const long long val = (long long)acc[v] + (b ? (long long)__ldg(b + c0 + v) : 0ll);
+                    const int q = requant_i8(val, __ldg(a.mult + c0 + v), a.act);
+                    wd[v >> 2] |= ((uint32_t)(q & 0xff)) << (8 * (v & 3));
+                }
+                int8_t *yp = reinterpret_cast<int8_t *>(a.y) +
+                             (((long long)d.n * a.OH + d.oh0 + i) * a.OW + ow) * a.C + c0;
+                *reinterpret_cast<uint4 *>(yp) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+                if (i + 1 < rows) {
+                    const int r0 = (i + 1) * stride;
+                    if (S == 1) {
+#pragma unroll
+                        for (int s = 0; s < 3; ++s) {
+                            win[0][s] = win[1][s];
+                            win[1][s] = win[2][s];
+                            win[2][s] = halo(r0 + 2, cw + s);
+                        }
+                    } else if (S == 2) {
+#pragma unroll
+                        for (int s = 0; s < 3; ++s) {
+                            win[0][s] = win[2][s];
+                            win[1][s] = halo(r0 + 1, cw + s);
+                            win[2][s] = halo(r0 + 2, cw + s);
+                        }
+                    } else {
+#pragma unroll
+                        for (int r = 0; r < 3; ++r)
+#pragma unroll
+                            for (int s = 0; s < 3; ++s) win[r][s] = halo(r0 + r, cw + s);
+                    }
+                }
             }
         }
+        __syncwarp();
+        __syncthreads();
     }
 }
 
@@ -352,7 +444,7 @@ bool dw3x3_supported(const conv_plan *p) {
     if (!(p->groups == C && p->s.c_out == C && p->s.k_h == 3 && p->s.k_w == 3 && C % V == 0)) return false;
     if (p->stride > 64) return false;                        // halo box sides are at most 256
     if ((long long)p->s.n * p->s.h * p->s.w >= (1ll << 31)) return false;
-    return true;
+    return true;  // tile counts fit an int: at most N*H*W tiles
 }
 
 int dw3x3_configure(conv_plan *p) {
@@ -377,7 +469,7 @@ int dw3x3_configure(conv_plan *p) {
         }
     }
     const int cbv = best_cbv;
-    int th = 8;
+    int th = kMaxTh;
     if (th > p->oh) th = p->oh;
     while ((th - 1) * S + 3 > 256) --th;
     DwGeom &g = p->dw;
@@ -389,9 +481,17 @@ int dw3x3_configure(conv_plan *p) {
     g.tiles_w = (p->ow + best_tw - 1) / best_tw;
     g.tiles_h = (p->oh + th - 1) / th;
     g.tiles_c = (cvt + cbv - 1) / cbv;
-    g.smem = g.hin * g.win * cbv * dw_vbytes(p->dtype);
+    const int halo = g.hin * g.win * cbv * dw_vbytes(p->dtype);
+    g.smem = 2 * ((halo + 127) & ~127);  // two halo buffers (double buffering)
     g.threads = ((best_tw * cbv + 31) / 32) * 32;
-    g.blocks = (long long)g.tiles_c * g.tiles_w * g.tiles_h * p->s.n;
+    g.tiles = (long long)g.tiles_c * g.tiles_w * g.tiles_h * p->s.n;
+    // Persistent grid: two CTAs per SM, a multiple of the channel-block count
+    // (each CTA then keeps one channel block), at most one CTA per tile.
+    long long grid = (long long)p->num_sms * 2;
+    if (grid > g.tiles) grid = g.tiles;
+    if (grid > g.tiles_c) grid -= grid % g.tiles_c;
+    else grid = g.tiles_c;  // one CTA per channel block (tiles is a multiple of tiles_c)
+    g.blocks = grid;
     return conv_grant_smem(select(p->dtype, S), p->device, g.smem);
 }
 
@@ -417,6 +517,7 @@ cudaError_t launch_dw3x3(const conv_plan *p, const void *x, const void *w, const
     a.stride = p->stride; a.pad_h = p->pad_h; a.pad_w = p->pad_w;
     a.th = g.th; a.tw = g.tw; a.cbv = g.cbv; a.hin = g.hin; a.win = g.win;
     a.tiles_w = g.tiles_w; a.tiles_h = g.tiles_h; a.tiles_c = g.tiles_c;
+    a.tiles_total = (int)g.tiles;
     a.act = (int)p->act;
     a.bias = bias;
     a.mult = p->d_mult;

@@ -89,7 +89,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
 template <int BN, int BK, bool FLAT>
 __global__ void __launch_bounds__(cta_threads(BN), 1)
 igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  const IgArgs a) {
+                  const __grid_constant__ CUtensorMap tmY, const IgArgs a) {
     constexpr uint32_t kRowBytes = BK * 2;
     constexpr uint32_t kAStage = kBM * BK * 2;
     constexpr uint32_t kBStage = BN * BK * 2;
@@ -98,6 +98,7 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     constexpr int kGroups = epi_groups(BN);
     constexpr int kCols = BN / kGroups;  // accumulator columns per epilogue thread (32 or 64)
     static_assert(kCols % 32 == 0, "epilogue reads TMEM 32 columns at a time");
+    constexpr uint32_t kOutStage = kBM * 64;  // 128 rows x 32 bf16 columns
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
@@ -106,7 +107,8 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const int stages = a.stages;
     const uint32_t sA = base;
     const uint32_t sB = base + stages * kAStage;
-    const uint32_t sBar = sB + stages * kBStage;
+    const uint32_t sOut = sB + stages * kBStage;  // per epilogue group: 128 rows x 64 B output staging
+    const uint32_t sBar = sOut + kGroups * kOutStage;
     auto full_bar = [&](int s) { return sBar + 8u * s; };
     auto empty_bar = [&](int s) { return sBar + 8u * (stages + s); };
     auto tfull_bar = [&](int b) { return sBar + 8u * (2 * stages + b); };
@@ -131,6 +133,7 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         tc::fence_mbar_init();
         tc::tma_prefetch_desc(&tmA);
         tc::tma_prefetch_desc(&tmB);
+        tc::tma_prefetch_desc(&tmY);
     }
     if (warp == 1) {
         tc::tmem_alloc(tc::smem_u32((const void *)tmem_holder), kTmemCols);
@@ -231,6 +234,7 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         const int grp = (warp - 2) >> 2;
         const int row = q * 32 + lane;
         const int c_base = grp * kCols;
+        const bool issuer = ((warp - 2) & 3) == 0 && lane == 0;  // issues the group's TMA stores
         int lt = 0;
         for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x, ++lt) {
             const int buf = lt & 1;
@@ -251,50 +255,69 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             tc::fence_before_sync();
             tc::mbar_arrive(tempty_bar(buf));
 
+            // Output slice: bias, activation, bf16, staged in shared memory
+            // (64-byte swizzle, matching the store's tensor map) and written by
+            // one TMA tensor store per 32 columns.  The box is the tile's
+            // bh x bw pixel rectangle (or 128 flat rows): rows past it are
+            // never stored and pixels outside the image are clipped by TMA.
             const int nb = tile % a.tiles_n;
             const int mt = tile / a.tiles_n;
-            bool valid;
-            long long pix;
+            int n = 0, oh0 = 0, ow0 = 0, m0 = 0;
             if (FLAT) {
-                pix = (long long)mt * kBM + row;
-                valid = pix < a.M;
+                m0 = mt * kBM;
             } else {
                 const int tw = mt % a.tiles_w;
                 const int t2 = mt / a.tiles_w;
-                const int th = t2 % a.tiles_h;
-                const int n = t2 / a.tiles_h;
-                const int dh = row / a.bw;
-                const int oh = th * a.bh + dh;
-                const int ow = tw * a.bw + (row - dh * a.bw);
-                valid = row < a.bw * a.bh && oh < a.OH && ow < a.OW;
-                pix = ((long long)n * a.OH + oh) * a.OW + ow;
+                oh0 = (t2 % a.tiles_h) * a.bh;
+                n = t2 / a.tiles_h;
+                ow0 = tw * a.bw;
             }
-            if (!valid) continue;
-            __nv_bfloat16 *yrow = a.y + pix * a.Cout;
-            const int co0 = nb * BN + c_base;
+            const uint32_t srow = sOut + (uint32_t)grp * kOutStage + (uint32_t)row * 64u;
+            const uint32_t swz = (uint32_t)((row >> 1) & 3);
 #pragma unroll
-            for (int j = 0; j < kCols / 8; ++j) {
-                const int cj = co0 + 8 * j;
-                if (cj >= a.Cout) break;
-                float v[8];
+            for (int c = 0; c < kCols; c += 32) {
+                const int co = nb * BN + c_base + c;
+                // the previous store from this staging buffer has read it
+                if (issuer) tc::bulk_wait_read0();
+                tc::named_bar_sync(1 + grp, 128);
+                if (co < a.Cout) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(acc[8 * j + e]);
-                if (a.bias) {
-                    const float4 b0 = __ldg(reinterpret_cast<const float4 *>(a.bias + cj));
-                    const float4 b1 = __ldg(reinterpret_cast<const float4 *>(a.bias + cj) + 1);
-                    v[0] += b0.x; v[1] += b0.y; v[2] += b0.z; v[3] += b0.w;
-                    v[4] += b1.x; v[5] += b1.y; v[6] += b1.z; v[7] += b1.w;
+                    for (int j = 0; j < 4; ++j) {
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(acc[c + 8 * j + e]);
+                        if (a.bias && co + 8 * j < a.Cout) {  // Cout % 8 == 0: 8 columns all in or all out
+                            const float4 b0 = __ldg(reinterpret_cast<const float4 *>(a.bias + co + 8 * j));
+                            const float4 b1 = __ldg(reinterpret_cast<const float4 *>(a.bias + co + 8 * j) + 1);
+                            v[0] += b0.x; v[1] += b0.y; v[2] += b0.z; v[3] += b0.w;
+                            v[4] += b1.x; v[5] += b1.y; v[6] += b1.z; v[7] += b1.w;
+                        }
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            __nv_bfloat162 h2 = __floats2bfloat162_rn(activate_fast(v[2 * e], a.act),
+                                                                      activate_fast(v[2 * e + 1], a.act));
+                            pk[e] = *reinterpret_cast<uint32_t *>(&h2);
+                        }
+                        const uint32_t dst = srow + ((((uint32_t)j) ^ swz) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pk[0]),
+                                     "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
+                                     : "memory");
+                    }
                 }
-                uint32_t packed[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    __nv_bfloat162 h2 = __floats2bfloat162_rn(activate_fast(v[2 * e], a.act),
-                                                              activate_fast(v[2 * e + 1], a.act));
-                    packed[e] = *reinterpret_cast<uint32_t *>(&h2);
+                tc::fence_proxy_async_smem();  // staged values visible to the TMA engine
+                tc::named_bar_sync(1 + grp, 128);
+                if (issuer && co < a.Cout) {
+                    const uint32_t src = sOut + (uint32_t)grp * kOutStage;
+                    if (FLAT)
+                        tc::tma_store_2d(&tmY, src, co, m0);
+                    else
+                        tc::tma_store_4d(&tmY, src, co, ow0, oh0, n);
+                    tc::bulk_commit();
                 }
-                *reinterpret_cast<uint4 *>(yrow + cj) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
             }
         }
+        if (issuer) tc::bulk_wait0();  // all of this CTA's stores are complete
     }
 
     // Warps 0 and 1 ran their loops on lane 0 only: reconverge each warp
@@ -415,11 +438,12 @@ int igemm_configure(conv_plan *p) {
     g.num_tiles = g.tiles_n * g.tiles_m;
 
     const int stage_bytes = (kBM + g.bn) * g.bk * 2;
-    const int budget = 227 * 1024 - 1024 - 256;
+    const int out_bytes = epi_groups(g.bn) * kBM * 64;  // epilogue output staging
+    const int budget = 227 * 1024 - 1024 - 256 - out_bytes;
     g.stages = budget / stage_bytes;
     if (g.stages > 8) g.stages = 8;
     if (g.stages < 2) return CONV_ERR_UNSUPPORTED;
-    g.smem = 1024 + g.stages * stage_bytes + 8 * (2 * g.stages + 4) + 16;
+    g.smem = 1024 + g.stages * stage_bytes + out_bytes + 8 * (2 * g.stages + 4) + 16;
     // Ask for more than half of an SM's shared memory so that no two CTAs of
     // this persistent kernel share an SM: each CTA then owns its TMEM
     // columns (2 * BN <= 512) without waiting for another to free them.
@@ -474,6 +498,29 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
         if (rc != CUDA_SUCCESS) return CONV_ERR_CUDA;
     }
 
+    alignas(64) CUtensorMap tmY;
+    {
+        const cuuint32_t box_n = 32;  // 32 output channels (64 bytes) per store box
+        if (g.flat) {
+            const cuuint64_t dims[2] = {(cuuint64_t)p->s.c_out, (cuuint64_t)p->s.n * p->s.h * p->s.w};
+            const cuuint64_t strides[1] = {(cuuint64_t)p->s.c_out * 2};
+            const cuuint32_t box[2] = {box_n, (cuuint32_t)kBM};
+            rc = encode(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, dims, strides, box, ones,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        } else {
+            const cuuint64_t dims[4] = {(cuuint64_t)p->s.c_out, (cuuint64_t)p->ow, (cuuint64_t)p->oh,
+                                        (cuuint64_t)p->s.n};
+            const cuuint64_t strides[3] = {(cuuint64_t)p->s.c_out * 2, (cuuint64_t)p->ow * p->s.c_out * 2,
+                                           (cuuint64_t)p->oh * p->ow * p->s.c_out * 2};
+            const cuuint32_t box[4] = {box_n, (cuuint32_t)g.bw, (cuuint32_t)g.bh, 1};
+            rc = encode(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, y, dims, strides, box, ones,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        }
+        if (rc != CUDA_SUCCESS) return CONV_ERR_CUDA;
+    }
+
     IgArgs a;
     a.H = p->s.h; a.W = p->s.w; a.Cin = p->s.c_in; a.Cout = p->s.c_out; a.KH = p->s.k_h; a.KW = p->s.k_w;
     a.stride = S; a.pad_h = p->pad_h; a.pad_w = p->pad_w; a.OH = p->oh; a.OW = p->ow;
@@ -487,7 +534,7 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
     a.status = p->d_status;
 
     void *k = select_kernel(g.bn, g.bk, g.flat != 0);
-    void *args[] = {&tmA, &tmB, &a};
+    void *args[] = {&tmA, &tmB, &tmY, &a};
     cudaError_t e = cudaLaunchKernel(k, dim3(g.grid), dim3(cta_threads(g.bn)), args, (size_t)g.smem, st);
     return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
