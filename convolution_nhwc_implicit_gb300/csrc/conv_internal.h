@@ -32,6 +32,7 @@ struct IgemmGeom {
     int grid;      // persistent CTAs
     int smem;      // dynamic shared memory bytes
     int in_i8;     // operands are int8 (converted to bf16 on chip)
+    int swap;      // 1: MMA M = output channels, N = 256 pixels (Cout <= 128)
 };
 
 struct DwGeom {

@@ -49,17 +49,20 @@ using namespace convk;
 
 namespace {
 
-constexpr int kBM = 128;
+constexpr int kBM = 128;     // output pixels per tile (normal mode)
+constexpr int kBMSwap = 256; // output pixels per tile (swapped mode)
+constexpr int kTP = 272;     // swapped-mode transpose rows: 128 bf16 channels + 16 bytes of padding
 
-// Epilogue warpgroups per CTA: each takes BN / groups columns of every tile.
-__host__ __device__ constexpr int epi_groups(int bn) { return bn >= 128 ? 4 : 2; }
+// Epilogue warpgroups per CTA: each takes a slice of every tile's columns.
+__host__ __device__ constexpr int epi_groups(int bn, bool swap) { return swap ? 4 : (bn >= 128 ? 4 : 2); }
 // Threads per CTA: the TMA warp, the MMA warp and the epilogue warpgroups.
-__host__ __device__ constexpr int cta_threads(int bn) { return 64 + 128 * epi_groups(bn); }
+__host__ __device__ constexpr int cta_threads(int bn, bool swap) { return 64 + 128 * epi_groups(bn, swap); }
 
 struct IgArgs {
     int H, W, Cin, Cout, KH, KW, stride, pad_h, pad_w, OH, OW;
     int bw, bh, tiles_w, tiles_h, tiles_n, num_tiles, cblocks, kblocks, stages;
     long long M;         // flat mode: rows of x viewed as [N*H*W, Cin]
+    int flat;
     uint32_t a_bytes;    // bytes TMA writes per A box
     int act;
     const float *bias;
@@ -86,19 +89,91 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     }
 }
 
-template <int BN, int BK, bool FLAT>
-__global__ void __launch_bounds__(cta_threads(BN), 1)
+// Epilogue of the swapped mode for one tile.  The accumulator is D[co][px]:
+// thread `row` of the group holds output channel co = nb*128 + row and reads
+// the group's kCols pixel columns 16 at a time.  Each 16-pixel chunk goes
+// through shared memory (rows of 128 channels, padded to kTP bytes) to turn
+// channel-per-thread values into pixel rows, which the group then writes
+// with 16-byte stores (eight threads cover one pixel's 128 channels).
+template <int kCols>
+__device__ __forceinline__ void epilogue_swapped(const IgArgs &a, int tile, uint32_t taddr, uint32_t tempty,
+                                                 int row, int grp, int c_base, uint8_t *tbuf, int gt) {
+    const int nb = tile % a.tiles_n;
+    const int mt = tile / a.tiles_n;
+    const int co = nb * 128 + row;
+    const float bias = (a.bias && co < a.Cout) ? __ldg(a.bias + co) : 0.0f;
+    // Pull the whole slice out of TMEM first and hand the buffer back.
+    uint32_t acc[kCols];
+#pragma unroll
+    for (int c = 0; c < kCols; c += 16) tc::tmem_ld_32x16(taddr + (uint32_t)c, *reinterpret_cast<uint32_t(*)[16]>(acc + c));
+    tc::tmem_ld_wait();
+    tc::fence_before_sync();
+    tc::mbar_arrive(tempty);
+
+    int n = 0, oh0 = 0, ow0 = 0;
+    long long m0 = 0;
+    if (a.flat) {
+        m0 = (long long)mt * kBMSwap;
+    } else {
+        const int tw = mt % a.tiles_w;
+        const int t2 = mt / a.tiles_w;
+        oh0 = (t2 % a.tiles_h) * a.bh;
+        n = t2 / a.tiles_h;
+        ow0 = tw * a.bw;
+    }
+    // this thread's part of the write-out: pixel gt / 8 of the chunk, channels (gt % 8) * 16 .. + 15
+    const int wpx = gt >> 3;
+    const int wco = nb * 128 + (gt & 7) * 16;
+#pragma unroll
+    for (int c = 0; c < kCols; c += 16) {
+        tc::named_bar_sync(1 + grp, 128);  // the previous chunk's rows have been read
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const __nv_bfloat16 h = __float2bfloat16_rn(activate_fast(__uint_as_float(acc[c + i]) + bias, a.act));
+            *reinterpret_cast<__nv_bfloat16 *>(tbuf + i * kTP + row * 2) = h;
+        }
+        tc::named_bar_sync(1 + grp, 128);
+        const int p = c_base + c + wpx;  // pixel index inside the tile
+        long long pix;
+        bool valid;
+        if (a.flat) {
+            pix = m0 + p;
+            valid = pix < a.M;
+        } else {
+            const int dh = p / a.bw;
+            const int oh = oh0 + dh, ow = ow0 + (p - dh * a.bw);
+            valid = p < a.bw * a.bh && oh < a.OH && ow < a.OW;
+            pix = ((long long)n * a.OH + oh) * a.OW + ow;
+        }
+        if (valid) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(tbuf + wpx * kTP + (gt & 7) * 32);
+            __nv_bfloat16 *dst = a.y + pix * a.Cout + wco;
+            if (wco < a.Cout) *reinterpret_cast<uint4 *>(dst) = src[0];
+            if (wco + 8 < a.Cout) *reinterpret_cast<uint4 *>(dst + 8) = src[1];
+        }
+    }
+}
+
+// SWAP = false: MMA M = 128 pixels, N = BN output channels (D[pixel][co]).
+// SWAP = true (layers with Cout <= 128): the operands trade places, MMA M =
+// 128 output channels (weights as A), N = 256 pixels (activations as B),
+// D[co][pixel]; every MMA then has N = 256, the only width at which tcgen05
+// reaches its peak rate (the issue cost of an MMA does not shrink with N).
+template <int BN, int BK, bool FLAT, bool SWAP>
+__global__ void __launch_bounds__(cta_threads(BN, SWAP), 1)
 igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmY, const IgArgs a) {
+    constexpr int kPix = SWAP ? kBMSwap : kBM;  // pixel rows of a tile
+    constexpr int kAcc = SWAP ? kBMSwap : BN;   // accumulator columns of a tile
     constexpr uint32_t kRowBytes = BK * 2;
-    constexpr uint32_t kAStage = kBM * BK * 2;
-    constexpr uint32_t kBStage = BN * BK * 2;
-    constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators of BN fp32 columns
-    constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kBM, BN);
-    constexpr int kGroups = epi_groups(BN);
-    constexpr int kCols = BN / kGroups;  // accumulator columns per epilogue thread (32 or 64)
-    static_assert(kCols % 32 == 0, "epilogue reads TMEM 32 columns at a time");
-    constexpr uint32_t kOutStage = kBM * 64;  // 128 rows x 32 bf16 columns
+    constexpr uint32_t kAStage = kPix * BK * 2;  // activation (pixel) tile
+    constexpr uint32_t kBStage = BN * BK * 2;    // weight tile
+    constexpr uint32_t kTmemCols = 2 * kAcc;     // two accumulators
+    constexpr uint32_t kIdesc = SWAP ? tc::idesc_bf16_f32(128, kBMSwap) : tc::idesc_bf16_f32(kBM, BN);
+    constexpr int kGroups = epi_groups(BN, SWAP);
+    constexpr int kCols = kAcc / kGroups;  // accumulator columns per epilogue thread
+    static_assert(SWAP ? (BN == 128 && kCols % 16 == 0) : (kCols % 32 == 0), "epilogue column slices");
+    constexpr uint32_t kOutStage = SWAP ? 16 * kTP : kBM * 64;  // per group: transpose rows / store staging
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
@@ -158,7 +233,7 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 int n = 0, oh0 = 0, ow0 = 0;
                 int m0 = 0;
                 if (FLAT) {
-                    m0 = mt * kBM;
+                    m0 = mt * kPix;
                 } else {
                     const int tw = mt % a.tiles_w;
                     const int t2 = mt / a.tiles_w;
@@ -204,7 +279,7 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                   KSTATUS_TIMEOUT_MMA))
                     break;
                 tc::fence_after_sync();
-                const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+                const uint32_t d = tmem_base + (uint32_t)(buf * kAcc);
                 for (int kb = 0; kb < a.kblocks; ++kb) {
                     if (!wait_bounded(full_bar(stage), phase, abort_flag, a.status, KSTATUS_TIMEOUT_MMA)) {
                         ok = false;
@@ -215,9 +290,12 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const uint32_t bS = sB + stage * kBStage;
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        const uint64_t ad = tc::smem_desc_kmajor(aS + 32u * k, kRowBytes);
-                        const uint64_t bd = tc::smem_desc_kmajor(bS + 32u * k, kRowBytes);
-                        tc::mma_bf16(d, ad, bd, kIdesc, (kb | k) != 0 ? 1u : 0u);
+                        const uint64_t pd = tc::smem_desc_kmajor(aS + 32u * k, kRowBytes);  // pixels
+                        const uint64_t wd = tc::smem_desc_kmajor(bS + 32u * k, kRowBytes);  // weights
+                        if (SWAP)
+                            tc::mma_bf16(d, wd, pd, kIdesc, (kb | k) != 0 ? 1u : 0u);
+                        else
+                            tc::mma_bf16(d, pd, wd, kIdesc, (kb | k) != 0 ? 1u : 0u);
                     }
                     tc::mma_commit(empty_bar(stage));  // stage free once these MMAs complete
                     if (++stage == stages) { stage = 0; phase ^= 1u; }
@@ -244,6 +322,12 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             __syncwarp();  // tcgen05.ld below is warp-collective (.sync.aligned)
             if (!__all_sync(0xffffffffu, got)) break;
             tc::fence_after_sync();
+            if constexpr (SWAP) {
+                epilogue_swapped<kCols>(a, tile, tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kAcc + c_base),
+                                        tempty_bar(buf), row, grp, c_base, gbase + (sOut - base) + grp * kOutStage,
+                                        threadIdx.x - 64 - grp * 128);
+                continue;
+            }
             // Move this thread's slice of the accumulator into registers, then
             // hand the TMEM buffer back to the MMA warp before doing the math.
             uint32_t acc[kCols];
@@ -264,7 +348,7 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const int mt = tile / a.tiles_n;
             int n = 0, oh0 = 0, ow0 = 0, m0 = 0;
             if (FLAT) {
-                m0 = mt * kBM;
+                m0 = mt * kPix;
             } else {
                 const int tw = mt % a.tiles_w;
                 const int t2 = mt / a.tiles_w;
@@ -352,14 +436,14 @@ CUtensorMapSwizzle swizzle_for(int bk) {
     return bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : (bk == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
 }
 
-template <int BN, int BK, bool FLAT>
+template <int BN, int BK, bool FLAT, bool SWAP>
 void *kernel_ptr() {
-    return reinterpret_cast<void *>(&igemm_bf16_kernel<BN, BK, FLAT>);
+    return reinterpret_cast<void *>(&igemm_bf16_kernel<BN, BK, FLAT, SWAP>);
 }
 
 template <int BN, int BK>
 void *kernel_ptr_flat(bool flat) {
-    return flat ? kernel_ptr<BN, BK, true>() : kernel_ptr<BN, BK, false>();
+    return flat ? kernel_ptr<BN, BK, true, false>() : kernel_ptr<BN, BK, false, false>();
 }
 
 template <int BN>
@@ -371,7 +455,19 @@ void *kernel_ptr_bk(int bk, bool flat) {
     }
 }
 
-void *select_kernel(int bn, int bk, bool flat) {
+template <int BK>
+void *kernel_ptr_swap(bool flat) {
+    return flat ? kernel_ptr<128, BK, true, true>() : kernel_ptr<128, BK, false, true>();
+}
+
+void *select_kernel(int bn, int bk, bool flat, bool swap) {
+    if (swap) {
+        switch (bk) {
+        case 64: return kernel_ptr_swap<64>(flat);
+        case 32: return kernel_ptr_swap<32>(flat);
+        default: return kernel_ptr_swap<16>(flat);
+        }
+    }
     switch (bn) {
     case 256: return kernel_ptr_bk<256>(bk, flat);
     case 128: return kernel_ptr_bk<128>(bk, flat);
@@ -400,19 +496,24 @@ int igemm_configure(conv_plan *p) {
     g.cblocks = p->s.c_in / g.bk;
     g.kblocks = p->s.k_h * p->s.k_w * g.cblocks;
 
+    // Layers with at most 128 output channels run with the operands swapped:
+    // 256-pixel tiles as the MMA's N (full-rate MMAs) and the weights as M.
+    g.swap = p->s.c_out <= 128 ? 1 : 0;
+    const int P = g.swap ? kBMSwap : kBM;  // pixels per tile
+
     // M tiling.
     if (g.flat) {
         const long long M = (long long)p->s.n * p->s.h * p->s.w;
-        g.bw = kBM; g.bh = 1;
+        g.bw = P; g.bh = 1;
         g.tiles_w = 1; g.tiles_h = 1;
-        g.tiles_m = (int)((M + kBM - 1) / kBM);
+        g.tiles_m = (int)((M + P - 1) / P);
     } else {
         // Smallest number of bh x bw rectangles covering the output; among
         // equal counts, the widest (longest contiguous NHWC runs).
         long long best = -1;
-        for (int bw = 1; bw <= kBM && bw <= p->ow * 2; ++bw) {
+        for (int bw = 1; bw <= P && bw <= p->ow * 2; ++bw) {
             if (bw * S > 256) break;
-            int bh = kBM / bw;
+            int bh = P / bw;
             if (bh > p->oh) bh = p->oh;
             while (bh * S > 256) --bh;
             if (bh < 1) continue;
@@ -426,19 +527,25 @@ int igemm_configure(conv_plan *p) {
         g.tiles_m = g.tiles_w * g.tiles_h * p->s.n;
     }
 
-    // N tile: estimated time ~ waves x (BN + fixed per-tile cost).
-    long long best_cost = -1;
-    for (int bn : {256, 128, 64}) {
-        const long long tn = (p->s.c_out + bn - 1) / bn;
-        const long long tiles = tn * g.tiles_m;
-        const long long waves = (tiles + p->num_sms - 1) / p->num_sms;
-        const long long cost = waves * (bn + 48);
-        if (best_cost < 0 || cost < best_cost) { best_cost = cost; g.bn = bn; g.tiles_n = (int)tn; }
+    if (g.swap) {
+        g.bn = 128;
+        g.tiles_n = 1;
+    } else {
+        // N tile: an MMA costs about the same for any N <= 256, so wider tiles
+        // are cheaper per output; estimated time ~ waves x (BN + fixed cost).
+        long long best_cost = -1;
+        for (int bn : {256, 128, 64}) {
+            const long long tn = (p->s.c_out + bn - 1) / bn;
+            const long long tiles = tn * g.tiles_m;
+            const long long waves = (tiles + p->num_sms - 1) / p->num_sms;
+            const long long cost = waves * (bn + 48);
+            if (best_cost < 0 || cost < best_cost) { best_cost = cost; g.bn = bn; g.tiles_n = (int)tn; }
+        }
     }
     g.num_tiles = g.tiles_n * g.tiles_m;
 
-    const int stage_bytes = (kBM + g.bn) * g.bk * 2;
-    const int out_bytes = epi_groups(g.bn) * kBM * 64;  // epilogue output staging
+    const int stage_bytes = (P + g.bn) * g.bk * 2;
+    const int out_bytes = g.swap ? 4 * 16 * kTP : epi_groups(g.bn, false) * kBM * 64;  // epilogue staging
     const int budget = 227 * 1024 - 1024 - 256 - out_bytes;
     g.stages = budget / stage_bytes;
     if (g.stages > 8) g.stages = 8;
@@ -446,16 +553,17 @@ int igemm_configure(conv_plan *p) {
     g.smem = 1024 + g.stages * stage_bytes + out_bytes + 8 * (2 * g.stages + 4) + 16;
     // Ask for more than half of an SM's shared memory so that no two CTAs of
     // this persistent kernel share an SM: each CTA then owns its TMEM
-    // columns (2 * BN <= 512) without waiting for another to free them.
+    // columns (at most 512) without waiting for another to free them.
     if (g.smem < 116 * 1024) g.smem = 116 * 1024;
     g.grid = g.num_tiles < p->num_sms ? g.num_tiles : p->num_sms;
 
     if (!tensor_map_encoder()) return CONV_ERR_CUDA;
-    const int rc = conv_grant_smem(select_kernel(g.bn, g.bk, g.flat != 0), p->device, g.smem);
+    const int rc = conv_grant_smem(select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0), p->device, g.smem);
     if (rc != CONV_OK) return rc;
     snprintf(p->desc, sizeof(p->desc),
-             "igemm_bf16_tcgen05 %s BM=128 BN=%d BK=%d tile=%dx%d stages=%d tiles=%d grid=%d",
-             g.flat ? "flat" : "spatial", g.bn, g.bk, g.bh, g.bw, g.stages, g.num_tiles, g.grid);
+             "igemm_bf16_tcgen05 %s%s %s BK=%d tile=%dx%d stages=%d tiles=%d grid=%d", g.flat ? "flat" : "spatial",
+             g.swap ? " swapped" : "", g.swap ? "M=128co N=256px" : (g.bn == 256 ? "M=128px N=256co" : (g.bn == 128 ? "M=128px N=128co" : "M=128px N=64co")),
+             g.bk, g.bh, g.bw, g.stages, g.num_tiles, g.grid);
     return CONV_OK;
 }
 
@@ -471,7 +579,7 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
     if (g.flat) {
         const cuuint64_t dims[2] = {(cuuint64_t)p->s.c_in, (cuuint64_t)p->s.n * p->s.h * p->s.w};
         const cuuint64_t strides[1] = {(cuuint64_t)p->s.c_in * 2};
-        const cuuint32_t box[2] = {(cuuint32_t)g.bk, (cuuint32_t)kBM};
+        const cuuint32_t box[2] = {(cuuint32_t)g.bk, (cuuint32_t)(g.swap ? kBMSwap : kBM)};
         rc = encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims, strides, box, ones,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(g.bk), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -504,7 +612,7 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
         if (g.flat) {
             const cuuint64_t dims[2] = {(cuuint64_t)p->s.c_out, (cuuint64_t)p->s.n * p->s.h * p->s.w};
             const cuuint64_t strides[1] = {(cuuint64_t)p->s.c_out * 2};
-            const cuuint32_t box[2] = {box_n, (cuuint32_t)kBM};
+            const cuuint32_t box[2] = {box_n, (cuuint32_t)(g.swap ? kBMSwap : kBM)};
             rc = encode(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, dims, strides, box, ones,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -527,14 +635,16 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
     a.bw = g.bw; a.bh = g.bh; a.tiles_w = g.tiles_w; a.tiles_h = g.tiles_h; a.tiles_n = g.tiles_n;
     a.num_tiles = g.num_tiles; a.cblocks = g.cblocks; a.kblocks = g.kblocks; a.stages = g.stages;
     a.M = (long long)p->s.n * p->s.h * p->s.w;
-    a.a_bytes = (uint32_t)((g.flat ? kBM : g.bw * g.bh) * g.bk * 2);
+    a.a_bytes = (uint32_t)((g.flat ? (g.swap ? kBMSwap : kBM) : g.bw * g.bh) * g.bk * 2);
+    a.flat = g.flat;
     a.act = (int)p->act;
     a.bias = (const float *)bias;
     a.y = (__nv_bfloat16 *)y;
     a.status = p->d_status;
 
-    void *k = select_kernel(g.bn, g.bk, g.flat != 0);
+    void *k = select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0);
     void *args[] = {&tmA, &tmB, &tmY, &a};
-    cudaError_t e = cudaLaunchKernel(k, dim3(g.grid), dim3(cta_threads(g.bn)), args, (size_t)g.smem, st);
+    cudaError_t e =
+        cudaLaunchKernel(k, dim3(g.grid), dim3(cta_threads(g.bn, g.swap != 0)), args, (size_t)g.smem, st);
     return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
