@@ -335,9 +335,11 @@ def oracle_sample(layers, budget_s, seed=0):
     for d in layers:
         s = d.spec
         if s.dtype == "i8":
-            raise NotImplementedError("bench workloads are float")
-        prepared.append((s, d.x.double().numpy(), d.w.double().numpy(),
-                         None if d.b is None else d.b.double().numpy()))
+            M = oracle.requant_multipliers(s.in_scale, s.out_scale, d.w_scales.numpy())
+            prepared.append((s, d.x.numpy(), d.w.numpy(), None if d.b is None else d.b.numpy(), M))
+        else:
+            prepared.append((s, d.x.double().numpy(), d.w.double().numpy(),
+                             None if d.b is None else d.b.double().numpy(), None))
     rng = np.random.default_rng(seed)
 
     def pts_for(s, count):
@@ -347,13 +349,16 @@ def oracle_sample(layers, budget_s, seed=0):
 
     def run(frac):
         fl, secs, npts = 0.0, 0.0, 0
-        for s, x, w, b in prepared:
+        for s, x, w, b, M in prepared:
             oh, ow = output_hw(s)
             total = s.n * oh * ow * s.cout
             count = max(16, int(total * frac))
             pts = pts_for(s, count)
             t0 = time.perf_counter()
-            oracle.conv_f64_points(x, w, b, pts, s.stride, s.pad_h, s.pad_w, s.groups, s.act)
+            if M is not None:
+                oracle.conv_i8_points(x, w, b, M, pts, s.stride, s.pad_h, s.pad_w, s.groups, s.act == "relu")
+            else:
+                oracle.conv_f64_points(x, w, b, pts, s.stride, s.pad_h, s.pad_w, s.groups, s.act)
             secs += time.perf_counter() - t0
             fl += 2.0 * macs(s) * count / total
             npts += count

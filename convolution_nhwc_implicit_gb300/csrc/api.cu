@@ -209,8 +209,13 @@ int conv_plan_create_ex(const conv_shape_t *shape, int stride, int pad_h, int pa
                  dtype == CONV_F32 ? "f32" : (dtype == CONV_BF16 ? "bf16" : "i8"), p->dw.th, p->dw.tw,
                  p->dw.cbv * (dtype == CONV_I8 ? 16 : 4), p->dw.hin, p->dw.win, p->dw.threads, p->dw.blocks);
     } else {
-        snprintf(p->desc, sizeof(p->desc), "direct %s",
-                 dtype == CONV_F32 ? "f32-ffma" : (dtype == CONV_BF16 ? "bf16-ffma" : "i8-dp4a"));
+        direct_configure(p);
+        if (p->dct > 0)
+            snprintf(p->desc, sizeof(p->desc), "direct %s smem-weights co/thread=%d px/thread=%d",
+                     dtype == CONV_F32 ? "f32-ffma" : "bf16-ffma", p->dct, p->dpt);
+        else
+            snprintf(p->desc, sizeof(p->desc), "direct %s",
+                     dtype == CONV_F32 ? "f32-ffma" : (dtype == CONV_BF16 ? "bf16-ffma" : "i8-dp4a"));
     }
     *out_plan = p;
     return CONV_OK;

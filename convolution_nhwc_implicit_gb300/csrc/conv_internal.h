@@ -59,6 +59,7 @@ struct conv_plan {
     int *d_status;     // device status word (bounded-wait timeouts)
     IgemmGeom ig;
     DwGeom dw;
+    int dct, dpt;      // direct kernel: channels / pixels per thread of the smem variant (dct 0: generic)
     char desc[192];
 };
 
@@ -76,6 +77,7 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
 
 // Plan-time helpers of each family.
 bool direct_supported(const conv_plan *p);
+void direct_configure(conv_plan *p);
 bool dw3x3_supported(const conv_plan *p);
 int dw3x3_configure(conv_plan *p);  // CONV_* status
 bool igemm_supported(const conv_plan *p);

@@ -142,6 +142,117 @@ direct_conv_i8(DirectArgs a, const int8_t *__restrict__ x, const int8_t *__restr
     }
 }
 
+// ---------------------------------------------------------------------------
+// Direct convolution with the weights staged in shared memory (fp32 / bf16).
+// A CTA owns one chunk of CT output channels of one group and 128 * PT
+// output pixels; its weights are staged once as fp32 [K][CT] (K = k_h * k_w
+// * Cin/groups).  A thread owns PT pixels x CT channels: per reduction step
+// it loads one input value per pixel and reads the CT weights as shared-
+// memory broadcasts (every thread of the CTA reads the same row), then issues
+// CT FMAs per pixel.  Used for layers the tensor-core path
+// does not take: fp32 layers, Cin = 1 or 3 stems, grouped layers.
+constexpr int kDThreads = 128;
+constexpr int kDMaxSmemFloats = 12288;  // 48 KB of staged weights
+
+template <typename T> struct Out;
+template <> struct Out<float> {
+    __device__ static __forceinline__ float act(float v, int a) { return activate(v, a); }
+};
+template <> struct Out<__nv_bfloat16> {
+    __device__ static __forceinline__ float act(float v, int a) { return activate_fast(v, a); }
+};
+
+template <typename T, int CT, int PT>
+__global__ void __launch_bounds__(kDThreads)
+direct_conv_smem(DirectArgs a, int chunks_per_group, const T *__restrict__ x, const T *__restrict__ w,
+                 const float *__restrict__ bias, T *__restrict__ y) {
+    extern __shared__ __align__(16) float wsm[];  // [K][CT]
+    const int K = a.KH * a.KW * a.cin_g;
+    const int g = blockIdx.y / chunks_per_group;
+    const int cc = blockIdx.y - g * chunks_per_group;
+    const int co0 = g * a.cout_g + cc * CT;
+    const int nco = min(CT, a.cout_g - cc * CT);
+    // Stage this chunk's weights as [K][CT]: consecutive threads write
+    // consecutive channels of one k (no bank conflicts); the strided global
+    // reads hit the same few lines of w for all threads of a warp.
+    for (int i = threadIdx.x; i < K * CT; i += kDThreads) {
+        const int k = i / CT, j = i - k * CT;
+        wsm[i] = j < nco ? Elem<T>::to_f(__ldg(w + (long long)(co0 + j) * K + k)) : 0.0f;
+    }
+    __syncthreads();
+
+    const int g0 = g * a.cin_g;
+    long long pix[PT];
+    int ihb[PT], iwb[PT], nn[PT];
+    bool pv[PT];
+#pragma unroll
+    for (int i = 0; i < PT; ++i) {
+        pix[i] = ((long long)blockIdx.x * PT + i) * kDThreads + threadIdx.x;
+        pv[i] = pix[i] < a.npix;
+        const long long pp = pv[i] ? pix[i] : 0;
+        const int ow = (int)(pp % a.OW);
+        const long long t = pp / a.OW;
+        const int oh = (int)(t % a.OH);
+        nn[i] = (int)(t / a.OH);
+        ihb[i] = oh * a.stride - a.pad_h;
+        iwb[i] = ow * a.stride - a.pad_w;
+    }
+    float acc[PT][CT];
+#pragma unroll
+    for (int i = 0; i < PT; ++i)
+#pragma unroll
+        for (int j = 0; j < CT; ++j) acc[i][j] = 0.0f;
+
+    for (int r = 0; r < a.KH; ++r) {
+        for (int s = 0; s < a.KW; ++s) {
+            const T *xp[PT];
+            bool ok[PT];
+#pragma unroll
+            for (int i = 0; i < PT; ++i) {
+                const int ih = ihb[i] + r, iw = iwb[i] + s;
+                ok[i] = pv[i] && ih >= 0 && ih < a.H && iw >= 0 && iw < a.W;  // zero padding
+                xp[i] = x + (((long long)nn[i] * a.H + (ok[i] ? ih : 0)) * a.W + (ok[i] ? iw : 0)) * a.Cin + g0;
+            }
+            const float *wrow = wsm + (r * a.KW + s) * a.cin_g * CT;
+            for (int ci = 0; ci < a.cin_g; ++ci, wrow += CT) {
+                float xv[PT];
+#pragma unroll
+                for (int i = 0; i < PT; ++i) xv[i] = ok[i] ? Elem<T>::to_f(__ldg(xp[i] + ci)) : 0.0f;
+#pragma unroll
+                for (int j = 0; j < CT; j += 4) {
+                    const float4 w4 = *reinterpret_cast<const float4 *>(wrow + j);
+#pragma unroll
+                    for (int i = 0; i < PT; ++i) {
+                        acc[i][j] = __fmaf_rn(xv[i], w4.x, acc[i][j]);
+                        acc[i][j + 1] = __fmaf_rn(xv[i], w4.y, acc[i][j + 1]);
+                        acc[i][j + 2] = __fmaf_rn(xv[i], w4.z, acc[i][j + 2]);
+                        acc[i][j + 3] = __fmaf_rn(xv[i], w4.w, acc[i][j + 3]);
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < PT; ++i) {
+        if (!pv[i]) continue;
+        T *yp = y + pix[i] * a.Cout + co0;
+        T out[CT];
+#pragma unroll
+        for (int j = 0; j < CT; ++j)
+            out[j] = Elem<T>::from_f(Out<T>::act(acc[i][j] + (bias && j < nco ? __ldg(bias + co0 + j) : 0.0f), a.act));
+        const bool vec = nco == CT && ((reinterpret_cast<uintptr_t>(yp) & 15) == 0) && (CT * sizeof(T)) % 16 == 0;
+        if (vec) {
+#pragma unroll
+            for (int j = 0; j < CT; j += 16 / (int)sizeof(T))
+                *reinterpret_cast<uint4 *>(yp + j) = *reinterpret_cast<const uint4 *>(out + j);
+        } else {
+#pragma unroll
+            for (int j = 0; j < CT; ++j)
+                if (j < nco) yp[j] = out[j];
+        }
+    }
+}
+
 DirectArgs make_args(const conv_plan *p) {
     DirectArgs a;
     a.N = p->s.n; a.H = p->s.h; a.W = p->s.w; a.Cin = p->s.c_in; a.Cout = p->s.c_out;
@@ -155,7 +266,61 @@ DirectArgs make_args(const conv_plan *p) {
     return a;
 }
 
+template <typename T, int CT>
+void *smem_kernel_pt(int pt) {
+    return pt == 2 ? reinterpret_cast<void *>(&direct_conv_smem<T, CT, 2>)
+                   : reinterpret_cast<void *>(&direct_conv_smem<T, CT, 1>);
+}
+
+template <typename T>
+void *smem_kernel(int ct, int pt) {
+    switch (ct) {
+    case 32: return smem_kernel_pt<T, 32>(pt);
+    case 16: return smem_kernel_pt<T, 16>(pt);
+    case 8: return smem_kernel_pt<T, 8>(pt);
+    default: return smem_kernel_pt<T, 4>(pt);
+    }
+}
+
+template <typename T>
+cudaError_t launch_smem(const conv_plan *p, DirectArgs a, const void *x, const void *w, const void *bias, void *y,
+                        cudaStream_t st) {
+    const int ct = p->dct, pt = p->dpt;
+    const int chunks = (a.cout_g + ct - 1) / ct;
+    const int K = a.KH * a.KW * a.cin_g;
+    dim3 grid((unsigned)((a.npix + (long long)kDThreads * pt - 1) / ((long long)kDThreads * pt)),
+              (unsigned)(p->groups * chunks));
+    void *k = smem_kernel<T>(ct, pt);
+    void *args[] = {&a, (void *)&chunks, (void *)&x, (void *)&w, (void *)&bias, &y};
+    return cudaLaunchKernel(k, grid, dim3(kDThreads), args, (size_t)K * ct * sizeof(float), st);
+}
+
 }  // namespace
+
+void direct_configure(conv_plan *p) {
+    // Shared-memory variant for float layers whose staged weights fit: the
+    // widest channel chunk (<= 32, covering the group) whose K x CT floats fit.
+    p->dct = 0;
+    p->dpt = 1;
+    if (p->dtype == CONV_I8) return;
+    const int cout_g = p->s.c_out / p->groups;
+    const long long K = (long long)p->s.k_h * p->s.k_w * (p->s.c_in / p->groups);
+    int ct = 32;
+    while (ct > 4 && ct / 2 >= cout_g) ct /= 2;  // no wider than the group needs
+    while (ct >= 4 && K * ct > kDMaxSmemFloats) ct /= 2;
+    if (ct < 4) return;
+    const long long npix = (long long)p->s.n * p->oh * p->ow;
+    // Small layers: narrower chunks until the grid has a few CTAs per SM.
+    while (ct > 4 && ((npix + kDThreads - 1) / kDThreads) * p->groups * ((cout_g + ct - 1) / ct) <
+                         (long long)p->num_sms * 4)
+        ct /= 2;
+    const long long chunks = (long long)p->groups * ((cout_g + ct - 1) / ct);
+    if (chunks > 65535) return;
+    p->dct = ct;
+    // Two pixels per thread when there are threads to spare: weight rows are
+    // then read once for two pixels.
+    p->dpt = npix * chunks >= (long long)p->num_sms * kDThreads * 16 ? 2 : 1;
+}
 
 bool direct_supported(const conv_plan *p) {
     const int cout_g = p->s.c_out / p->groups;
@@ -170,10 +335,12 @@ cudaError_t launch_direct(const conv_plan *p, const void *x, const void *w, cons
     dim3 grid((unsigned)((a.npix + kThreads - 1) / kThreads), (unsigned)(p->groups * a.chunks_per_group));
     switch (p->dtype) {
     case CONV_F32:
+        if (p->dct > 0) return launch_smem<float>(p, a, x, w, bias, y, st);
         direct_conv_float<float><<<grid, kThreads, 0, st>>>(
             a, (const float *)x, (const float *)w, (const float *)bias, (float *)y);
         break;
     case CONV_BF16:
+        if (p->dct > 0) return launch_smem<__nv_bfloat16>(p, a, x, w, bias, y, st);
         direct_conv_float<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
             a, (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)w, (const float *)bias,
             (__nv_bfloat16 *)y);

@@ -457,11 +457,15 @@ int dw3x3_configure(conv_plan *p) {
     // columns too), then the most threads.
     int best_tw = 1, best_cbv = 1;
     long long best_cost = -1;
+    // Enough tiles to give every SM two CTAs, if the layer allows.
+    const long long rows_tiles = (long long)p->s.n * ((p->oh + kMaxTh - 1) / kMaxTh);
     for (int cbv : {32, 16, 8, 4, 2, 1}) {
         if (cbv > maxv || cbv > cvt || cvt % cbv != 0) continue;
         for (int tw = 1; tw * cbv <= 256 && (tw - 1) * S + 3 <= 256; ++tw) {
             const long long tiles = (p->ow + tw - 1) / tw;
-            const long long cost = tiles * ((tw - 1) * S + 3) * (cvt / cbv);
+            long long cost = tiles * ((tw - 1) * S + 3) * (cvt / cbv);
+            if (tiles * (cvt / cbv) * rows_tiles < (long long)p->num_sms * 2 && tw * cbv > 32)
+                cost = cost * 4;  // too few CTAs to keep the GPU busy
             const bool better = best_cost < 0 || cost < best_cost ||
                                 (cost == best_cost && tw * cbv > best_tw * best_cbv);
             if (better) { best_cost = cost; best_tw = tw; best_cbv = cbv; }

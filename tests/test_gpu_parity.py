@@ -59,6 +59,9 @@ IGEMM = [
     L("3x3_no_bias", 1, 11, 11, 64, 64, 3, 3, 1, 1, 1, b_dist=None),
     L("7x7_s2_p3", 1, 30, 30, 32, 64, 7, 7, 2, 3, 3),
     L("3x3_single_pixel", 1, 1, 1, 64, 64, 3, 3, 1, 1, 1),
+    L("ragged_cout_two_ntiles", 1, 12, 12, 128, 320, 3, 3, 1, 1, 1),
+    L("1x1_flat_long_k", 2, 8, 8, 512, 384, 1, 1, act="relu"),
+    L("3x3_s2_few_tiles", 1, 20, 20, 256, 512, 3, 3, 2, 1, 1),
 ]
 
 
