@@ -136,7 +136,7 @@ int conv_plan_create_ex(const conv_shape_t *shape, int stride, int pad_h, int pa
     if (!out_plan) return CONV_ERR_NULL_ARG;
     *out_plan = nullptr;
     if (!shape) return CONV_ERR_NULL_ARG;
-    if ((int)algo < CONV_ALGO_AUTO || (int)algo > CONV_ALGO_IGEMM) return CONV_ERR_INVALID_ARG;
+    if ((int)algo < CONV_ALGO_AUTO || (int)algo > CONV_ALGO_IGEMM_N64) return CONV_ERR_INVALID_ARG;
     int oh = 0, ow = 0;
     int rc = validate(shape, stride, pad_h, pad_w, groups, dtype, act, quant, &oh, &ow);
     if (rc != CONV_OK) return rc;
@@ -165,7 +165,7 @@ int conv_plan_create_ex(const conv_shape_t *shape, int stride, int pad_h, int pa
     int chosen = -1;
     if (algo == CONV_ALGO_AUTO)
         chosen = can_ig ? CONV_ALGO_IGEMM : (can_dw ? CONV_ALGO_DEPTHWISE : (can_direct ? CONV_ALGO_DIRECT : -1));
-    else if (algo == CONV_ALGO_IGEMM && can_ig) chosen = CONV_ALGO_IGEMM;
+    else if (algo >= CONV_ALGO_IGEMM && can_ig) chosen = CONV_ALGO_IGEMM;
     else if (algo == CONV_ALGO_DEPTHWISE && can_dw) chosen = CONV_ALGO_DEPTHWISE;
     else if (algo == CONV_ALGO_DIRECT && can_direct) chosen = CONV_ALGO_DIRECT;
     if (chosen < 0) {
@@ -200,7 +200,8 @@ int conv_plan_create_ex(const conv_shape_t *shape, int stride, int pad_h, int pa
     }
 
     if (chosen == CONV_ALGO_IGEMM) {
-        rc = igemm_configure(p);
+        // tile layout: 0 = estimated fastest, else swapped / N256 / N128 / N64
+        rc = igemm_configure(p, algo >= CONV_ALGO_IGEMM_SWAPPED ? (int)algo - CONV_ALGO_IGEMM_SWAPPED + 1 : 0);
         if (rc != CONV_OK) { conv_plan_destroy(p); return rc; }
     } else if (chosen == CONV_ALGO_DEPTHWISE) {
         rc = dw3x3_configure(p);
@@ -231,6 +232,8 @@ void conv_plan_destroy(conv_plan_t *plan) {
     if (!plan) return;
     if (plan->d_status) cudaFree(plan->d_status);
     if (plan->d_mult) cudaFree(plan->d_mult);
+    if (plan->d_xprep) cudaFree(plan->d_xprep);
+    if (plan->d_wprep) cudaFree(plan->d_wprep);
     delete plan;
 }
 

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -29,10 +30,15 @@ struct IgemmGeom {
     int cblocks;   // Cin / bk
     int kblocks;   // k_h * k_w * cblocks: K blocks per tile
     int stages;    // shared-memory pipeline depth
+    int out_bufs;  // epilogue output staging buffers per group (1 or 2)
     int grid;      // persistent CTAs
     int smem;      // dynamic shared memory bytes
     int in_i8;     // operands are int8 (converted to bf16 on chip)
     int swap;      // 1: MMA M = output channels, N = 256 pixels (Cout <= 128)
+    int prep;      // 1: x and w are widened to bf16 / channel-padded first
+    int cin;       // input channels the kernel sees (padded when prep)
+    int fold;      // 1: the k_w taps are folded into the (padded) channels by the pre-pass
+    int kw, wx, padw;  // kernel width, x width and w padding the kernel sees (1, W', 0 when fold)
 };
 
 struct DwGeom {
@@ -57,6 +63,8 @@ struct conv_plan {
     int num_sms;
     float *d_mult;     // int8: requantisation multipliers M[co] (device)
     int *d_status;     // device status word (bounded-wait timeouts)
+    __nv_bfloat16 *d_xprep, *d_wprep;  // bf16 (channel-padded) copies of x and w for the tensor-core path
+    int cin_p;         // channels of those copies
     IgemmGeom ig;
     DwGeom dw;
     int dct, dpt;      // direct kernel: channels / pixels per thread of the smem variant (dct 0: generic)
@@ -75,13 +83,18 @@ cudaError_t launch_dw3x3(const conv_plan *p, const void *x, const void *w, const
 int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *bias, void *y,
                  cudaStream_t st);
 
+// Widens int8 to bf16 / pads channels into the plan's d_xprep, d_wprep.
+cudaError_t launch_prep(const conv_plan *p, const void *x, const void *w, cudaStream_t st);
+
 // Plan-time helpers of each family.
 bool direct_supported(const conv_plan *p);
 void direct_configure(conv_plan *p);
 bool dw3x3_supported(const conv_plan *p);
 int dw3x3_configure(conv_plan *p);  // CONV_* status
 bool igemm_supported(const conv_plan *p);
-int igemm_configure(conv_plan *p);  // fills p->ig, sets kernel attributes; CONV_* status
+// Fills p->ig and sets kernel attributes; CONV_* status.  layout 0 picks
+// the tile layout by estimated time; 1..4 force swapped, N256, N128, N64.
+int igemm_configure(conv_plan *p, int layout);
 
 // Host-side argument checks shared by the entry points (api.cu).
 int conv_validate_layer(const conv_shape_t *s, int stride, int pad_h, int pad_w, int groups,

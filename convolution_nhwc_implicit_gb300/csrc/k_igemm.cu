@@ -65,8 +65,11 @@ struct IgArgs {
     int flat;
     uint32_t a_bytes;    // bytes TMA writes per A box
     int act;
-    const float *bias;
-    __nv_bfloat16 *y;
+    const void *bias;    // fp32 [Cout] (bf16 output) or int32 [Cout] (int8 output), or null
+    void *y;             // bf16 or int8 NHWC output
+    int out_i8;          // 1: int8 output, requantised with mult[co]
+    const float *mult;   // int8: requantisation multipliers M[co]
+    int out_bufs;        // normal mode: output staging buffers per epilogue group (1 or 2)
     int *status;
 };
 
@@ -101,7 +104,10 @@ __device__ __forceinline__ void epilogue_swapped(const IgArgs &a, int tile, uint
     const int nb = tile % a.tiles_n;
     const int mt = tile / a.tiles_n;
     const int co = nb * 128 + row;
-    const float bias = (a.bias && co < a.Cout) ? __ldg(a.bias + co) : 0.0f;
+    const bool cov = co < a.Cout;
+    const float fbias = (!a.out_i8 && a.bias && cov) ? __ldg(reinterpret_cast<const float *>(a.bias) + co) : 0.0f;
+    const long long ibias = (a.out_i8 && a.bias && cov) ? (long long)__ldg(reinterpret_cast<const int32_t *>(a.bias) + co) : 0ll;
+    const float mult = (a.out_i8 && cov) ? __ldg(a.mult + co) : 0.0f;
     // Pull the whole slice out of TMEM first and hand the buffer back.
     uint32_t acc[kCols];
 #pragma unroll
@@ -127,10 +133,19 @@ __device__ __forceinline__ void epilogue_swapped(const IgArgs &a, int tile, uint
 #pragma unroll
     for (int c = 0; c < kCols; c += 16) {
         tc::named_bar_sync(1 + grp, 128);  // the previous chunk's rows have been read
+        if (a.out_i8) {
+            // exact integer accumulator -> + bias -> requantise (rows of 128 bytes)
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const __nv_bfloat16 h = __float2bfloat16_rn(activate_fast(__uint_as_float(acc[c + i]) + bias, a.act));
-            *reinterpret_cast<__nv_bfloat16 *>(tbuf + i * kTP + row * 2) = h;
+            for (int i = 0; i < 16; ++i) {
+                const long long v = (long long)__float2int_rn(__uint_as_float(acc[c + i])) + ibias;
+                tbuf[i * kTP + row] = (uint8_t)(int8_t)requant_i8(v, mult, a.act);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const __nv_bfloat16 h = __float2bfloat16_rn(activate_fast(__uint_as_float(acc[c + i]) + fbias, a.act));
+                *reinterpret_cast<__nv_bfloat16 *>(tbuf + i * kTP + row * 2) = h;
+            }
         }
         tc::named_bar_sync(1 + grp, 128);
         const int p = c_base + c + wpx;  // pixel index inside the tile
@@ -145,9 +160,14 @@ __device__ __forceinline__ void epilogue_swapped(const IgArgs &a, int tile, uint
             valid = p < a.bw * a.bh && oh < a.OH && ow < a.OW;
             pix = ((long long)n * a.OH + oh) * a.OW + ow;
         }
-        if (valid) {
+        if (valid && a.out_i8) {
+            // 16 int8 channels per thread (Cout % 16 == 0 on this path)
+            const uint4 *src = reinterpret_cast<const uint4 *>(tbuf + wpx * kTP + (gt & 7) * 16);
+            int8_t *dst = reinterpret_cast<int8_t *>(a.y) + pix * a.Cout + wco;
+            if (wco < a.Cout) *reinterpret_cast<uint4 *>(dst) = src[0];
+        } else if (valid) {
             const uint4 *src = reinterpret_cast<const uint4 *>(tbuf + wpx * kTP + (gt & 7) * 32);
-            __nv_bfloat16 *dst = a.y + pix * a.Cout + wco;
+            __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(a.y) + pix * a.Cout + wco;
             if (wco < a.Cout) *reinterpret_cast<uint4 *>(dst) = src[0];
             if (wco + 8 < a.Cout) *reinterpret_cast<uint4 *>(dst + 8) = src[1];
         }
@@ -183,7 +203,7 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const uint32_t sA = base;
     const uint32_t sB = base + stages * kAStage;
     const uint32_t sOut = sB + stages * kBStage;  // per epilogue group: 128 rows x 64 B output staging
-    const uint32_t sBar = sOut + kGroups * kOutStage;
+    const uint32_t sBar = sOut + kGroups * a.out_bufs * kOutStage;
     auto full_bar = [&](int s) { return sBar + 8u * s; };
     auto empty_bar = [&](int s) { return sBar + 8u * (stages + s); };
     auto tfull_bar = [&](int b) { return sBar + 8u * (2 * stages + b); };
@@ -313,6 +333,8 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         const int row = q * 32 + lane;
         const int c_base = grp * kCols;
         const bool issuer = ((warp - 2) & 3) == 0 && lane == 0;  // issues the group's TMA stores
+        const uint32_t sStage = sOut + (uint32_t)(grp * a.out_bufs) * kOutStage;  // this group's staging
+        int oc = 0;  // TMA stores this group has issued (selects the staging buffer)
         int lt = 0;
         for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x, ++lt) {
             const int buf = lt & 1;
@@ -324,7 +346,7 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             tc::fence_after_sync();
             if constexpr (SWAP) {
                 epilogue_swapped<kCols>(a, tile, tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kAcc + c_base),
-                                        tempty_bar(buf), row, grp, c_base, gbase + (sOut - base) + grp * kOutStage,
+                                        tempty_bar(buf), row, grp, c_base, gbase + (sOut - base) + grp * a.out_bufs * kOutStage,
                                         threadIdx.x - 64 - grp * 128);
                 continue;
             }
@@ -356,23 +378,53 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 n = t2 / a.tiles_h;
                 ow0 = tw * a.bw;
             }
-            const uint32_t srow = sOut + (uint32_t)grp * kOutStage + (uint32_t)row * 64u;
             const uint32_t swz = (uint32_t)((row >> 1) & 3);
 #pragma unroll
             for (int c = 0; c < kCols; c += 32) {
                 const int co = nb * BN + c_base + c;
-                // the previous store from this staging buffer has read it
-                if (issuer) tc::bulk_wait_read0();
+                if (co >= a.Cout) continue;  // the same for the whole group
+                const uint32_t sbuf = sStage + (uint32_t)(oc & (a.out_bufs - 1)) * kOutStage;
+                const uint32_t srow = sbuf + (uint32_t)row * 64u;
+                // the store that last used this staging buffer has read it
+                // (with two buffers that is every store but the latest)
+                if (issuer) {
+                    if (a.out_bufs == 2)
+                        tc::bulk_wait_read1();
+                    else
+                        tc::bulk_wait_read0();
+                }
                 tc::named_bar_sync(1 + grp, 128);
-                if (co < a.Cout) {
+                if (a.out_i8) {
+                    // int8 output: the accumulator is an exact integer (< 2^24);
+                    // + int32 bias, requantise, saturate.  Rows of 32 bytes,
+                    // stored unswizzled (the int8 store map has no swizzle).
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int cc = co + e;
+                        long long v = (long long)__float2int_rn(__uint_as_float(acc[c + e]));
+                        if (a.bias) v += (long long)__ldg(reinterpret_cast<const int32_t *>(a.bias) + cc);
+                        const int q = requant_i8(v, __ldg(a.mult + cc), a.act);
+                        if ((e & 3) == 0) pk[e >> 2] = 0u;
+                        pk[e >> 2] |= ((uint32_t)(q & 0xff)) << (8 * (e & 3));
+                    }
+                    const uint32_t dst8 = sbuf + (uint32_t)row * 32u;
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst8), "r"(pk[0]), "r"(pk[1]),
+                                 "r"(pk[2]), "r"(pk[3])
+                                 : "memory");
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst8 + 16u), "r"(pk[4]),
+                                 "r"(pk[5]), "r"(pk[6]), "r"(pk[7])
+                                 : "memory");
+                } else {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         float v[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(acc[c + 8 * j + e]);
                         if (a.bias && co + 8 * j < a.Cout) {  // Cout % 8 == 0: 8 columns all in or all out
-                            const float4 b0 = __ldg(reinterpret_cast<const float4 *>(a.bias + co + 8 * j));
-                            const float4 b1 = __ldg(reinterpret_cast<const float4 *>(a.bias + co + 8 * j) + 1);
+                            const float *fb = reinterpret_cast<const float *>(a.bias) + co + 8 * j;
+                            const float4 b0 = __ldg(reinterpret_cast<const float4 *>(fb));
+                            const float4 b1 = __ldg(reinterpret_cast<const float4 *>(fb) + 1);
                             v[0] += b0.x; v[1] += b0.y; v[2] += b0.z; v[3] += b0.w;
                             v[4] += b1.x; v[5] += b1.y; v[6] += b1.z; v[7] += b1.w;
                         }
@@ -391,14 +443,14 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
                 tc::fence_proxy_async_smem();  // staged values visible to the TMA engine
                 tc::named_bar_sync(1 + grp, 128);
-                if (issuer && co < a.Cout) {
-                    const uint32_t src = sOut + (uint32_t)grp * kOutStage;
+                if (issuer) {
                     if (FLAT)
-                        tc::tma_store_2d(&tmY, src, co, m0);
+                        tc::tma_store_2d(&tmY, sbuf, co, m0);
                     else
-                        tc::tma_store_4d(&tmY, src, co, ow0, oh0, n);
+                        tc::tma_store_4d(&tmY, sbuf, co, ow0, oh0, n);
                     tc::bulk_commit();
                 }
+                ++oc;
             }
         }
         if (issuer) tc::bulk_wait0();  // all of this CTA's stores are complete
@@ -477,75 +529,142 @@ void *select_kernel(int bn, int bk, bool flat, bool swap) {
 
 }  // namespace
 
+// Layers whose k_w taps of all input channels fit in 16 channels (the
+// 3-channel image stem: 3 x 3 = 9) have those taps folded into the padding:
+// the pre-pass writes, for every input row position u, the k_w x Cin values
+// x[h][u - pad_w + s][ci] (s-major) as one 16-channel pixel, and the kernel
+// runs a k_h x 1 convolution over that tensor.  The padded copy has as many
+// bytes as the plain channel-padded one, with k_w times fewer K blocks.
+static bool igemm_fold(const conv_plan *p) {
+    const bool prep = p->dtype == CONV_I8 || p->s.c_in % 16 != 0;
+    return prep && p->s.k_w > 1 && p->s.k_w * p->s.c_in <= 16;
+}
+
+// Input channels the tensor-core kernel sees: Cin, or Cin (k_w x Cin when
+// folded) rounded up to 16 when the operands go through the widening
+// pre-pass (int8 layers, and bf16 layers whose channel rows are not whole
+// 32-byte units).
+static int igemm_cin(const conv_plan *p) {
+    if (igemm_fold(p)) return 16;
+    const bool prep = p->dtype == CONV_I8 || p->s.c_in % 16 != 0;
+    return prep ? (p->s.c_in + 15) / 16 * 16 : p->s.c_in;
+}
+
 bool igemm_supported(const conv_plan *p) {
-    if (p->dtype != CONV_BF16 || p->groups != 1) return false;
-    if (p->s.c_in % 16 != 0 || p->s.c_out % 8 != 0) return false;
+    if (p->groups != 1 || p->dtype == CONV_F32) return false;  // fp32 stays on FFMA (never TF32)
+    if (p->dtype == CONV_BF16 && p->s.c_out % 8 != 0) return false;
+    if (p->dtype == CONV_I8) {
+        // int8 output rows are stored 16 bytes at a time; exactness of the
+        // fp32 accumulation needs K * 128 * 127 < 2^24 (K <= 1024).
+        if (p->s.c_out % 16 != 0) return false;
+        if ((long long)p->s.k_h * (igemm_fold(p) ? 1 : p->s.k_w) * igemm_cin(p) > 1024) return false;
+    }
     if (p->stride > 8) return false;  // TMA element strides are at most 8
-    const long long pixels_in = (long long)p->s.n * p->s.h * p->s.w;
+    const long long pixels_in = (long long)p->s.n * p->s.h * (p->s.w + 2 * p->pad_w);
     if (pixels_in > 0xFFFFFFFFll) return false;  // TMA dimension limit
     if ((long long)p->s.n * p->oh * p->ow > 0x7FFFFFFFll) return false;
     return true;
 }
 
-int igemm_configure(conv_plan *p) {
+int igemm_configure(conv_plan *p, int layout) {
     IgemmGeom &g = p->ig;
     const int S = p->stride;
     g.in_i8 = 0;
-    g.flat = (p->s.k_h == 1 && p->s.k_w == 1 && S == 1 && p->pad_h == 0 && p->pad_w == 0) ? 1 : 0;
-    g.bk = p->s.c_in % 64 == 0 ? 64 : (p->s.c_in % 32 == 0 ? 32 : 16);
-    g.cblocks = p->s.c_in / g.bk;
-    g.kblocks = p->s.k_h * p->s.k_w * g.cblocks;
+    const int cin = igemm_cin(p);
+    g.prep = (cin != p->s.c_in || p->dtype == CONV_I8) ? 1 : 0;
+    g.cin = cin;
+    g.fold = igemm_fold(p) ? 1 : 0;
+    g.kw = g.fold ? 1 : p->s.k_w;
+    g.padw = g.fold ? 0 : p->pad_w;
+    g.wx = g.fold ? p->s.w + 2 * p->pad_w - p->s.k_w + 1 : p->s.w;
+    g.flat = (p->s.k_h == 1 && g.kw == 1 && S == 1 && p->pad_h == 0 && g.padw == 0) ? 1 : 0;
+    g.bk = cin % 64 == 0 ? 64 : (cin % 32 == 0 ? 32 : 16);
+    g.cblocks = cin / g.bk;
+    if (g.prep) {
+        // plan-owned bf16 copies of x and w (channels padded to `cin`)
+        const size_t xb = (size_t)p->s.n * p->s.h * g.wx * cin * 2;
+        const size_t wb = (size_t)p->s.c_out * p->s.k_h * g.kw * cin * 2;
+        p->cin_p = cin;
+        if (xb && cudaMalloc(&p->d_xprep, xb) != cudaSuccess) return CONV_ERR_OOM;
+        if (cudaMalloc(&p->d_wprep, wb) != cudaSuccess) return CONV_ERR_OOM;
+    }
+    g.kblocks = p->s.k_h * g.kw * g.cblocks;
 
-    // Layers with at most 128 output channels run with the operands swapped:
-    // 256-pixel tiles as the MMA's N (full-rate MMAs) and the weights as M.
-    g.swap = p->s.c_out <= 128 ? 1 : 0;
-    const int P = g.swap ? kBMSwap : kBM;  // pixels per tile
-
-    // M tiling.
-    if (g.flat) {
-        const long long M = (long long)p->s.n * p->s.h * p->s.w;
-        g.bw = P; g.bh = 1;
-        g.tiles_w = 1; g.tiles_h = 1;
-        g.tiles_m = (int)((M + P - 1) / P);
-    } else {
-        // Smallest number of bh x bw rectangles covering the output; among
-        // equal counts, the widest (longest contiguous NHWC runs).
-        long long best = -1;
-        for (int bw = 1; bw <= P && bw <= p->ow * 2; ++bw) {
-            if (bw * S > 256) break;
-            int bh = P / bw;
-            if (bh > p->oh) bh = p->oh;
-            while (bh * S > 256) --bh;
-            if (bh < 1) continue;
-            const long long tw = (p->ow + bw - 1) / bw, th = (p->oh + bh - 1) / bh;
-            const long long tiles = tw * th * p->s.n;
-            if (best < 0 || tiles < best || (tiles == best && bw > g.bw)) {
-                best = tiles; g.bw = bw; g.bh = bh; g.tiles_w = (int)tw; g.tiles_h = (int)th;
+    // Candidate layouts: swapped (Cout <= 128) with 256-pixel tiles, or
+    // normal with 128-pixel tiles and BN in {256, 128, 64}.  Each is scored
+    // by an estimate of its time: waves x (per-tile cost + fixed cost), the
+    // per-tile cost being the largest of
+    //   MMA issue   128 cycles per K=16 step whatever N is (so N = 256 is
+    //               the only full-rate width),
+    //   operand feed (pixels + BN) * K * 2 bytes from L2 at ~80 B/cycle,
+    //   epilogue    accumulator lanes x columns (wasted lanes included)
+    //               x cycles per value / 128 lanes per cycle per SM,
+    // with the epilogue costing ~16 cycles per value with Mish (two MUFU
+    // operations), ~10 for an int8 requantisation and ~6 otherwise.
+    const long long K = (long long)p->s.k_h * g.kw * cin;
+    const long long epi_c = p->dtype == CONV_I8 ? 10 : (p->act == CONV_ACT_MISH ? 16 : 6);
+    long long best_cost = -1, best_tiles = 0;
+    for (int cand = 0; cand < 4; ++cand) {
+        const bool swap = cand == 0;
+        if (swap && p->s.c_out > 128) continue;
+        if (layout != 0 && layout != cand + 1) continue;
+        const int bn = swap ? 128 : (cand == 1 ? 256 : (cand == 2 ? 128 : 64));
+        const int P = swap ? kBMSwap : kBM;
+        int bw = P, bh = 1, tw = 1, th = 1;
+        long long tiles_m;
+        if (g.flat) {
+            const long long M = (long long)p->s.n * p->s.h * g.wx;
+            tiles_m = (M + P - 1) / P;
+        } else {
+            // Smallest number of bh x bw rectangles covering the output; among
+            // equal counts, the widest (longest contiguous NHWC runs).
+            long long best = -1;
+            for (int cw = 1; cw <= P && cw <= p->ow * 2; ++cw) {
+                if (cw * S > 256) break;
+                int ch = P / cw;
+                if (ch > p->oh) ch = p->oh;
+                while (ch * S > 256) --ch;
+                if (ch < 1) continue;
+                const long long ctw = (p->ow + cw - 1) / cw, cth = (p->oh + ch - 1) / ch;
+                const long long t = ctw * cth * p->s.n;
+                if (best < 0 || t < best || (t == best && cw > bw)) {
+                    best = t; bw = cw; bh = ch; tw = (int)ctw; th = (int)cth;
+                }
+                if (cw >= p->ow) break;
             }
-            if (bw >= p->ow) break;
+            tiles_m = best;
         }
-        g.tiles_m = g.tiles_w * g.tiles_h * p->s.n;
-    }
-
-    if (g.swap) {
-        g.bn = 128;
-        g.tiles_n = 1;
-    } else {
-        // N tile: an MMA costs about the same for any N <= 256, so wider tiles
-        // are cheaper per output; estimated time ~ waves x (BN + fixed cost).
-        long long best_cost = -1;
-        for (int bn : {256, 128, 64}) {
-            const long long tn = (p->s.c_out + bn - 1) / bn;
-            const long long tiles = tn * g.tiles_m;
-            const long long waves = (tiles + p->num_sms - 1) / p->num_sms;
-            const long long cost = waves * (bn + 48);
-            if (best_cost < 0 || cost < best_cost) { best_cost = cost; g.bn = bn; g.tiles_n = (int)tn; }
+        const long long tiles_n = swap ? 1 : (p->s.c_out + bn - 1) / bn;
+        const long long tiles = tiles_m * tiles_n;
+        const long long waves = (tiles + p->num_sms - 1) / p->num_sms;
+        const long long t_mma = K / 16 * 128;
+        const long long t_feed = (P + bn) * K * 2 / 80;
+        const long long t_epi = 128LL * (swap ? P : bn) * epi_c / 128;
+        long long t_tile = t_mma > t_feed ? t_mma : t_feed;
+        if (t_epi > t_tile) t_tile = t_epi;
+        const long long cost = waves * (t_tile + 500);
+        // ties: more tiles (more SMs busy), then the narrower N tile
+        if (best_cost < 0 || cost < best_cost || (cost == best_cost && tiles > best_tiles) ||
+            (cost == best_cost && tiles == best_tiles && bn < g.bn)) {
+            best_cost = cost;
+            best_tiles = tiles;
+            g.swap = swap ? 1 : 0; g.bn = bn; g.tiles_n = (int)tiles_n; g.tiles_m = (int)tiles_m;
+            g.bw = bw; g.bh = bh; g.tiles_w = tw; g.tiles_h = th;
         }
     }
+    if (best_cost < 0) return CONV_ERR_UNSUPPORTED;  // forced swapped layout with c_out > 128
+    const int P = g.swap ? kBMSwap : kBM;  // pixels per tile
     g.num_tiles = g.tiles_n * g.tiles_m;
 
     const int stage_bytes = (P + g.bn) * g.bk * 2;
-    const int out_bytes = g.swap ? 4 * 16 * kTP : epi_groups(g.bn, false) * kBM * 64;  // epilogue staging
+    // Epilogue staging: swapped mode, 16 transpose rows per group; normal
+    // mode, 128 rows x 64 B per group and buffer.  Two buffers per group let
+    // a group fill one while the TMA store of the other is still reading it;
+    // they are used when the operand ring keeps at least 4 stages.
+    const int one_buf = g.swap ? 4 * 16 * kTP : epi_groups(g.bn, false) * kBM * 64;
+    g.out_bufs = 1;
+    if (!g.swap && (227 * 1024 - 1024 - 256 - 2 * one_buf) / stage_bytes >= 4) g.out_bufs = 2;
+    const int out_bytes = one_buf * g.out_bufs;
     const int budget = 227 * 1024 - 1024 - 256 - out_bytes;
     g.stages = budget / stage_bytes;
     if (g.stages > 8) g.stages = 8;
@@ -561,15 +680,24 @@ int igemm_configure(conv_plan *p) {
     const int rc = conv_grant_smem(select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0), p->device, g.smem);
     if (rc != CONV_OK) return rc;
     snprintf(p->desc, sizeof(p->desc),
-             "igemm_bf16_tcgen05 %s%s %s BK=%d tile=%dx%d stages=%d tiles=%d grid=%d", g.flat ? "flat" : "spatial",
+             "igemm_%s_tcgen05 %s%s %s BK=%d tile=%dx%d stages=%d out_bufs=%d tiles=%d grid=%d",
+             p->dtype == CONV_I8 ? (g.fold ? "i8-as-bf16-kwfold" : "i8-as-bf16")
+                                 : (g.fold ? "bf16-cpad-kwfold" : (g.prep ? "bf16-cpad" : "bf16")),
+             g.flat ? "flat" : "spatial",
              g.swap ? " swapped" : "", g.swap ? "M=128co N=256px" : (g.bn == 256 ? "M=128px N=256co" : (g.bn == 128 ? "M=128px N=128co" : "M=128px N=64co")),
-             g.bk, g.bh, g.bw, g.stages, g.num_tiles, g.grid);
+             g.bk, g.bh, g.bw, g.stages, g.out_bufs, g.num_tiles, g.grid);
     return CONV_OK;
 }
 
 int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *bias, void *y,
                  cudaStream_t st) {
     const IgemmGeom &g = p->ig;
+    if (g.prep) {
+        if (launch_prep(p, x, w, st) != cudaSuccess) return CONV_ERR_CUDA;
+        x = p->d_xprep;
+        w = p->d_wprep;
+    }
+    const int cin = g.cin;
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return CONV_ERR_CUDA;
     const int S = p->stride;
@@ -577,17 +705,17 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
     const cuuint32_t ones[4] = {1, 1, 1, 1};
     CUresult rc;
     if (g.flat) {
-        const cuuint64_t dims[2] = {(cuuint64_t)p->s.c_in, (cuuint64_t)p->s.n * p->s.h * p->s.w};
-        const cuuint64_t strides[1] = {(cuuint64_t)p->s.c_in * 2};
+        const cuuint64_t dims[2] = {(cuuint64_t)cin, (cuuint64_t)p->s.n * p->s.h * g.wx};
+        const cuuint64_t strides[1] = {(cuuint64_t)cin * 2};
         const cuuint32_t box[2] = {(cuuint32_t)g.bk, (cuuint32_t)(g.swap ? kBMSwap : kBM)};
         rc = encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims, strides, box, ones,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(g.bk), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     } else {
-        const cuuint64_t dims[4] = {(cuuint64_t)p->s.c_in, (cuuint64_t)p->s.w, (cuuint64_t)p->s.h,
+        const cuuint64_t dims[4] = {(cuuint64_t)cin, (cuuint64_t)g.wx, (cuuint64_t)p->s.h,
                                     (cuuint64_t)p->s.n};
-        const cuuint64_t strides[3] = {(cuuint64_t)p->s.c_in * 2, (cuuint64_t)p->s.w * p->s.c_in * 2,
-                                       (cuuint64_t)p->s.h * p->s.w * p->s.c_in * 2};
+        const cuuint64_t strides[3] = {(cuuint64_t)cin * 2, (cuuint64_t)g.wx * cin * 2,
+                                       (cuuint64_t)p->s.h * g.wx * cin * 2};
         const cuuint32_t box[4] = {(cuuint32_t)g.bk, (cuuint32_t)(g.bw * S), (cuuint32_t)(g.bh * S), 1};
         const cuuint32_t estr[4] = {1, (cuuint32_t)S, (cuuint32_t)S, 1};
         rc = encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(x), dims, strides, box, estr,
@@ -596,7 +724,7 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
     }
     if (rc != CUDA_SUCCESS) return CONV_ERR_CUDA;
     {
-        const cuuint64_t K = (cuuint64_t)p->s.k_h * p->s.k_w * p->s.c_in;
+        const cuuint64_t K = (cuuint64_t)p->s.k_h * g.kw * cin;
         const cuuint64_t dims[2] = {K, (cuuint64_t)p->s.c_out};
         const cuuint64_t strides[1] = {K * 2};
         const cuuint32_t box[2] = {(cuuint32_t)g.bk, (cuuint32_t)g.bn};
@@ -608,38 +736,45 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
 
     alignas(64) CUtensorMap tmY;
     {
-        const cuuint32_t box_n = 32;  // 32 output channels (64 bytes) per store box
+        // 32 output channels per store box: 64 bytes (bf16, 64-byte swizzle)
+        // or 32 bytes (int8, unswizzled)
+        const bool i8 = p->dtype == CONV_I8;
+        const cuuint64_t es = i8 ? 1 : 2;
+        const CUtensorMapDataType dt = i8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        const CUtensorMapSwizzle sw = i8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_64B;
+        const cuuint32_t box_n = 32;
         if (g.flat) {
-            const cuuint64_t dims[2] = {(cuuint64_t)p->s.c_out, (cuuint64_t)p->s.n * p->s.h * p->s.w};
-            const cuuint64_t strides[1] = {(cuuint64_t)p->s.c_out * 2};
+            const cuuint64_t dims[2] = {(cuuint64_t)p->s.c_out, (cuuint64_t)p->s.n * p->oh * p->ow};
+            const cuuint64_t strides[1] = {(cuuint64_t)p->s.c_out * es};
             const cuuint32_t box[2] = {box_n, (cuuint32_t)(g.swap ? kBMSwap : kBM)};
-            rc = encode(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, dims, strides, box, ones,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            rc = encode(&tmY, dt, 2, y, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         } else {
             const cuuint64_t dims[4] = {(cuuint64_t)p->s.c_out, (cuuint64_t)p->ow, (cuuint64_t)p->oh,
                                         (cuuint64_t)p->s.n};
-            const cuuint64_t strides[3] = {(cuuint64_t)p->s.c_out * 2, (cuuint64_t)p->ow * p->s.c_out * 2,
-                                           (cuuint64_t)p->oh * p->ow * p->s.c_out * 2};
+            const cuuint64_t strides[3] = {(cuuint64_t)p->s.c_out * es, (cuuint64_t)p->ow * p->s.c_out * es,
+                                           (cuuint64_t)p->oh * p->ow * p->s.c_out * es};
             const cuuint32_t box[4] = {box_n, (cuuint32_t)g.bw, (cuuint32_t)g.bh, 1};
-            rc = encode(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, y, dims, strides, box, ones,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            rc = encode(&tmY, dt, 4, y, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         }
         if (rc != CUDA_SUCCESS) return CONV_ERR_CUDA;
     }
 
     IgArgs a;
-    a.H = p->s.h; a.W = p->s.w; a.Cin = p->s.c_in; a.Cout = p->s.c_out; a.KH = p->s.k_h; a.KW = p->s.k_w;
-    a.stride = S; a.pad_h = p->pad_h; a.pad_w = p->pad_w; a.OH = p->oh; a.OW = p->ow;
+    a.H = p->s.h; a.W = g.wx; a.Cin = cin; a.Cout = p->s.c_out; a.KH = p->s.k_h; a.KW = g.kw;
+    a.stride = S; a.pad_h = p->pad_h; a.pad_w = g.padw; a.OH = p->oh; a.OW = p->ow;
     a.bw = g.bw; a.bh = g.bh; a.tiles_w = g.tiles_w; a.tiles_h = g.tiles_h; a.tiles_n = g.tiles_n;
     a.num_tiles = g.num_tiles; a.cblocks = g.cblocks; a.kblocks = g.kblocks; a.stages = g.stages;
-    a.M = (long long)p->s.n * p->s.h * p->s.w;
+    a.M = (long long)p->s.n * p->s.h * g.wx;
     a.a_bytes = (uint32_t)((g.flat ? (g.swap ? kBMSwap : kBM) : g.bw * g.bh) * g.bk * 2);
     a.flat = g.flat;
     a.act = (int)p->act;
-    a.bias = (const float *)bias;
-    a.y = (__nv_bfloat16 *)y;
+    a.bias = bias;
+    a.y = y;
+    a.out_i8 = p->dtype == CONV_I8 ? 1 : 0;
+    a.mult = p->d_mult;
+    a.out_bufs = g.out_bufs;
     a.status = p->d_status;
 
     void *k = select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0);

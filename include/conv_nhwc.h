@@ -94,6 +94,12 @@ typedef enum {
     CONV_ALGO_DIRECT = 1,     /* CUDA-core direct convolution, any shape  */
     CONV_ALGO_DEPTHWISE = 2,  /* depthwise 3x3 register/L1 stencil        */
     CONV_ALGO_IGEMM = 3,      /* tcgen05 implicit GEMM (TMA, TMEM)        */
+    /* CONV_ALGO_IGEMM with a fixed tile layout instead of the estimated
+     * fastest one (conv_plan_algo then reports CONV_ALGO_IGEMM):          */
+    CONV_ALGO_IGEMM_SWAPPED = 4, /* MMA M = 128 output channels, N = 256 pixels (c_out <= 128) */
+    CONV_ALGO_IGEMM_N256 = 5,    /* MMA M = 128 pixels, N = 256 output channels */
+    CONV_ALGO_IGEMM_N128 = 6,    /* MMA M = 128 pixels, N = 128 output channels */
+    CONV_ALGO_IGEMM_N64 = 7,     /* MMA M = 128 pixels, N = 64 output channels  */
 } conv_algo_t;
 
 enum {

@@ -65,9 +65,86 @@ IGEMM = [
 ]
 
 
-@pytest.mark.parametrize("spec", IGEMM, ids=lambda s: s.name)
-def test_igemm_bf16(spec):
-    check(spec, "igemm", "igemm")
+# Every case runs with the layout the plan picks and with each forced tile
+# layout: swapped (c_out <= 128 only), N = 256, 128 and 64.
+_LAYOUT_DESC = {"igemm_swapped": "swapped", "igemm_n256": "N=256co", "igemm_n128": "N=128co",
+                "igemm_n64": "N=64co"}
+
+
+def with_layouts(specs):
+    out = []
+    for spec in specs:
+        for lay in ["igemm", "igemm_swapped", "igemm_n256", "igemm_n128", "igemm_n64"]:
+            if lay == "igemm_swapped" and spec.cout > 128:
+                continue
+            out.append(pytest.param(spec, lay, id=f"{spec.name}-{lay}"))
+    return out
+
+
+def check_layout(spec, layout):
+    plan = check(spec, layout, "igemm")
+    if layout in _LAYOUT_DESC:
+        assert _LAYOUT_DESC[layout] in plan.describe(), plan.describe()
+    return plan
+
+
+@pytest.mark.parametrize("spec,layout", with_layouts(IGEMM))
+def test_igemm_bf16(spec, layout):
+    check_layout(spec, layout)
+
+
+def test_swapped_layout_needs_cout_le_128():
+    spec = L("swap_cout256", 1, 8, 8, 64, 256, 3, 3, 1, 1, 1)
+    d = make_layer(spec, torch.Generator("cpu").manual_seed(0))
+    with pytest.raises(RuntimeError, match="UNSUPPORTED"):
+        make_plan(spec, d, "igemm_swapped")
+
+
+# int8 on the tensor cores (operands widened to bf16, exact fp32 accumulation):
+# results must be bit-identical to the oracle's int64 accumulation.
+IGEMM_I8 = [
+    L("i8_3x3_64to64_ragged", 1, 21, 19, 64, 64, 3, 3, 1, 1, 1, dtype="i8"),
+    L("i8_3x3_relu_sat", 2, 13, 11, 64, 48, 3, 3, 1, 1, 1, dtype="i8", act="relu",
+      b_dist=("int", -300000, 300000)),
+    L("i8_1x1_32to64", 1, 24, 20, 32, 64, 1, 1, dtype="i8"),
+    L("i8_3x3_s2_cin48_pad", 1, 17, 15, 48, 32, 3, 3, 2, 1, 1, dtype="i8"),
+    L("i8_cout256_normal_mode", 1, 9, 9, 32, 256, 3, 3, 1, 1, 1, dtype="i8"),
+    L("i8_k_1024", 1, 8, 8, 1024, 16, 1, 1, dtype="i8", act="relu"),
+    L("i8_cin3_pad", 1, 18, 16, 3, 16, 3, 3, 1, 1, 1, dtype="i8"),
+    L("i8_kwfold_s2", 1, 19, 22, 4, 32, 3, 3, 2, 1, 1, dtype="i8", act="relu"),
+]
+
+
+@pytest.mark.parametrize("spec,layout", with_layouts(IGEMM_I8))
+def test_igemm_int8_exact(spec, layout):
+    plan = check_layout(spec, layout)
+    assert "i8-as-bf16" in plan.describe()
+
+
+# bf16 layers whose channel rows are too short for TMA: channels padded to 16.
+IGEMM_CPAD = [
+    L("cpad_stem_cin3", 1, 37, 45, 3, 32, 3, 3, 1, 1, 1),
+    L("cpad_cin24_s2", 2, 15, 13, 24, 64, 3, 3, 2, 1, 1, act="relu"),
+    L("cpad_cin1_10x4", 1, 49, 10, 1, 64, 10, 4, 2, 5, 1, act="none"),
+    # k_w x Cin <= 16: the k_w taps are folded into the padded channels
+    L("kwfold_1x3_flat", 1, 9, 40, 4, 32, 1, 3, 1, 0, 1),
+    L("kwfold_s2_overpad_w", 1, 21, 23, 5, 24, 3, 3, 2, 1, 2, act="relu"),
+    L("kwfold_5x2_no_pad", 2, 11, 12, 8, 16, 5, 2, 1, 0, 0),
+]
+
+
+@pytest.mark.parametrize("spec,layout", with_layouts(IGEMM_CPAD))
+def test_igemm_channel_padding(spec, layout):
+    plan = check_layout(spec, layout)
+    assert "cpad" in plan.describe()
+    assert ("kwfold" in plan.describe()) == (spec.kw > 1 and spec.kw * spec.cin <= 16)
+
+
+def test_int8_plan_without_tensor_core_path_falls_to_dp4a():
+    # K = 9 * 256 > 1024: the exact-accumulation bound is not met
+    spec = L("i8_long_k", 1, 6, 6, 256, 16, 3, 3, 1, 1, 1, dtype="i8")
+    plan = check(spec, "auto", "direct")
+    assert "dp4a" in plan.describe()
 
 
 # ------------------------------------------------ depthwise 3x3
