@@ -35,6 +35,7 @@ struct IgemmGeom {
     int smem;      // dynamic shared memory bytes
     int in_i8;     // operands are int8 (converted to bf16 on chip)
     int swap;      // 1: MMA M = output channels, N = 256 pixels (Cout <= 128)
+    int pair;      // 1: CTA-pair MMA, M = 2 x 128 pixels over a cluster of two CTAs, N = 256
     int prep;      // 1: x and w are widened to bf16 / channel-padded first
     int cin;       // input channels the kernel sees (padded when prep)
     int fold;      // 1: the k_w taps are folded into the (padded) channels by the pre-pass
@@ -93,7 +94,8 @@ bool dw3x3_supported(const conv_plan *p);
 int dw3x3_configure(conv_plan *p);  // CONV_* status
 bool igemm_supported(const conv_plan *p);
 // Fills p->ig and sets kernel attributes; CONV_* status.  layout 0 picks
-// the tile layout by estimated time; 1..4 force swapped, N256, N128, N64.
+// the tile layout by estimated time; 1..5 force swapped, N256, N128, N64,
+// CTA pair.
 int igemm_configure(conv_plan *p, int layout);
 
 // Host-side argument checks shared by the entry points (api.cu).

@@ -61,6 +61,7 @@ __host__ __device__ constexpr int cta_threads(int bn, bool swap) { return 64 + 1
 struct IgArgs {
     int H, W, Cin, Cout, KH, KW, stride, pad_h, pad_w, OH, OW;
     int bw, bh, tiles_w, tiles_h, tiles_n, num_tiles, cblocks, kblocks, stages;
+    int tiles_m;         // pixel tiles (pair mode: each CTA of a pair takes one of two)
     long long M;         // flat mode: rows of x viewed as [N*H*W, Cin]
     int flat;
     uint32_t a_bytes;    // bytes TMA writes per A box
@@ -75,12 +76,15 @@ struct IgArgs {
 
 // Waits for phase `parity` of `bar`, giving up after kWaitBudgetNs or when
 // another role of the CTA has given up.  Returns false on give-up.
+// CLUSTER: acquire at cluster scope (arrivals may come from the peer CTA).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                              int *status, int code) {
-    if (tc::mbar_try_wait(bar, parity)) return true;
+    auto poll = [&]() { return CLUSTER ? tc::mbar_try_wait_cluster(bar, parity) : tc::mbar_try_wait(bar, parity); };
+    if (poll()) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
-        if (tc::mbar_try_wait(bar, parity)) return true;
+        if (poll()) return true;
         if ((i & 63u) == 0u) {
             if (*abort_flag) return false;
             if (globaltimer_ns() - t0 > kWaitBudgetNs) {
@@ -179,17 +183,31 @@ __device__ __forceinline__ void epilogue_swapped(const IgArgs &a, int tile, uint
 // 128 output channels (weights as A), N = 256 pixels (activations as B),
 // D[co][pixel]; every MMA then has N = 256, the only width at which tcgen05
 // reaches its peak rate (the issue cost of an MMA does not shrink with N).
-template <int BN, int BK, bool FLAT, bool SWAP>
+//
+// PAIR (normal layout only): a cluster of two CTAs on two SMs computes a
+// 256-pixel x BN tile with tcgen05's CTA-pair MMA (M = 256).  Each CTA stages
+// its own 128 pixel rows and HALF of the BN weight rows; the even CTA issues
+// the MMAs, which read both CTAs' shared memory and write each CTA's 128
+// accumulator rows into its own TMEM.  Per SM this stages (128 + BN/2) rows
+// per K block instead of 128 + BN: a third less shared-memory traffic for
+// BN = 256, which is what limits the single-CTA layout on large layers.
+// Both CTAs' loads complete on the even CTA's full barrier; the even CTA's
+// commits arrive on both CTAs' empty / accumulator-full barriers; both CTAs'
+// epilogue warps arrive on the even CTA's accumulator-empty barrier.
+template <int BN, int BK, bool FLAT, bool SWAP, bool PAIR>
 __global__ void __launch_bounds__(cta_threads(BN, SWAP), 1)
 igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmY, const IgArgs a) {
-    constexpr int kPix = SWAP ? kBMSwap : kBM;  // pixel rows of a tile
+    static_assert(!(PAIR && SWAP), "the CTA-pair mode uses the normal layout");
+    constexpr int kPix = SWAP ? kBMSwap : kBM;  // pixel rows of a tile (per CTA)
     constexpr int kAcc = SWAP ? kBMSwap : BN;   // accumulator columns of a tile
+    constexpr int kBRows = PAIR ? BN / 2 : BN;  // weight rows this CTA stages
     constexpr uint32_t kRowBytes = BK * 2;
     constexpr uint32_t kAStage = kPix * BK * 2;  // activation (pixel) tile
-    constexpr uint32_t kBStage = BN * BK * 2;    // weight tile
+    constexpr uint32_t kBStage = kBRows * BK * 2;  // weight tile (this CTA's part)
     constexpr uint32_t kTmemCols = 2 * kAcc;     // two accumulators
-    constexpr uint32_t kIdesc = SWAP ? tc::idesc_bf16_f32(128, kBMSwap) : tc::idesc_bf16_f32(kBM, BN);
+    constexpr uint32_t kIdesc = SWAP ? tc::idesc_bf16_f32(128, kBMSwap)
+                                     : tc::idesc_bf16_f32(PAIR ? 2 * kBM : kBM, BN);
     constexpr int kGroups = epi_groups(BN, SWAP);
     constexpr int kCols = kAcc / kGroups;  // accumulator columns per epilogue thread
     static_assert(SWAP ? (BN == 128 && kCols % 16 == 0) : (kCols % 32 == 0), "epilogue column slices");
@@ -214,6 +232,10 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // Work unit: the CTA, or in pair mode the cluster (CTAs 2u and 2u + 1).
+    const uint32_t rank = PAIR ? tc::cluster_ctarank() : 0u;
+    const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -222,7 +244,7 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(tfull_bar(b), 1);
-            tc::mbar_init(tempty_bar(b), 128 * kGroups);
+            tc::mbar_init(tempty_bar(b), PAIR ? 2 * 4 * kGroups : 128 * kGroups);  // pair: one per warp
         }
         *abort_flag = 0;
         tc::fence_mbar_init();
@@ -231,13 +253,19 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         tc::tma_prefetch_desc(&tmY);
     }
     if (warp == 1) {
-        tc::tmem_alloc(tc::smem_u32((const void *)tmem_holder), kTmemCols);
-        tc::tmem_relinquish();
+        if constexpr (PAIR) {
+            tc::tmem_alloc_pair(tc::smem_u32((const void *)tmem_holder), kTmemCols);
+            tc::tmem_relinquish_pair();
+        } else {
+            tc::tmem_alloc(tc::smem_u32((const void *)tmem_holder), kTmemCols);
+            tc::tmem_relinquish();
+        }
     }
     // __syncthreads is an aligned barrier: every warp must reach it converged.
     __syncwarp();
     tc::fence_before_sync();
     __syncthreads();
+    if constexpr (PAIR) tc::cluster_sync();  // the peer's barriers are initialised
     tc::fence_after_sync();
     const uint32_t tmem_base = *tmem_holder;
 
@@ -247,9 +275,13 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
+            // pair mode: both CTAs' loads complete on the even CTA's barriers
+            const uint32_t full0 = PAIR ? tc::mapa_shared(full_bar(0), 0) : full_bar(0);
+            for (int tile = unit; tile < a.num_tiles && ok; tile += units) {
                 const int nb = tile % a.tiles_n;
-                const int mt = tile / a.tiles_n;
+                // pair mode: this CTA's pixel tile (past tiles_m: an empty
+                // half, loaded as zeros from outside the tensor, never stored)
+                const int mt = PAIR ? (tile / a.tiles_n) * 2 + (int)rank : tile / a.tiles_n;
                 int n = 0, oh0 = 0, ow0 = 0;
                 int m0 = 0;
                 if (FLAT) {
@@ -268,15 +300,27 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         ok = false;
                         break;
                     }
-                    tc::mbar_arrive_expect_tx(full_bar(stage), a.a_bytes + kBStage);
                     const uint32_t dA = sA + stage * kAStage;
                     const uint32_t dB = sB + stage * kBStage;
-                    if (FLAT)
-                        tc::tma_load_2d(dA, &tmA, full_bar(stage), cb * BK, m0);
-                    else
-                        tc::tma_load_4d(dA, &tmA, full_bar(stage), cb * BK,
-                                        ow0 * a.stride - a.pad_w + s, oh0 * a.stride - a.pad_h + r, n);
-                    tc::tma_load_2d(dB, &tmB, full_bar(stage), (r * a.KW + s) * a.Cin + cb * BK, nb * BN);
+                    const int kx = (r * a.KW + s) * a.Cin + cb * BK;
+                    if constexpr (PAIR) {
+                        const uint32_t fb = full0 + 8u * stage;
+                        if (rank == 0) tc::mbar_arrive_expect_tx(full_bar(stage), 2u * (a.a_bytes + kBStage));
+                        if (FLAT)
+                            tc::tma_load_2d_pair(dA, &tmA, fb, cb * BK, m0);
+                        else
+                            tc::tma_load_4d_pair(dA, &tmA, fb, cb * BK, ow0 * a.stride - a.pad_w + s,
+                                                 oh0 * a.stride - a.pad_h + r, n);
+                        tc::tma_load_2d_pair(dB, &tmB, fb, kx, nb * BN + (int)rank * kBRows);
+                    } else {
+                        tc::mbar_arrive_expect_tx(full_bar(stage), a.a_bytes + kBStage);
+                        if (FLAT)
+                            tc::tma_load_2d(dA, &tmA, full_bar(stage), cb * BK, m0);
+                        else
+                            tc::tma_load_4d(dA, &tmA, full_bar(stage), cb * BK,
+                                            ow0 * a.stride - a.pad_w + s, oh0 * a.stride - a.pad_h + r, n);
+                        tc::tma_load_2d(dB, &tmB, full_bar(stage), kx, nb * BN);
+                    }
                     if (++stage == stages) { stage = 0; phase ^= 1u; }
                     if (++cb == a.cblocks) {
                         cb = 0;
@@ -286,17 +330,17 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // ------------------------------------------------ MMA issuer (pair mode: even CTA only)
+        if (lane == 0 && rank == 0) {
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
             int lt = 0;
-            for (int tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x, ++lt) {
+            for (int tile = unit; tile < a.num_tiles && ok; tile += units, ++lt) {
                 const int buf = lt & 1;
                 const uint32_t use = (uint32_t)(lt >> 1);
-                if (!wait_bounded(tempty_bar(buf), (use & 1u) ^ 1u, abort_flag, a.status,
-                                  KSTATUS_TIMEOUT_MMA))
+                if (!wait_bounded<PAIR>(tempty_bar(buf), (use & 1u) ^ 1u, abort_flag, a.status,
+                                        KSTATUS_TIMEOUT_MMA))
                     break;
                 tc::fence_after_sync();
                 const uint32_t d = tmem_base + (uint32_t)(buf * kAcc);
@@ -312,15 +356,26 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     for (int k = 0; k < BK / 16; ++k) {
                         const uint64_t pd = tc::smem_desc_kmajor(aS + 32u * k, kRowBytes);  // pixels
                         const uint64_t wd = tc::smem_desc_kmajor(bS + 32u * k, kRowBytes);  // weights
-                        if (SWAP)
+                        if (PAIR)
+                            tc::mma_bf16_pair(d, pd, wd, kIdesc, (kb | k) != 0 ? 1u : 0u);
+                        else if (SWAP)
                             tc::mma_bf16(d, wd, pd, kIdesc, (kb | k) != 0 ? 1u : 0u);
                         else
                             tc::mma_bf16(d, pd, wd, kIdesc, (kb | k) != 0 ? 1u : 0u);
                     }
-                    tc::mma_commit(empty_bar(stage));  // stage free once these MMAs complete
+                    // stage free (in both CTAs of a pair) once these MMAs complete
+                    if (PAIR)
+                        tc::mma_commit_pair(empty_bar(stage), 0x3);
+                    else
+                        tc::mma_commit(empty_bar(stage));
                     if (++stage == stages) { stage = 0; phase ^= 1u; }
                 }
-                if (ok) tc::mma_commit(tfull_bar(buf));  // accumulator ready
+                if (ok) {  // accumulator ready
+                    if (PAIR)
+                        tc::mma_commit_pair(tfull_bar(buf), 0x3);
+                    else
+                        tc::mma_commit(tfull_bar(buf));
+                }
             }
         }
     } else {
@@ -336,7 +391,9 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         const uint32_t sStage = sOut + (uint32_t)(grp * a.out_bufs) * kOutStage;  // this group's staging
         int oc = 0;  // TMA stores this group has issued (selects the staging buffer)
         int lt = 0;
-        for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x, ++lt) {
+        // pair mode: accumulator-empty arrivals go to the even CTA's barrier
+        const uint32_t tempty0 = PAIR ? tc::mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
+        for (int tile = unit; tile < a.num_tiles; tile += units, ++lt) {
             const int buf = lt & 1;
             const uint32_t use = (uint32_t)(lt >> 1);
             const bool got = wait_bounded(tfull_bar(buf), use & 1u, abort_flag, a.status,
@@ -359,7 +416,12 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 tc::tmem_ld_32x32(tbase + (uint32_t)c, *reinterpret_cast<uint32_t(*)[32]>(acc + c));
             tc::tmem_ld_wait();
             tc::fence_before_sync();
-            tc::mbar_arrive(tempty_bar(buf));
+            if constexpr (PAIR) {
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive_cluster(tempty0 + 8u * buf);
+            } else {
+                tc::mbar_arrive(tempty_bar(buf));
+            }
 
             // Output slice: bias, activation, bf16, staged in shared memory
             // (64-byte swizzle, matching the store's tensor map) and written by
@@ -367,7 +429,8 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             // bh x bw pixel rectangle (or 128 flat rows): rows past it are
             // never stored and pixels outside the image are clipped by TMA.
             const int nb = tile % a.tiles_n;
-            const int mt = tile / a.tiles_n;
+            const int mt = PAIR ? (tile / a.tiles_n) * 2 + (int)rank : tile / a.tiles_n;
+            if (PAIR && mt >= a.tiles_m) continue;  // the empty half of the last pair tile
             int n = 0, oh0 = 0, ow0 = 0, m0 = 0;
             if (FLAT) {
                 m0 = mt * kPix;
@@ -462,9 +525,15 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     __syncwarp();
     tc::fence_before_sync();
     __syncthreads();
+    // pair mode: neither CTA leaves (or frees TMEM) while the other may still
+    // use its shared memory or TMEM
+    if constexpr (PAIR) tc::cluster_sync();
     if (warp == 1) {
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem_base, kTmemCols);
+        if constexpr (PAIR)
+            tc::tmem_dealloc_pair(tmem_base, kTmemCols);
+        else
+            tc::tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
@@ -488,9 +557,9 @@ CUtensorMapSwizzle swizzle_for(int bk) {
     return bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : (bk == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
 }
 
-template <int BN, int BK, bool FLAT, bool SWAP>
+template <int BN, int BK, bool FLAT, bool SWAP, bool PAIR = false>
 void *kernel_ptr() {
-    return reinterpret_cast<void *>(&igemm_bf16_kernel<BN, BK, FLAT, SWAP>);
+    return reinterpret_cast<void *>(&igemm_bf16_kernel<BN, BK, FLAT, SWAP, PAIR>);
 }
 
 template <int BN, int BK>
@@ -512,7 +581,19 @@ void *kernel_ptr_swap(bool flat) {
     return flat ? kernel_ptr<128, BK, true, true>() : kernel_ptr<128, BK, false, true>();
 }
 
-void *select_kernel(int bn, int bk, bool flat, bool swap) {
+template <int BK>
+void *kernel_ptr_pair(bool flat) {
+    return flat ? kernel_ptr<256, BK, true, false, true>() : kernel_ptr<256, BK, false, false, true>();
+}
+
+void *select_kernel(int bn, int bk, bool flat, bool swap, bool pair) {
+    if (pair) {
+        switch (bk) {
+        case 64: return kernel_ptr_pair<64>(flat);
+        case 32: return kernel_ptr_pair<32>(flat);
+        default: return kernel_ptr_pair<16>(flat);
+        }
+    }
     if (swap) {
         switch (bk) {
         case 64: return kernel_ptr_swap<64>(flat);
@@ -590,13 +671,16 @@ int igemm_configure(conv_plan *p, int layout) {
     }
     g.kblocks = p->s.k_h * g.kw * g.cblocks;
 
-    // Candidate layouts: swapped (Cout <= 128) with 256-pixel tiles, or
-    // normal with 128-pixel tiles and BN in {256, 128, 64}.  Each is scored
-    // by an estimate of its time: waves x (per-tile cost + fixed cost), the
-    // per-tile cost being the largest of
+    // Candidate layouts: swapped (Cout <= 128) with 256-pixel tiles; normal
+    // with 128-pixel tiles and BN in {256, 128, 64}; the CTA pair with
+    // 2 x 128-pixel tiles and BN = 256.  Each is scored by an estimate of
+    // its time: waves x (per-tile cost + fixed cost), the per-tile cost
+    // (per SM) being the largest of
     //   MMA issue   128 cycles per K=16 step whatever N is (so N = 256 is
     //               the only full-rate width),
-    //   operand feed (pixels + BN) * K * 2 bytes from L2 at ~80 B/cycle,
+    //   shared memory  the staged operand bytes are written once by TMA and
+    //               read once by the MMAs: 2 * (pixel rows + weight rows
+    //               staged) * K * 2 bytes at 128 B/cycle,
     //   epilogue    accumulator lanes x columns (wasted lanes included)
     //               x cycles per value / 128 lanes per cycle per SM,
     // with the epilogue costing ~16 cycles per value with Mish (two MUFU
@@ -604,11 +688,13 @@ int igemm_configure(conv_plan *p, int layout) {
     const long long K = (long long)p->s.k_h * g.kw * cin;
     const long long epi_c = p->dtype == CONV_I8 ? 10 : (p->act == CONV_ACT_MISH ? 16 : 6);
     long long best_cost = -1, best_tiles = 0;
-    for (int cand = 0; cand < 4; ++cand) {
+    for (int cand = 0; cand < 5; ++cand) {
         const bool swap = cand == 0;
+        const bool pair = cand == 4;
         if (swap && p->s.c_out > 128) continue;
+        if (pair && p->num_sms < 2) continue;
         if (layout != 0 && layout != cand + 1) continue;
-        const int bn = swap ? 128 : (cand == 1 ? 256 : (cand == 2 ? 128 : 64));
+        const int bn = swap ? 128 : (cand == 1 || pair ? 256 : (cand == 2 ? 128 : 64));
         const int P = swap ? kBMSwap : kBM;
         int bw = P, bh = 1, tw = 1, th = 1;
         long long tiles_m;
@@ -635,12 +721,14 @@ int igemm_configure(conv_plan *p, int layout) {
             tiles_m = best;
         }
         const long long tiles_n = swap ? 1 : (p->s.c_out + bn - 1) / bn;
-        const long long tiles = tiles_m * tiles_n;
-        const long long waves = (tiles + p->num_sms - 1) / p->num_sms;
+        // pair mode: a unit of work is a pair tile on two SMs
+        const long long tiles = (pair ? (tiles_m + 1) / 2 : tiles_m) * tiles_n;
+        const long long slots = pair ? p->num_sms / 2 : p->num_sms;
+        const long long waves = (tiles + slots - 1) / slots;
         const long long t_mma = K / 16 * 128;
-        const long long t_feed = (P + bn) * K * 2 / 80;
+        const long long t_smem = (P + (pair ? bn / 2 : bn)) * K / 32;
         const long long t_epi = 128LL * (swap ? P : bn) * epi_c / 128;
-        long long t_tile = t_mma > t_feed ? t_mma : t_feed;
+        long long t_tile = t_mma > t_smem ? t_mma : t_smem;
         if (t_epi > t_tile) t_tile = t_epi;
         const long long cost = waves * (t_tile + 500);
         // ties: more tiles (more SMs busy), then the narrower N tile
@@ -648,15 +736,16 @@ int igemm_configure(conv_plan *p, int layout) {
             (cost == best_cost && tiles == best_tiles && bn < g.bn)) {
             best_cost = cost;
             best_tiles = tiles;
-            g.swap = swap ? 1 : 0; g.bn = bn; g.tiles_n = (int)tiles_n; g.tiles_m = (int)tiles_m;
+            g.swap = swap ? 1 : 0; g.pair = pair ? 1 : 0; g.bn = bn; g.tiles_n = (int)tiles_n;
+            g.tiles_m = (int)tiles_m;
             g.bw = bw; g.bh = bh; g.tiles_w = tw; g.tiles_h = th;
         }
     }
     if (best_cost < 0) return CONV_ERR_UNSUPPORTED;  // forced swapped layout with c_out > 128
-    const int P = g.swap ? kBMSwap : kBM;  // pixels per tile
-    g.num_tiles = g.tiles_n * g.tiles_m;
+    const int P = g.swap ? kBMSwap : kBM;  // pixels per tile (per CTA)
+    g.num_tiles = g.tiles_n * (g.pair ? (g.tiles_m + 1) / 2 : g.tiles_m);  // work units
 
-    const int stage_bytes = (P + g.bn) * g.bk * 2;
+    const int stage_bytes = (P + (g.pair ? g.bn / 2 : g.bn)) * g.bk * 2;
     // Epilogue staging: swapped mode, 16 transpose rows per group; normal
     // mode, 128 rows x 64 B per group and buffer.  Two buffers per group let
     // a group fill one while the TMA store of the other is still reading it;
@@ -674,17 +763,38 @@ int igemm_configure(conv_plan *p, int layout) {
     // this persistent kernel share an SM: each CTA then owns its TMEM
     // columns (at most 512) without waiting for another to free them.
     if (g.smem < 116 * 1024) g.smem = 116 * 1024;
-    g.grid = g.num_tiles < p->num_sms ? g.num_tiles : p->num_sms;
-
     if (!tensor_map_encoder()) return CONV_ERR_CUDA;
-    const int rc = conv_grant_smem(select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0), p->device, g.smem);
+    void *kern = select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0, g.pair != 0);
+    const int rc = conv_grant_smem(kern, p->device, g.smem);
     if (rc != CONV_OK) return rc;
+    if (g.pair) {
+        // as many CTA pairs as can be resident at once (a pair occupies two
+        // SMs of one GPC), at most one per work unit
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * g.num_tiles);
+        cfg.blockDim = dim3(cta_threads(g.bn, false));
+        cfg.dynamicSmemBytes = (size_t)g.smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2; attr.val.clusterDim.y = 1; attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1)
+            return CONV_ERR_UNSUPPORTED;
+        g.grid = 2 * (g.num_tiles < clusters ? g.num_tiles : clusters);
+    } else {
+        g.grid = g.num_tiles < p->num_sms ? g.num_tiles : p->num_sms;
+    }
     snprintf(p->desc, sizeof(p->desc),
              "igemm_%s_tcgen05 %s%s %s BK=%d tile=%dx%d stages=%d out_bufs=%d tiles=%d grid=%d",
              p->dtype == CONV_I8 ? (g.fold ? "i8-as-bf16-kwfold" : "i8-as-bf16")
                                  : (g.fold ? "bf16-cpad-kwfold" : (g.prep ? "bf16-cpad" : "bf16")),
              g.flat ? "flat" : "spatial",
-             g.swap ? " swapped" : "", g.swap ? "M=128co N=256px" : (g.bn == 256 ? "M=128px N=256co" : (g.bn == 128 ? "M=128px N=128co" : "M=128px N=64co")),
+             g.swap ? " swapped" : (g.pair ? " cta-pair" : ""),
+             g.swap ? "M=128co N=256px"
+                    : (g.pair ? "M=256px N=256co"
+                              : (g.bn == 256 ? "M=128px N=256co" : (g.bn == 128 ? "M=128px N=128co" : "M=128px N=64co"))),
              g.bk, g.bh, g.bw, g.stages, g.out_bufs, g.num_tiles, g.grid);
     return CONV_OK;
 }
@@ -727,7 +837,7 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
         const cuuint64_t K = (cuuint64_t)p->s.k_h * g.kw * cin;
         const cuuint64_t dims[2] = {K, (cuuint64_t)p->s.c_out};
         const cuuint64_t strides[1] = {K * 2};
-        const cuuint32_t box[2] = {(cuuint32_t)g.bk, (cuuint32_t)g.bn};
+        const cuuint32_t box[2] = {(cuuint32_t)g.bk, (cuuint32_t)(g.pair ? g.bn / 2 : g.bn)};
         rc = encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(w), dims, strides, box, ones,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(g.bk), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -766,6 +876,7 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
     a.stride = S; a.pad_h = p->pad_h; a.pad_w = g.padw; a.OH = p->oh; a.OW = p->ow;
     a.bw = g.bw; a.bh = g.bh; a.tiles_w = g.tiles_w; a.tiles_h = g.tiles_h; a.tiles_n = g.tiles_n;
     a.num_tiles = g.num_tiles; a.cblocks = g.cblocks; a.kblocks = g.kblocks; a.stages = g.stages;
+    a.tiles_m = g.tiles_m;
     a.M = (long long)p->s.n * p->s.h * g.wx;
     a.a_bytes = (uint32_t)((g.flat ? (g.swap ? kBMSwap : kBM) : g.bw * g.bh) * g.bk * 2);
     a.flat = g.flat;
@@ -777,9 +888,23 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
     a.out_bufs = g.out_bufs;
     a.status = p->d_status;
 
-    void *k = select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0);
+    void *k = select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0, g.pair != 0);
     void *args[] = {&tmA, &tmB, &tmY, &a};
-    cudaError_t e =
-        cudaLaunchKernel(k, dim3(g.grid), dim3(cta_threads(g.bn, g.swap != 0)), args, (size_t)g.smem, st);
+    cudaError_t e;
+    if (g.pair) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(g.grid);
+        cfg.blockDim = dim3(cta_threads(g.bn, false));
+        cfg.dynamicSmemBytes = (size_t)g.smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2; attr.val.clusterDim.y = 1; attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelExC(&cfg, k, args);
+    } else {
+        e = cudaLaunchKernel(k, dim3(g.grid), dim3(cta_threads(g.bn, g.swap != 0)), args, (size_t)g.smem, st);
+    }
     return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }

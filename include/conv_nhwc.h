@@ -100,6 +100,7 @@ typedef enum {
     CONV_ALGO_IGEMM_N256 = 5,    /* MMA M = 128 pixels, N = 256 output channels */
     CONV_ALGO_IGEMM_N128 = 6,    /* MMA M = 128 pixels, N = 128 output channels */
     CONV_ALGO_IGEMM_N64 = 7,     /* MMA M = 128 pixels, N = 64 output channels  */
+    CONV_ALGO_IGEMM_PAIR = 8,    /* CTA-pair MMA on two SMs: M = 256 pixels, N = 256 */
 } conv_algo_t;
 
 enum {

@@ -66,15 +66,15 @@ IGEMM = [
 
 
 # Every case runs with the layout the plan picks and with each forced tile
-# layout: swapped (c_out <= 128 only), N = 256, 128 and 64.
-_LAYOUT_DESC = {"igemm_swapped": "swapped", "igemm_n256": "N=256co", "igemm_n128": "N=128co",
-                "igemm_n64": "N=64co"}
+# layout: swapped (c_out <= 128 only), N = 256, 128 and 64, and the CTA pair.
+_LAYOUT_DESC = {"igemm_swapped": "swapped", "igemm_n256": "M=128px N=256co", "igemm_n128": "N=128co",
+                "igemm_n64": "N=64co", "igemm_pair": "cta-pair"}
 
 
 def with_layouts(specs):
     out = []
     for spec in specs:
-        for lay in ["igemm", "igemm_swapped", "igemm_n256", "igemm_n128", "igemm_n64"]:
+        for lay in ["igemm", "igemm_swapped", "igemm_n256", "igemm_n128", "igemm_n64", "igemm_pair"]:
             if lay == "igemm_swapped" and spec.cout > 128:
                 continue
             out.append(pytest.param(spec, lay, id=f"{spec.name}-{lay}"))
