@@ -206,8 +206,9 @@ int conv_plan_create_ex(const conv_shape_t *shape, int stride, int pad_h, int pa
     } else if (chosen == CONV_ALGO_DEPTHWISE) {
         rc = dw3x3_configure(p);
         if (rc != CONV_OK) { conv_plan_destroy(p); return rc; }
-        snprintf(p->desc, sizeof(p->desc), "dw3x3 %s tile=%dx%dx%dch halo=%dx%d threads=%d blocks=%lld",
-                 dtype == CONV_F32 ? "f32" : (dtype == CONV_BF16 ? "bf16" : "i8"), p->dw.th, p->dw.tw,
+        snprintf(p->desc, sizeof(p->desc), "dw3x3 %s%s tile=%dx%dx%dch halo=%dx%d threads=%d blocks=%lld",
+                 dtype == CONV_F32 ? "f32" : (dtype == CONV_BF16 ? "bf16" : "i8"), p->dw.kind == 1 ? " rows" : "",
+                 p->dw.th, p->dw.tw,
                  p->dw.cbv * (dtype == CONV_I8 ? 16 : 4), p->dw.hin, p->dw.win, p->dw.threads, p->dw.blocks);
     } else {
         direct_configure(p);

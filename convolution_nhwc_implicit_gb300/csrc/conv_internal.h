@@ -43,6 +43,7 @@ struct IgemmGeom {
 };
 
 struct DwGeom {
+    int kind;      // 0: general kernel; 1: bf16 stride-1 rolling-row kernel
     int th, tw;    // output rows / columns of one CTA tile
     int cbv;       // 16-byte channel vectors per tile
     int hin, win;  // input halo rows / columns (one TMA box)

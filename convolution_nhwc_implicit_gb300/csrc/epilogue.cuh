@@ -36,6 +36,41 @@ __device__ __forceinline__ float mish_fast(float v) {
     return v * __fdividef(t, t + 2.0f);
 }
 
+// Packed fp32 pairs (the sm_100 family's f32x2 instructions, through CUDA's
+// float2 builtins): each lane of the pair is rounded once, exactly like the
+// scalar instruction.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+// Hardware 2^x and 1/x approximations (MUFU), subnormals flushed.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Mish of two values for bf16 outputs, in the Wormhole page's form
+// mish(v) = v (1 - 2 / ((1 + e^v)^2 + 1)) (section 9, K1), with e^v =
+// 2^(v log2 e).  No clamp is needed: past v ~ 44 the square overflows to
+// +inf and the reciprocal to 0, giving v; for v << 0 the bracket is
+// 1 - (1 - e^v) (cancellation, absolute error ~|v| 2^-24, far below bf16
+// resolution of the result's scale).  Two MUFU operations per value, the
+// rest in packed pairs.
+__device__ __forceinline__ float2 mish2_fast(float2 v) {
+    const float2 e = mul2(v, make_float2(1.4426950408889634f, 1.4426950408889634f));
+    const float2 n = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+    const float2 w = add2(n, make_float2(1.0f, 1.0f));
+    const float2 d = fma2(w, w, make_float2(1.0f, 1.0f));
+    const float2 r = make_float2(rcp_approx(d.x), rcp_approx(d.y));
+    const float2 s = fma2(r, make_float2(-2.0f, -2.0f), make_float2(1.0f, 1.0f));
+    return mul2(v, s);
+}
+
 // Activation for bf16 outputs.
 __device__ __forceinline__ float activate_fast(float v, int act) {
     if (act == ACT_RELU) return fmaxf(v, 0.0f);

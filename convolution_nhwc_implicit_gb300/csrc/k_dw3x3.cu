@@ -82,6 +82,8 @@ template <typename T> __host__ __device__ constexpr int V_OF() { return DwT<T>::
 
 // Two fp32 FMAs in one packed instruction (each lane rounded once, like
 // two __fmaf_rn): (d0, d1) = (a0 * b0 + c0, a1 * b1 + c1).
+// (Inline PTX here: with the float2 builtin the register allocation of the
+// general kernel below spills.)
 __device__ __forceinline__ void ffma2(float &d0, float &d1, float a0, float a1, float b0, float b1, float c0,
                                       float c1) {
     asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
@@ -287,6 +289,147 @@ dw3x3_float_kernel(const __grid_constant__ CUtensorMap tmX, const T *__restrict_
     }
 }
 
+// bf16, stride 1: rolling row accumulators.  A thread owns 4 channels x 2
+// adjacent output columns of the tile and walks down its input halo rows
+// once.  Each input row (4 pixels: the two columns' 3-wide windows overlap)
+// is loaded and widened once and feeds the three output rows whose windows
+// contain it (as their tap row 2, 1 and 0), whose partial sums stay in
+// registers; an output row is finished when its tap row 2 has been added:
+// activation, bf16, one 8-byte store per column.  Per output value that is
+// half a shared-memory load, two widening operations and 4.5 packed FMAs.
+// The tile (CBV 4-channel vectors x TW columns x TH rows) is a compile-time
+// shape: the walk is fully unrolled, the rolling accumulators are plain
+// registers and every shared-memory address is an immediate offset.
+template <int CBV, int TW, int TH>
+__global__ void __launch_bounds__(CBV * TW / 2, (CBV * TW / 2) <= 128 ? 4 : 2)
+dw3x3_bf16_rows_kernel(const __grid_constant__ CUtensorMap tmX, const __nv_bfloat16 *__restrict__ w,
+                       const DwArgs a) {
+    constexpr int kWin = TW + 2, kHin = TH + 2;
+    constexpr uint32_t kPix = CBV * 8;  // bytes of one halo pixel: CBV vectors of 4 bf16
+    constexpr uint32_t kHalo = kHin * kWin * kPix;
+    constexpr uint32_t kBuf = (kHalo + 127u) & ~127u;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t bars[2];
+    const uint32_t sbase = tc::smem_u32(smem);
+    const uint32_t sbar0 = tc::smem_u32(&bars[0]);
+    if (threadIdx.x == 0) {
+        tc::mbar_init(sbar0, 1);
+        tc::mbar_init(sbar0 + 8, 1);
+        tc::fence_mbar_init();
+        if ((int)blockIdx.x < a.tiles_total) issue_halo<4>(&tmX, a, sbase, sbar0, blockIdx.x, 1, kHalo);
+    }
+    __syncwarp();
+    __syncthreads();
+
+    const int cv = threadIdx.x % CBV;
+    const int cp = threadIdx.x / CBV;  // column pair (all CBV * TW / 2 threads are active)
+    const int tcb = blockIdx.x % a.tiles_c;  // the same for all of this CTA's tiles
+    const int c0 = (tcb * CBV + cv) * 4;
+
+    // Weights (OHWI [C][3][3]: the 4 channels' 36 taps are contiguous) as
+    // fp32 pairs wt[k][q] = (w[c0 + 2q][k], w[c0 + 2q + 1][k]); bias pairs.
+    float2 wt[9][2];
+    float2 bv[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    {
+        const uint2 *wp = reinterpret_cast<const uint2 *>(w + (long long)c0 * 9);
+        float raw[36];
+#pragma unroll
+        for (int i = 0; i < 9; ++i) {
+            const uint2 u = __ldg(wp + i);
+            raw[4 * i + 0] = __uint_as_float(u.x << 16);
+            raw[4 * i + 1] = __uint_as_float(u.x & 0xffff0000u);
+            raw[4 * i + 2] = __uint_as_float(u.y << 16);
+            raw[4 * i + 3] = __uint_as_float(u.y & 0xffff0000u);
+        }
+#pragma unroll
+        for (int k = 0; k < 9; ++k) {
+            wt[k][0] = make_float2(raw[k], raw[9 + k]);
+            wt[k][1] = make_float2(raw[18 + k], raw[27 + k]);
+        }
+        const float *b = reinterpret_cast<const float *>(a.bias);
+        if (b) {
+            const float4 b4 = __ldg(reinterpret_cast<const float4 *>(b + c0));
+            bv[0] = make_float2(b4.x, b4.y);
+            bv[1] = make_float2(b4.z, b4.w);
+        }
+    }
+    const long long ystep = (long long)a.OW * a.C;
+    const int act = a.act;
+    int k = 0;
+    for (int t = blockIdx.x; t < a.tiles_total; t += gridDim.x, ++k) {
+        const int buf = k & 1;
+        if (threadIdx.x == 0 && t + (int)gridDim.x < a.tiles_total)
+            issue_halo<4>(&tmX, a, sbase + (buf ^ 1) * kBuf, sbar0 + 8 * (buf ^ 1), t + gridDim.x, 1, kHalo);
+        const bool ok = wait_halo(sbar0 + 8 * buf, (uint32_t)(k >> 1) & 1u, a.status);
+        if (__syncthreads_or(!ok)) return;  // block-uniform give-up
+        const DwTile d = tile_of(a, t);
+        const uint8_t *hp = smem + buf * kBuf + cv * 8 + (2 * cp) * kPix;
+        const int ow = d.ow0 + 2 * cp;
+        const bool st0 = ow < a.OW, st1 = ow + 1 < a.OW;
+        const int rows = a.OH - d.oh0;  // output rows of this tile inside the image (may exceed TH)
+        __nv_bfloat16 *yp = reinterpret_cast<__nv_bfloat16 *>(a.y) +
+                            (((long long)d.n * a.OH + d.oh0) * a.OW + ow) * a.C + c0;
+        float2 acc[3][2][2];  // [output row % 3][column][channel pair]
+#pragma unroll
+        for (int hr = 0; hr < TH + 2; ++hr) {
+            float2 xv[4][2];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const uint2 u = *reinterpret_cast<const uint2 *>(hp + (hr * kWin + p) * kPix);
+                xv[p][0] = make_float2(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u));
+                xv[p][1] = make_float2(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+            }
+            // input row hr is tap row r of output row hr - r; tap s outermost
+            // so that consecutive FMAs feed independent accumulators
+#pragma unroll
+            for (int s = 0; s < 3; ++s)
+#pragma unroll
+                for (int r = 0; r < 3; ++r) {
+                    const int o = hr - r;
+                    if (o < 0 || o >= TH) continue;
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+#pragma unroll
+                        for (int q = 0; q < 2; ++q)
+                            acc[o % 3][j][q] = fma2(xv[j + s][q], wt[r * 3 + s][q],
+                                                    (r == 0 && s == 0) ? bv[q] : acc[o % 3][j][q]);
+                }
+            if (hr >= 2) {  // output row hr - 2 has all its taps
+                const int o = hr - 2;
+                if (o < rows) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        float2 v0 = acc[o % 3][j][0], v1 = acc[o % 3][j][1];
+                        if (act == ACT_MISH) {
+                            v0 = mish2_fast(v0);
+                            v1 = mish2_fast(v1);
+                        } else if (act == ACT_RELU) {
+                            v0 = make_float2(fmaxf(v0.x, 0.f), fmaxf(v0.y, 0.f));
+                            v1 = make_float2(fmaxf(v1.x, 0.f), fmaxf(v1.y, 0.f));
+                        }
+                        __nv_bfloat162 lo = __floats2bfloat162_rn(v0.x, v0.y);
+                        __nv_bfloat162 hi = __floats2bfloat162_rn(v1.x, v1.y);
+                        if (j == 0 ? st0 : st1)
+                            *reinterpret_cast<uint2 *>(yp + j * a.C) =
+                                make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+                    }
+                }
+                yp += ystep;
+            }
+        }
+        __syncwarp();
+        __syncthreads();  // this buffer is free for the TMA two tiles ahead
+    }
+}
+
+// Tile shapes of the rolling-row kernel (CBV x TW x TH): whole warps, at most
+// 256 threads.
+#define DW_ROWS_SHAPES(X) \
+    X(32, 8, 8) X(32, 8, 4) X(32, 4, 8) X(32, 4, 4) X(32, 16, 8) X(32, 16, 4) \
+    X(16, 8, 8) X(16, 8, 4) X(16, 16, 8) X(16, 16, 4) X(16, 32, 8) X(16, 32, 4) \
+    X(8, 8, 8) X(8, 8, 4) X(8, 16, 8) X(8, 16, 4) X(8, 32, 8) X(8, 32, 4) \
+    X(4, 16, 8) X(4, 16, 4) X(4, 32, 8) X(4, 32, 4) X(2, 32, 8) X(2, 32, 4)
+
 // int8: 16 channels per thread, packed window and weights, exact int32.
 template <int S>
 __global__ void __launch_bounds__(256, 2)
@@ -417,6 +560,14 @@ void *kernel_for(int stride) {
     return reinterpret_cast<void *>(&dw3x3_float_kernel<T, 0>);
 }
 
+void *select_rows(int cbv, int tw, int th) {
+#define DW_ROWS_CASE(C, W, H) \
+    if (cbv == C && tw == W && th == H) return reinterpret_cast<void *>(&dw3x3_bf16_rows_kernel<C, W, H>);
+    DW_ROWS_SHAPES(DW_ROWS_CASE)
+#undef DW_ROWS_CASE
+    return nullptr;
+}
+
 void *select(conv_dtype_t dt, int stride) {
     switch (dt) {
     case CONV_F32: return kernel_for<float>(stride);
@@ -447,8 +598,62 @@ bool dw3x3_supported(const conv_plan *p) {
     return true;  // tile counts fit an int: at most N*H*W tiles
 }
 
+// bf16 stride-1 layers: the rolling-row kernel.  Tile = th x tw output
+// pixels x 4 cbv channels, a thread per 4 channels x 2 columns.  Among tiles
+// of whole warps whose two halo buffers leave room for two CTAs per SM, the
+// one with the least estimated work on the busiest SM: tiles per SM x (halo
+// bytes + output bytes + a per-row cost of the TMA box + a fixed cost).
+static int dw3x3_rows_configure(conv_plan *p) {
+    const int C = p->s.c_in;
+    DwGeom &g = p->dw;
+    long long best = -1;
+    for (int cbv : {32, 16, 8, 4, 2}) {
+        if ((C / 4) % cbv != 0) continue;
+        for (int tw = 2; tw <= 32; tw += 2) {
+            const int threads = cbv * tw / 2;
+            if (threads > 256) break;
+            if (threads % 32 != 0) continue;
+            for (int th : {8, 4}) {
+                if (!select_rows(cbv, tw, th)) continue;  // shapes with a compiled kernel only
+                const int win = tw + 2, hin = th + 2;
+                const int halo = hin * win * cbv * 8;
+                const int smem = 2 * ((halo + 127) & ~127);
+                if (smem > 110 * 1024) continue;
+                const long long tiles = (long long)(C / 4 / cbv) * ((p->ow + tw - 1) / tw) *
+                                        ((p->oh + th - 1) / th) * p->s.n;
+                const long long per_sm = (tiles + p->num_sms - 1) / p->num_sms;
+                const long long cost = per_sm * (halo + tw * th * cbv * 8 + hin * win * 64 + 2048);
+                if (best < 0 || cost < best || (cost == best && threads > g.threads)) {
+                    best = cost;
+                    g.cbv = cbv; g.tw = tw; g.th = th; g.threads = threads; g.smem = smem;
+                    g.hin = hin; g.win = win;
+                }
+            }
+        }
+    }
+    if (best < 0) return CONV_ERR_UNSUPPORTED;
+    g.kind = 1;
+    g.tiles_w = (p->ow + g.tw - 1) / g.tw;
+    g.tiles_h = (p->oh + g.th - 1) / g.th;
+    g.tiles_c = C / 4 / g.cbv;
+    g.tiles = (long long)g.tiles_c * g.tiles_w * g.tiles_h * p->s.n;
+    // Persistent grid: the CTAs resident at once (shared memory, threads,
+    // 128 registers a thread), a multiple of the channel-block count.
+    int res = (227 * 1024) / (g.smem + 1024);
+    if (res > 2048 / g.threads) res = 2048 / g.threads;
+    if (res > 65536 / (g.threads * 128)) res = 65536 / (g.threads * 128);
+    long long grid = (long long)p->num_sms * res;
+    if (grid > g.tiles) grid = g.tiles;
+    if (grid > g.tiles_c) grid -= grid % g.tiles_c;
+    else grid = g.tiles_c;
+    g.blocks = grid;
+    return conv_grant_smem(select_rows(g.cbv, g.tw, g.th), p->device, g.smem);
+}
+
 int dw3x3_configure(conv_plan *p) {
     const int S = p->stride;
+    p->dw.kind = 0;
+    if (p->dtype == CONV_BF16 && S == 1 && p->s.c_in % 8 == 0) return dw3x3_rows_configure(p);
     const int V = dw_chans(p->dtype);
     const int cvt = p->s.c_in / V;                 // channel vectors in a pixel
     const int maxv = 256 / dw_vbytes(p->dtype);    // at most 256 bytes of channels per tile pixel
@@ -527,7 +732,7 @@ cudaError_t launch_dw3x3(const conv_plan *p, const void *x, const void *w, const
     a.mult = p->d_mult;
     a.y = y;
     a.status = p->d_status;
-    void *k = select(p->dtype, p->stride);
+    void *k = g.kind == 1 ? select_rows(g.cbv, g.tw, g.th) : select(p->dtype, p->stride);
     void *args[] = {&tm, &w, &a};
     return cudaLaunchKernel(k, dim3((unsigned)g.blocks), dim3(g.threads), args, (size_t)g.smem, st);
 }

@@ -516,7 +516,9 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 ++oc;
             }
         }
-        if (issuer) tc::bulk_wait0();  // all of this CTA's stores are complete
+        // The staging buffers must outlive the stores' reads of them; the
+        // global writes themselves complete before the grid does.
+        if (issuer) tc::bulk_wait_read0();
     }
 
     // Warps 0 and 1 ran their loops on lane 0 only: reconverge each warp
@@ -750,9 +752,12 @@ int igemm_configure(conv_plan *p, int layout) {
     // mode, 128 rows x 64 B per group and buffer.  Two buffers per group let
     // a group fill one while the TMA store of the other is still reading it;
     // they are used when the operand ring keeps at least 4 stages.
+    // Short-K layers (few K blocks per tile) are limited by the epilogue and
+    // take the second buffer; long-K layers keep the shared memory for
+    // operand stages.
     const int one_buf = g.swap ? 4 * 16 * kTP : epi_groups(g.bn, false) * kBM * 64;
     g.out_bufs = 1;
-    if (!g.swap && (227 * 1024 - 1024 - 256 - 2 * one_buf) / stage_bytes >= 4) g.out_bufs = 2;
+    if (!g.swap && g.kblocks < 16 && (227 * 1024 - 1024 - 256 - 2 * one_buf) / stage_bytes >= 4) g.out_bufs = 2;
     const int out_bytes = one_buf * g.out_bufs;
     const int budget = 227 * 1024 - 1024 - 256 - out_bytes;
     g.stages = budget / stage_bytes;

@@ -163,6 +163,25 @@ def test_depthwise(spec):
     check(spec, "depthwise", "depthwise")
 
 
+# bf16 stride 1 runs on the rolling-row kernel: ragged row and column tiles,
+# each padding and activation, channel counts from one 8-channel block up.
+DW_ROWS = [
+    L("dwr_c8_p1_mish", 1, 9, 7, 8, 8, 3, 3, 1, 1, 1, groups=8),
+    L("dwr_c24_p0_relu", 2, 13, 11, 24, 24, 3, 3, 1, 0, 0, groups=24, act="relu"),
+    L("dwr_c40_p2_none", 1, 11, 17, 40, 40, 3, 3, 1, 2, 2, groups=40, act="none"),
+    L("dwr_c64_asym_pad", 2, 10, 23, 64, 64, 3, 3, 1, 1, 0, groups=64),
+    L("dwr_c136_ragged", 1, 21, 19, 136, 136, 3, 3, 1, 1, 1, groups=136),
+    L("dwr_c512_b3", 3, 17, 12, 512, 512, 3, 3, 1, 1, 1, groups=512, b_dist=None),
+    L("dwr_single_row", 1, 1, 30, 32, 32, 3, 3, 1, 1, 1, groups=32),
+]
+
+
+@pytest.mark.parametrize("spec", DW_ROWS, ids=lambda s: s.name)
+def test_depthwise_rows(spec):
+    plan = check(spec, "depthwise", "depthwise")
+    assert " rows " in plan.describe(), plan.describe()
+
+
 # ------------------------------------------------ direct (CUDA cores)
 
 DIRECT = [
