@@ -78,6 +78,13 @@ __device__ __forceinline__ float activate_fast(float v, int act) {
     return v;
 }
 
+// Two values at a time (packed Mish), for bf16 outputs.
+__device__ __forceinline__ float2 activate2_fast(float2 v, int act) {
+    if (act == ACT_RELU) return make_float2(fmaxf(v.x, 0.0f), fmaxf(v.y, 0.0f));
+    if (act == ACT_MISH) return mish2_fast(v);
+    return v;
+}
+
 __device__ __forceinline__ float activate(float v, int act) {
     if (act == ACT_RELU) return fmaxf(v, 0.0f);
     if (act == ACT_MISH) return mish_f32(v);

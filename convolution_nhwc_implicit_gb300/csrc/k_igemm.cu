@@ -146,9 +146,11 @@ __device__ __forceinline__ void epilogue_swapped(const IgArgs &a, int tile, uint
             }
         } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const __nv_bfloat16 h = __float2bfloat16_rn(activate_fast(__uint_as_float(acc[c + i]) + fbias, a.act));
-                *reinterpret_cast<__nv_bfloat16 *>(tbuf + i * kTP + row * 2) = h;
+            for (int i = 0; i < 16; i += 2) {
+                const float2 v = activate2_fast(
+                    make_float2(__uint_as_float(acc[c + i]) + fbias, __uint_as_float(acc[c + i + 1]) + fbias), a.act);
+                *reinterpret_cast<__nv_bfloat16 *>(tbuf + i * kTP + row * 2) = __float2bfloat16_rn(v.x);
+                *reinterpret_cast<__nv_bfloat16 *>(tbuf + (i + 1) * kTP + row * 2) = __float2bfloat16_rn(v.y);
             }
         }
         tc::named_bar_sync(1 + grp, 128);
@@ -494,8 +496,8 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         uint32_t pk[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            __nv_bfloat162 h2 = __floats2bfloat162_rn(activate_fast(v[2 * e], a.act),
-                                                                      activate_fast(v[2 * e + 1], a.act));
+                            const float2 f = activate2_fast(make_float2(v[2 * e], v[2 * e + 1]), a.act);
+                            __nv_bfloat162 h2 = __floats2bfloat162_rn(f.x, f.y);
                             pk[e] = *reinterpret_cast<uint32_t *>(&h2);
                         }
                         const uint32_t dst = srow + ((((uint32_t)j) ^ swz) << 4);
