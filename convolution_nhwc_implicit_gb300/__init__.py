@@ -44,6 +44,10 @@ class _Shape(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("n", "h", "w", "c_in", "c_out", "k_h", "k_w")]
 
 
+class _Output(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("y_channels", "y_channel_offset", "upsample", "residual")]
+
+
 class _Quant(ctypes.Structure):
     _fields_ = [("in_scale", ctypes.c_float), ("out_scale", ctypes.c_float),
                 ("w_scales", ctypes.POINTER(ctypes.c_float))]
@@ -73,8 +77,13 @@ def load_library():
     lib.conv_plan_create_ex.argtypes = [ctypes.POINTER(_Shape), c_int, c_int, c_int, c_int, c_int, c_int,
                                         ctypes.POINTER(_Quant), c_int, pp]
     lib.conv_plan_create_ex.restype = c_int
+    lib.conv_plan_create_fused.argtypes = [ctypes.POINTER(_Shape), c_int, c_int, c_int, c_int, c_int, c_int,
+                                           ctypes.POINTER(_Quant), ctypes.POINTER(_Output), c_int, pp]
+    lib.conv_plan_create_fused.restype = c_int
     lib.conv_run.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
     lib.conv_run.restype = c_int
+    lib.conv_run_fused.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+    lib.conv_run_fused.restype = c_int
     lib.conv_plan_destroy.argtypes = [c_void_p]
     lib.conv_plan_destroy.restype = None
     lib.conv_plan_output_shape.argtypes = [c_void_p, ctypes.POINTER(c_int), ctypes.POINTER(c_int)]
@@ -124,10 +133,13 @@ def _stream_handle(stream):
 
 
 class Plan:
-    """A validated layer bound to the current CUDA device (see conv_plan_create)."""
+    """A validated layer bound to the current CUDA device (see conv_plan_create).
+
+    ``out`` (optional) holds the output options of conv_plan_create_fused:
+    dict(y_channels=0, y_channel_offset=0, upsample=1, residual=False)."""
 
     def __init__(self, n, h, w, c_in, c_out, k_h, k_w, stride=1, pad_h=0, pad_w=0, groups=1,
-                 dtype="bf16", act="none", quant=None, algo="auto"):
+                 dtype="bf16", act="none", quant=None, algo="auto", out=None):
         lib = load_library()
         self._lib = lib
         self._handle = ctypes.c_void_p()
@@ -142,8 +154,16 @@ class Plan:
             self._ws = (ctypes.c_float * len(ws))(*ws)
             qp = ctypes.pointer(_Quant(float(in_scale), float(out_scale),
                                        ctypes.cast(self._ws, ctypes.POINTER(ctypes.c_float))))
-        rc = lib.conv_plan_create_ex(ctypes.byref(shape), stride, pad_h, pad_w, groups, DTYPES[dtype],
-                                     ACTS[act], qp, ALGOS[algo], ctypes.byref(self._handle))
+        op = None
+        self.out = dict(y_channels=c_out, y_channel_offset=0, upsample=1, residual=False)
+        if out is not None:
+            o = dict(self.out, **out)
+            o["y_channels"] = o["y_channels"] or c_out
+            self.out = o
+            op = ctypes.pointer(_Output(int(o["y_channels"]), int(o["y_channel_offset"]), int(o["upsample"]),
+                                        int(bool(o["residual"]))))
+        rc = lib.conv_plan_create_fused(ctypes.byref(shape), stride, pad_h, pad_w, groups, DTYPES[dtype],
+                                        ACTS[act], qp, op, ALGOS[algo], ctypes.byref(self._handle))
         if rc != 0:
             raise ConvError("conv_plan_create", rc)
         oh, ow = ctypes.c_int(), ctypes.c_int()
@@ -156,8 +176,15 @@ class Plan:
 
     @property
     def output_shape(self):
+        """Shape of the layer's own output [N, OH, OW, Cout]."""
         n, _, _, _, c_out, _, _ = self.shape
         return (n, self.oh, self.ow, c_out)
+
+    @property
+    def y_shape(self):
+        """Shape of the y buffer the plan writes into (with its output options)."""
+        u = self.out["upsample"]
+        return (self.shape[0], self.oh * u, self.ow * u, self.out["y_channels"])
 
     @property
     def algo(self) -> str:
@@ -166,9 +193,13 @@ class Plan:
     def describe(self) -> str:
         return self._lib.conv_plan_describe(self._handle).decode()
 
-    def run(self, x, w, b, y, stream=None) -> None:
-        """Enqueue y = act(conv(x, w) + b) on `stream` (default: torch's current stream)."""
-        rc = self._lib.conv_run(self._handle, _ptr(x), _ptr(w), _ptr(b), _ptr(y), _stream_handle(stream))
+    def run(self, x, w, b, y, stream=None, residual=None) -> None:
+        """Enqueue y = act(conv(x, w) + b) [+ residual] on `stream` (default: torch's current stream)."""
+        if residual is None:
+            rc = self._lib.conv_run(self._handle, _ptr(x), _ptr(w), _ptr(b), _ptr(y), _stream_handle(stream))
+        else:
+            rc = self._lib.conv_run_fused(self._handle, _ptr(x), _ptr(w), _ptr(b), _ptr(residual), _ptr(y),
+                                          _stream_handle(stream))
         if rc != 0:
             raise ConvError("conv_run", rc)
 

@@ -130,9 +130,9 @@ const char *conv_status_str(int status) {
     }
 }
 
-int conv_plan_create_ex(const conv_shape_t *shape, int stride, int pad_h, int pad_w, int groups,
-                        conv_dtype_t dtype, conv_act_t act, const conv_quant_t *quant, conv_algo_t algo,
-                        conv_plan_t **out_plan) {
+int conv_plan_create_fused(const conv_shape_t *shape, int stride, int pad_h, int pad_w, int groups,
+                           conv_dtype_t dtype, conv_act_t act, const conv_quant_t *quant,
+                           const conv_output_t *out, conv_algo_t algo, conv_plan_t **out_plan) {
     if (!out_plan) return CONV_ERR_NULL_ARG;
     *out_plan = nullptr;
     if (!shape) return CONV_ERR_NULL_ARG;
@@ -140,12 +140,29 @@ int conv_plan_create_ex(const conv_shape_t *shape, int stride, int pad_h, int pa
     int oh = 0, ow = 0;
     int rc = validate(shape, stride, pad_h, pad_w, groups, dtype, act, quant, &oh, &ow);
     if (rc != CONV_OK) return rc;
+    // Output options (validated before any CUDA call, like the layer).
+    conv_output_t o = {shape->c_out, 0, 1, 0};
+    if (out) {
+        o = *out;
+        if (o.y_channels == 0) o.y_channels = shape->c_out;
+        if (o.y_channel_offset < 0 || o.y_channels < 1 ||
+            (long long)o.y_channel_offset + shape->c_out > (long long)o.y_channels ||
+            (o.upsample != 1 && o.upsample != 2) || (o.residual != 0 && o.residual != 1))
+            return CONV_ERR_INVALID_ARG;
+        if (o.residual && dtype == CONV_I8) return CONV_ERR_UNSUPPORTED;
+        const long long es = conv_esize(dtype);
+        if ((o.y_channels * es) % 16 != 0 || (o.y_channel_offset * es) % 16 != 0) return CONV_ERR_MISALIGNED;
+        if ((long long)shape->n * oh * ow * o.upsample * o.upsample * o.y_channels >= (1ll << 40))
+            return CONV_ERR_UNSUPPORTED;
+    }
+    const bool fused = o.y_channels != shape->c_out || o.y_channel_offset != 0 || o.upsample != 1 || o.residual;
 
     conv_plan *p = new (std::nothrow) conv_plan();
     if (!p) return CONV_ERR_OOM;
     p->s = *shape;
     p->stride = stride; p->pad_h = pad_h; p->pad_w = pad_w; p->groups = groups;
     p->dtype = dtype; p->act = act; p->oh = oh; p->ow = ow;
+    p->y_c = o.y_channels; p->y_coff = o.y_channel_offset; p->up = o.upsample; p->has_res = o.residual;
 
     // Device properties.  The kernels are built for sm_103a only.
     cudaDeviceProp prop;
@@ -161,7 +178,9 @@ int conv_plan_create_ex(const conv_shape_t *shape, int stride, int pad_h, int pa
     p->num_sms = prop.multiProcessorCount;
 
     // Kernel family.
-    const bool can_ig = igemm_supported(p), can_dw = dw3x3_supported(p), can_direct = direct_supported(p);
+    // (the depthwise kernels have no output options: fused depthwise layers run on the direct kernel)
+    const bool can_ig = igemm_supported(p), can_dw = !fused && dw3x3_supported(p),
+               can_direct = direct_supported(p);
     int chosen = -1;
     if (algo == CONV_ALGO_AUTO)
         chosen = can_ig ? CONV_ALGO_IGEMM : (can_dw ? CONV_ALGO_DEPTHWISE : (can_direct ? CONV_ALGO_DIRECT : -1));
@@ -223,6 +242,13 @@ int conv_plan_create_ex(const conv_shape_t *shape, int stride, int pad_h, int pa
     return CONV_OK;
 }
 
+int conv_plan_create_ex(const conv_shape_t *shape, int stride, int pad_h, int pad_w, int groups,
+                        conv_dtype_t dtype, conv_act_t act, const conv_quant_t *quant, conv_algo_t algo,
+                        conv_plan_t **out_plan) {
+    return conv_plan_create_fused(shape, stride, pad_h, pad_w, groups, dtype, act, quant, nullptr, algo,
+                                  out_plan);
+}
+
 int conv_plan_create(const conv_shape_t *shape, int stride, int pad_h, int pad_w, int groups,
                      conv_dtype_t dtype, conv_act_t act, const conv_quant_t *quant, conv_plan_t **out_plan) {
     return conv_plan_create_ex(shape, stride, pad_h, pad_w, groups, dtype, act, quant, CONV_ALGO_AUTO,
@@ -252,27 +278,39 @@ int conv_plan_algo(const conv_plan_t *plan) {
 
 const char *conv_plan_describe(const conv_plan_t *plan) { return plan ? plan->desc : ""; }
 
-int conv_run(const conv_plan_t *plan, const void *x, const void *w, const void *bias, void *y, void *stream) {
+int conv_run_fused(const conv_plan_t *plan, const void *x, const void *w, const void *bias, const void *residual,
+                   void *y, void *stream) {
     if (!plan) return CONV_ERR_NULL_ARG;
     const conv_plan *p = plan;
+    if (p->has_res && !residual) return CONV_ERR_NULL_ARG;
+    if (!p->has_res && residual) return CONV_ERR_INVALID_ARG;
     if (p->s.n == 0) return CONV_OK;  // empty batch: nothing to compute
     if (!x || !w || !y) return CONV_ERR_NULL_ARG;
-    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias))) return CONV_ERR_MISALIGNED;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias)) ||
+        (residual && !aligned16(residual)))
+        return CONV_ERR_MISALIGNED;
     const size_t es = (size_t)conv_esize(p->dtype);
     const size_t xb = (size_t)p->s.n * p->s.h * p->s.w * p->s.c_in * es;
     const size_t wb = (size_t)p->s.c_out * p->s.k_h * p->s.k_w * (p->s.c_in / p->groups) * es;
     const size_t bb = bias ? (size_t)p->s.c_out * 4 : 0;
-    const size_t yb = (size_t)p->s.n * p->oh * p->ow * p->s.c_out * es;
-    if (overlaps(y, yb, x, xb) || overlaps(y, yb, w, wb) || overlaps(y, yb, bias, bb)) return CONV_ERR_ALIASING;
+    const size_t rb = residual ? (size_t)p->s.n * p->oh * p->ow * p->s.c_out * es : 0;
+    const size_t yb = (size_t)p->s.n * p->oh * p->up * p->ow * p->up * p->y_c * es;
+    if (overlaps(y, yb, x, xb) || overlaps(y, yb, w, wb) || overlaps(y, yb, bias, bb) ||
+        overlaps(y, yb, residual, rb))
+        return CONV_ERR_ALIASING;
 
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e;
     switch (p->algo) {
-    case CONV_ALGO_IGEMM: return launch_igemm(p, x, w, bias, y, st);
+    case CONV_ALGO_IGEMM: return launch_igemm(p, x, w, bias, residual, y, st);
     case CONV_ALGO_DEPTHWISE: e = launch_dw3x3(p, x, w, bias, y, st); break;
-    default: e = launch_direct(p, x, w, bias, y, st); break;
+    default: e = launch_direct(p, x, w, bias, residual, y, st); break;
     }
     return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+}
+
+int conv_run(const conv_plan_t *plan, const void *x, const void *w, const void *bias, void *y, void *stream) {
+    return conv_run_fused(plan, x, w, bias, nullptr, y, stream);
 }
 
 int conv_plan_check_device_status(conv_plan_t *plan, void *stream) {

@@ -70,6 +70,10 @@ struct conv_plan {
     IgemmGeom ig;
     DwGeom dw;
     int dct, dpt;      // direct kernel: channels / pixels per thread of the smem variant (dct 0: generic)
+    // Output options (conv_output_t): y has y_c channels per pixel, the layer
+    // writes channels [y_coff, y_coff + c_out) of a (up*OH) x (up*OW) grid,
+    // adding the residual tensor when has_res.
+    int y_c, y_coff, up, has_res;
     char desc[192];
 };
 
@@ -78,12 +82,12 @@ static inline int conv_esize(conv_dtype_t t) { return t == CONV_F32 ? 4 : (t == 
 
 // Launchers (stream-ordered, no allocation, no synchronisation).
 cudaError_t launch_direct(const conv_plan *p, const void *x, const void *w, const void *bias,
-                          void *y, cudaStream_t st);
+                          const void *res, void *y, cudaStream_t st);
 cudaError_t launch_dw3x3(const conv_plan *p, const void *x, const void *w, const void *bias,
                          void *y, cudaStream_t st);
 // Returns a CONV_* status (tensor-map encoding can fail on the host).
-int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *bias, void *y,
-                 cudaStream_t st);
+int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *bias, const void *res,
+                 void *y, cudaStream_t st);
 
 // Widens int8 to bf16 / pads channels into the plan's d_xprep, d_wprep.
 cudaError_t launch_prep(const conv_plan *p, const void *x, const void *w, cudaStream_t st);
@@ -94,6 +98,9 @@ void direct_configure(conv_plan *p);
 bool dw3x3_supported(const conv_plan *p);
 int dw3x3_configure(conv_plan *p);  // CONV_* status
 bool igemm_supported(const conv_plan *p);
+// The tcgen05 kernel variant for layers with output options (a residual or
+// upsample replicas), compiled in its own translation unit.
+void *igemm_select_fused(int bn, int bk, bool flat, bool swap, bool pair);
 // Fills p->ig and sets kernel attributes; CONV_* status.  layout 0 picks
 // the tile layout by estimated time; 1..5 force swapped, N256, N128, N64,
 // CTA pair.

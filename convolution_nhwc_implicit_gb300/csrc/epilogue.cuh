@@ -91,6 +91,25 @@ __device__ __forceinline__ float activate(float v, int act) {
     return v;
 }
 
+// Where a layer's output goes and what is added to it (the conv_output_t
+// options): output pixel (n, oh, ow), channel co lands at element
+//   base(n, oh, ow) + rep(dy, dx) + co   for dy, dx in [0, up)
+// of y, a [N][up*OH][up*OW][Cy] buffer whose channels [c_off, c_off + Cout)
+// belong to the layer; res, if not null, is a dense [N][OH][OW][Cout] tensor
+// added after the activation.  The plain layer is Cy = Cout, c_off = 0,
+// up = 1: base = ((n*OH + oh)*OW + ow)*Cout.
+struct OutMap {
+    int Cy, c_off, up, OH, OW, Cout;
+    const void *res;
+    __device__ __forceinline__ long long base(int n, int oh, int ow) const {
+        return (((long long)n * OH + oh) * up * ((long long)OW * up) + (long long)ow * up) * Cy + c_off;
+    }
+    __device__ __forceinline__ long long rep(int dy, int dx) const {
+        return ((long long)dy * OW * up + dx) * Cy;
+    }
+    __device__ __forceinline__ bool plain() const { return up == 1 && c_off == 0 && Cy == Cout; }
+};
+
 // int8 requantisation: q = sat_[-128,127](rne(float(v) * M)), then ReLU as
 // max(q, 0).  Each step rounds to nearest-even in IEEE single precision, so
 // the result is bit-reproducible on any IEEE machine.

@@ -31,12 +31,14 @@ struct DirectArgs {
     int cin_g, cout_g, chunks_per_group;
     long long npix;
     int act;
+    OutMap om;  // output placement and residual
 };
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 direct_conv_float(DirectArgs a, const T *__restrict__ x, const T *__restrict__ w,
                   const float *__restrict__ bias, T *__restrict__ y) {
+    const T *res = reinterpret_cast<const T *>(a.om.res);
     long long pix = (long long)blockIdx.x * kThreads + threadIdx.x;
     if (pix >= a.npix) return;
     const int g = blockIdx.y / a.chunks_per_group;
@@ -70,12 +72,15 @@ direct_conv_float(DirectArgs a, const T *__restrict__ x, const T *__restrict__ w
             }
         }
     }
-    T *yp = y + pix * a.Cout + co0;
+    T *yp = y + a.om.base(n, oh, ow) + co0;
 #pragma unroll
     for (int i = 0; i < kCot; ++i) {
         if (i < nco) {
-            float v = acc[i] + (bias ? __ldg(bias + co0 + i) : 0.0f);
-            yp[i] = Elem<T>::from_f(activate(v, a.act));
+            float v = activate(acc[i] + (bias ? __ldg(bias + co0 + i) : 0.0f), a.act);
+            if (res) v += Elem<T>::to_f(__ldg(res + pix * a.Cout + co0 + i));  // residual after the activation
+            const T o = Elem<T>::from_f(v);
+            for (int dy = 0; dy < a.om.up; ++dy)
+                for (int dx = 0; dx < a.om.up; ++dx) yp[a.om.rep(dy, dx) + i] = o;
         }
     }
 }
@@ -132,12 +137,14 @@ direct_conv_i8(DirectArgs a, const int8_t *__restrict__ x, const int8_t *__restr
             }
         }
     }
-    int8_t *yp = y + pix * a.Cout + co0;
+    int8_t *yp = y + a.om.base(n, oh, ow) + co0;
 #pragma unroll
     for (int i = 0; i < kCot; ++i) {
         if (i < nco) {
             long long v = (long long)acc[i] + (bias ? (long long)__ldg(bias + co0 + i) : 0ll);
-            yp[i] = (int8_t)requant_i8(v, __ldg(mult + co0 + i), a.act);
+            const int8_t q = (int8_t)requant_i8(v, __ldg(mult + co0 + i), a.act);
+            for (int dy = 0; dy < a.om.up; ++dy)
+                for (int dx = 0; dx < a.om.up; ++dx) yp[a.om.rep(dy, dx) + i] = q;
         }
     }
 }
@@ -232,24 +239,38 @@ direct_conv_smem(DirectArgs a, int chunks_per_group, const T *__restrict__ x, co
             }
         }
     }
+    const T *res = reinterpret_cast<const T *>(a.om.res);
 #pragma unroll
     for (int i = 0; i < PT; ++i) {
         if (!pv[i]) continue;
-        T *yp = y + pix[i] * a.Cout + co0;
+        long long yb = pix[i] * a.Cout;
+        if (!a.om.plain()) {
+            const int ow = (int)(pix[i] % a.OW);
+            const long long t = pix[i] / a.OW;
+            yb = a.om.base((int)(t / a.OH), (int)(t % a.OH), ow);
+        }
         T out[CT];
 #pragma unroll
-        for (int j = 0; j < CT; ++j)
-            out[j] = Elem<T>::from_f(Out<T>::act(acc[i][j] + (bias && j < nco ? __ldg(bias + co0 + j) : 0.0f), a.act));
-        const bool vec = nco == CT && ((reinterpret_cast<uintptr_t>(yp) & 15) == 0) && (CT * sizeof(T)) % 16 == 0;
-        if (vec) {
-#pragma unroll
-            for (int j = 0; j < CT; j += 16 / (int)sizeof(T))
-                *reinterpret_cast<uint4 *>(yp + j) = *reinterpret_cast<const uint4 *>(out + j);
-        } else {
-#pragma unroll
-            for (int j = 0; j < CT; ++j)
-                if (j < nco) yp[j] = out[j];
+        for (int j = 0; j < CT; ++j) {
+            float v = Out<T>::act(acc[i][j] + (bias && j < nco ? __ldg(bias + co0 + j) : 0.0f), a.act);
+            if (res && j < nco) v += Elem<T>::to_f(__ldg(res + pix[i] * a.Cout + co0 + j));  // after the activation
+            out[j] = Elem<T>::from_f(v);
         }
+        for (int dy = 0; dy < a.om.up; ++dy)
+            for (int dx = 0; dx < a.om.up; ++dx) {
+                T *yp = y + yb + a.om.rep(dy, dx) + co0;
+                const bool vec =
+                    nco == CT && ((reinterpret_cast<uintptr_t>(yp) & 15) == 0) && (CT * sizeof(T)) % 16 == 0;
+                if (vec) {
+#pragma unroll
+                    for (int j = 0; j < CT; j += 16 / (int)sizeof(T))
+                        *reinterpret_cast<uint4 *>(yp + j) = *reinterpret_cast<const uint4 *>(out + j);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < CT; ++j)
+                        if (j < nco) yp[j] = out[j];
+                }
+            }
     }
 }
 
@@ -263,6 +284,11 @@ DirectArgs make_args(const conv_plan *p) {
     a.chunks_per_group = (a.cout_g + kCot - 1) / kCot;
     a.npix = (long long)a.N * a.OH * a.OW;
     a.act = (int)p->act;
+    a.om.Cout = p->s.c_out; a.om.OH = p->oh; a.om.OW = p->ow;
+    a.om.Cy = p->up ? p->y_c : p->s.c_out;  // (up == 0: a plan struct without output options)
+    a.om.c_off = p->up ? p->y_coff : 0;
+    a.om.up = p->up ? p->up : 1;
+    a.om.res = nullptr;
     return a;
 }
 
@@ -284,7 +310,7 @@ void *smem_kernel(int ct, int pt) {
 
 template <typename T>
 cudaError_t launch_smem(const conv_plan *p, DirectArgs a, const void *x, const void *w, const void *bias, void *y,
-                        cudaStream_t st) {
+                        cudaStream_t st) {  // a.om carries the residual
     const int ct = p->dct, pt = p->dpt;
     const int chunks = (a.cout_g + ct - 1) / ct;
     const int K = a.KH * a.KW * a.cin_g;
@@ -330,8 +356,9 @@ bool direct_supported(const conv_plan *p) {
 }
 
 cudaError_t launch_direct(const conv_plan *p, const void *x, const void *w, const void *bias,
-                          void *y, cudaStream_t st) {
+                          const void *res, void *y, cudaStream_t st) {
     DirectArgs a = make_args(p);
+    a.om.res = res;
     dim3 grid((unsigned)((a.npix + kThreads - 1) / kThreads), (unsigned)(p->groups * a.chunks_per_group));
     switch (p->dtype) {
     case CONV_F32:

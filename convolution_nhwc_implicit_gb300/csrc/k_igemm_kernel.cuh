@@ -1,0 +1,738 @@
+#pragma once
+// Implicit-GEMM convolution on the 5th-generation tensor cores (tcgen05),
+// bf16 operands with fp32 accumulation in TMEM, for dense k x k and 1x1
+// layers.  im2col is never materialised ("nanoinfer", "1x1 convolutions are
+// already a GEMM": the patch matrix of a 1x1 stride-1 unpadded layer is the
+// input itself; for k x k layers each tap's patch rows are fetched straight
+// from the NHWC input by TMA).
+//
+// GEMM view: M = output pixels, N = Cout, K = k_h * k_w * Cin ordered
+// (r, s, ci).  NHWC activations and OHWI weights are then both K-contiguous
+// ("nanoinfer", cuBLAS layout comparison: both operands K-contiguous is the
+// fast layout for tensor cores), so the weight tensor is, as stored, the
+// K-major B operand [Cout][K].
+//
+// Tiles.  An M tile is 128 output pixels.  For a 1x1, stride-1, unpadded
+// layer ("flat" mode) it is 128 consecutive pixels of x viewed as
+// [N*H*W, Cin].  Otherwise it is a bh x bw rectangle of output pixels of one
+// image (bh * bw <= 128; rows past bh * bw are computed from stale shared
+// memory and never stored).  For tap (r, s) and channel block cb, the A tile
+// is one 4-D TMA box of the NHWC input starting at
+// (cb * BK, ow0 * S - pad_w + s, oh0 * S - pad_h + r, n) with element strides
+// (1, S, S, 1): TMA fills out-of-image coordinates with zeros, which is the
+// zero padding, and the element strides are the convolution stride.  The B
+// tile is the [BN x BK] block of the weights at K offset (r, s, cb).
+//
+// Warp roles (320 or 576 threads, one CTA per SM, persistent over tiles):
+//   warp 0      TMA producer: fills a ring of `stages` shared-memory stages
+//   warp 1      MMA issuer: tcgen05.mma M=128 x N=BN x K=16 per instruction,
+//               accumulating a tile in one of two TMEM buffers
+//   warps 2..    epilogue: 2 or 4 warpgroups, each draining a slice of the
+//               tile's columns (tcgen05.ld, one pixel row per thread), then
+//               + bias, ReLU / Mish, round to bf16, 16-byte stores.
+// Two TMEM accumulators let the epilogue of tile i overlap the MMAs of tile
+// i + 1; an epilogue thread returns its TMEM slice as soon as the values are
+// in registers.  Every wait on an mbarrier is bounded; a wait that runs out sets the
+// plan's status word and the CTA unwinds (frees its TMEM and returns).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include <type_traits>
+
+#include "conv_internal.h"
+#include "epilogue.cuh"
+#include "tc_ptx.cuh"
+
+using namespace convk;
+
+namespace {
+
+constexpr int kBM = 128;     // output pixels per tile (normal mode)
+constexpr int kBMSwap = 256; // output pixels per tile (swapped mode)
+constexpr int kTP = 272;     // swapped-mode transpose rows: 128 bf16 channels + 16 bytes of padding
+
+// Epilogue warpgroups per CTA: each takes a slice of every tile's columns.
+__host__ __device__ constexpr int epi_groups(int bn, bool swap) { return swap ? 4 : (bn >= 128 ? 4 : 2); }
+// Threads per CTA: the TMA warp, the MMA warp and the epilogue warpgroups.
+__host__ __device__ constexpr int cta_threads(int bn, bool swap) { return 64 + 128 * epi_groups(bn, swap); }
+
+struct IgArgs {
+    int H, W, Cin, Cout, KH, KW, stride, pad_h, pad_w, OH, OW;
+    int bw, bh, tiles_w, tiles_h, tiles_n, num_tiles, cblocks, kblocks, stages;
+    int tiles_m;         // pixel tiles (pair mode: each CTA of a pair takes one of two)
+    long long M;         // flat mode: rows of x viewed as [N*H*W, Cin]
+    int flat;
+    uint32_t a_bytes;    // bytes TMA writes per A box
+    int act;
+    const void *bias;    // fp32 [Cout] (bf16 output) or int32 [Cout] (int8 output), or null
+    void *y;             // bf16 or int8 NHWC output
+    int out_i8;          // 1: int8 output, requantised with mult[co]
+    const float *mult;   // int8: requantisation multipliers M[co]
+    int out_bufs;        // normal mode: output staging buffers per epilogue group (1 or 2)
+    OutMap om;           // output placement (concat slice, 2x upsample) and residual
+    int *status;
+};
+
+// The output tensor maps of the TMA-store epilogue: one per upsample
+// replica (dy, dx) (only the first without upsampling), each a view of y's
+// channel slice at that replica's pixels.
+struct YMaps {
+    CUtensorMap m[4];
+};
+
+// Waits for phase `parity` of `bar`, giving up after kWaitBudgetNs or when
+// another role of the CTA has given up.  Returns false on give-up.
+// CLUSTER: acquire at cluster scope (arrivals may come from the peer CTA).
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                             int *status, int code) {
+    auto poll = [&]() { return CLUSTER ? tc::mbar_try_wait_cluster(bar, parity) : tc::mbar_try_wait(bar, parity); };
+    if (poll()) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (poll()) return true;
+        if ((i & 63u) == 0u) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+                *abort_flag = 1;
+                atomicExch(status, code);
+                return false;
+            }
+        }
+    }
+}
+
+// Swapped-mode write-out: y element offset (channel 0 of the layer's slice,
+// replica (0, 0)) of pixel p of the tile, and whether p is inside the image.
+__device__ __forceinline__ void swapped_pixel(const IgArgs &a, long long m0, int n, int oh0, int ow0, int p,
+                                              long long &yb, bool &valid) {
+    if (a.flat) {  // (no upsampling in flat mode)
+        const long long pix = m0 + p;
+        valid = pix < a.M;
+        yb = pix * a.om.Cy + a.om.c_off;
+    } else {
+        const int dh = p / a.bw;
+        const int oh = oh0 + dh, ow = ow0 + (p - dh * a.bw);
+        valid = p < a.bw * a.bh && oh < a.OH && ow < a.OW;
+        yb = a.om.base(n, oh, ow);
+    }
+}
+
+// Pixel index (n, oh, ow flattened) of pixel p of a swapped-mode tile, or -1
+// outside the image.
+__device__ __forceinline__ long long swapped_pix(const IgArgs &a, long long m0, int n, int oh0, int ow0, int p) {
+    if (a.flat) return m0 + p < a.M ? m0 + p : -1;
+    const int dh = p / a.bw;
+    const int oh = oh0 + dh, ow = ow0 + (p - dh * a.bw);
+    if (p >= a.bw * a.bh || oh >= a.OH || ow >= a.OW) return -1;
+    return ((long long)n * a.OH + oh) * a.OW + ow;
+}
+
+// Epilogue of the swapped mode for one tile.  The accumulator is D[co][px]:
+// thread `row` of the group holds output channel co = nb*128 + row and reads
+// the group's kCols pixel columns 16 at a time.  Each 16-pixel chunk goes
+// through shared memory (rows of 128 channels, padded to kTP bytes) to turn
+// channel-per-thread values into pixel rows, which the group then writes
+// with 16-byte stores (eight threads cover one pixel's 128 channels).
+template <int kCols, bool FUSED>
+__device__ __forceinline__ void epilogue_swapped(const IgArgs &a, int tile, uint32_t taddr, uint32_t tempty,
+                                                 int row, int grp, int c_base, uint8_t *tbuf, int gt) {
+    const int nb = tile % a.tiles_n;
+    const int mt = tile / a.tiles_n;
+    const int co = nb * 128 + row;
+    const bool cov = co < a.Cout;
+    const float fbias = (!a.out_i8 && a.bias && cov) ? __ldg(reinterpret_cast<const float *>(a.bias) + co) : 0.0f;
+    const long long ibias = (a.out_i8 && a.bias && cov) ? (long long)__ldg(reinterpret_cast<const int32_t *>(a.bias) + co) : 0ll;
+    const float mult = (a.out_i8 && cov) ? __ldg(a.mult + co) : 0.0f;
+    // Pull the whole slice out of TMEM first and hand the buffer back.
+    uint32_t acc[kCols];
+#pragma unroll
+    for (int c = 0; c < kCols; c += 16) tc::tmem_ld_32x16(taddr + (uint32_t)c, *reinterpret_cast<uint32_t(*)[16]>(acc + c));
+    tc::tmem_ld_wait();
+    tc::fence_before_sync();
+    tc::mbar_arrive(tempty);
+
+    int n = 0, oh0 = 0, ow0 = 0;
+    long long m0 = 0;
+    if (a.flat) {
+        m0 = (long long)mt * kBMSwap;
+    } else {
+        const int tw = mt % a.tiles_w;
+        const int t2 = mt / a.tiles_w;
+        oh0 = (t2 % a.tiles_h) * a.bh;
+        n = t2 / a.tiles_h;
+        ow0 = tw * a.bw;
+    }
+    // this thread's part of the write-out: pixel gt / 8 of the chunk, channels (gt % 8) * 16 .. + 15
+    const int wpx = gt >> 3;
+    const int wco = nb * 128 + (gt & 7) * 16;
+#pragma unroll
+    for (int c = 0; c < kCols; c += 16) {
+        tc::named_bar_sync(1 + grp, 128);  // the previous chunk's rows have been read
+        if (a.out_i8) {
+            // exact integer accumulator -> + bias -> requantise (rows of 128 bytes)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const long long v = (long long)__float2int_rn(__uint_as_float(acc[c + i])) + ibias;
+                tbuf[i * kTP + row] = (uint8_t)(int8_t)requant_i8(v, mult, a.act);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+                const float2 v = activate2_fast(
+                    make_float2(__uint_as_float(acc[c + i]) + fbias, __uint_as_float(acc[c + i + 1]) + fbias), a.act);
+                *reinterpret_cast<__nv_bfloat16 *>(tbuf + i * kTP + row * 2) = __float2bfloat16_rn(v.x);
+                *reinterpret_cast<__nv_bfloat16 *>(tbuf + (i + 1) * kTP + row * 2) = __float2bfloat16_rn(v.y);
+            }
+        }
+        tc::named_bar_sync(1 + grp, 128);
+        const int p = c_base + c + wpx;  // pixel index inside the tile
+        long long yb;
+        bool valid;
+        swapped_pixel(a, m0, n, oh0, ow0, p, yb, valid);
+        if (valid && wco < a.Cout) {
+            // 16 int8 channels per thread (Cout % 16 == 0 on this path), to
+            // every upsample replica of the pixel
+            const uint4 v = *reinterpret_cast<const uint4 *>(tbuf + wpx * kTP + (gt & 7) * 16);
+            int8_t *dst = reinterpret_cast<int8_t *>(a.y) + yb + wco;
+            const int up = FUSED ? a.om.up : 1;
+            for (int dy = 0; dy < up; ++dy)
+                for (int dx = 0; dx < up; ++dx)
+                    *reinterpret_cast<uint4 *>(FUSED ? dst + a.om.rep(dy, dx) : dst) = v;
+        }
+    }
+}
+
+// bf16 output of the swapped mode.  The accumulator slice of this warp
+// (lanes = 32 output channels, kCols pixel columns) is read in 16-lane x
+// 8-column pieces, so that each thread holds pixel PAIRS of one channel
+// (bias + packed Mish) and the pieces are 8x8 fragments: stmatrix.trans
+// writes each fragment transposed, i.e. 8 channels (16 bytes) of one pixel
+// per row, into the transpose rows, whose 272-byte pitch keeps the eight
+// rows of a fragment on distinct banks.  The write-out is the same as the
+// general epilogue's.
+// FUSED: the layer has a residual or writes upsample replicas (a separate
+// instantiation, so that the plain epilogue carries none of that code).
+template <int kCols, bool FUSED>
+__device__ __forceinline__ void epilogue_swapped_bf16(const IgArgs &a, int tile, uint32_t taddr, uint32_t tempty,
+                                                      int grp, int c_base, uint8_t *tbuf, int gt, int q, int lane) {
+    const int nb = tile % a.tiles_n;
+    const int mt = tile / a.tiles_n;
+    // this thread's channels (within the 128-channel block): 32q + 16h + 8j + lane/4
+    float fb[2][2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int co = nb * 128 + 32 * q + 16 * h + 8 * j + (lane >> 2);
+            fb[h][j] = (a.bias && co < a.Cout) ? __ldg(reinterpret_cast<const float *>(a.bias) + co) : 0.0f;
+        }
+    // the slice in registers, then the TMEM buffer goes back to the MMA warp
+    uint32_t acc[2][kCols / 8][4];  // [lane half][8-column group][fragment registers]
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int g = 0; g < kCols / 8; ++g)
+            tc::tmem_ld_16x256(taddr + ((uint32_t)(16 * h) << 16) + (uint32_t)(8 * g), acc[h][g]);
+    tc::tmem_ld_wait();
+    tc::fence_before_sync();
+    tc::mbar_arrive(tempty);
+
+    int n = 0, oh0 = 0, ow0 = 0;
+    long long m0 = 0;
+    if (a.flat) {
+        m0 = (long long)mt * kBMSwap;
+    } else {
+        const int tw = mt % a.tiles_w;
+        const int t2 = mt / a.tiles_w;
+        oh0 = (t2 % a.tiles_h) * a.bh;
+        n = t2 / a.tiles_h;
+        ow0 = tw * a.bw;
+    }
+    const uint32_t tb = tc::smem_u32(tbuf);
+    // stmatrix row address of this thread: matrix (lane / 8) = (8-column group
+    // g0 + (lane / 16), channels + 8 * ((lane / 8) & 1)), row lane % 8
+    const uint32_t srow = tb + (uint32_t)((8 * (lane >> 4) + (lane & 7)) * kTP) +
+                          (uint32_t)((32 * q + 8 * ((lane >> 3) & 1)) * 2);
+    const int wpx = gt >> 3;
+    const int wco = nb * 128 + (gt & 7) * 16;
+    const __nv_bfloat16 *res = FUSED ? reinterpret_cast<const __nv_bfloat16 *>(a.om.res) : nullptr;
+#pragma unroll
+    for (int c = 0; c < kCols; c += 16) {
+        // residual rows of this thread's four pixels of the chunk (pixels
+        // c_base + c + 8 gg + 2 (lane % 4) + e)
+        int rpix[2][2] = {{-1, -1}, {-1, -1}};  // (pixel counts are below 2^31)
+        if (FUSED && res) {
+#pragma unroll
+            for (int gg = 0; gg < 2; ++gg)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                    rpix[gg][e] = (int)swapped_pix(a, m0, n, oh0, ow0, c_base + c + 8 * gg + 2 * (lane & 3) + e);
+        }
+        tc::named_bar_sync(1 + grp, 128);  // the previous chunk's rows have been read
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t fr[4];
+#pragma unroll
+            for (int gg = 0; gg < 2; ++gg) {
+                const uint32_t(&r)[4] = acc[h][c / 8 + gg];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    float2 v = activate2_fast(
+                        make_float2(__uint_as_float(r[2 * j]) + fb[h][j], __uint_as_float(r[2 * j + 1]) + fb[h][j]),
+                        a.act);
+                    if (FUSED && res) {  // residual after the activation (channel 16 h + 8 j of the thread's rows)
+                        const int co = nb * 128 + 32 * q + 16 * h + 8 * j + (lane >> 2);
+                        if (co < a.Cout) {
+                            if (rpix[gg][0] >= 0) v.x += __bfloat162float(res[(long long)rpix[gg][0] * a.Cout + co]);
+                            if (rpix[gg][1] >= 0) v.y += __bfloat162float(res[(long long)rpix[gg][1] * a.Cout + co]);
+                        }
+                    }
+                    __nv_bfloat162 b2 = __floats2bfloat162_rn(v.x, v.y);
+                    fr[2 * gg + j] = *reinterpret_cast<uint32_t *>(&b2);
+                }
+            }
+            tc::stmatrix_x4_trans(srow + (uint32_t)(16 * h * 2), fr[0], fr[1], fr[2], fr[3]);
+        }
+        tc::named_bar_sync(1 + grp, 128);
+        const int p = c_base + c + wpx;  // pixel index inside the tile
+        long long yb;
+        bool valid;
+        swapped_pixel(a, m0, n, oh0, ow0, p, yb, valid);
+        if (valid) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(tbuf + wpx * kTP + (gt & 7) * 32);
+            const uint4 v0 = src[0], v1 = src[1];
+            __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(a.y) + yb + wco;
+            const int up = FUSED ? a.om.up : 1;
+            for (int dy = 0; dy < up; ++dy)
+                for (int dx = 0; dx < up; ++dx) {
+                    __nv_bfloat16 *d = FUSED ? dst + a.om.rep(dy, dx) : dst;
+                    if (wco < a.Cout) *reinterpret_cast<uint4 *>(d) = v0;
+                    if (wco + 8 < a.Cout) *reinterpret_cast<uint4 *>(d + 8) = v1;
+                }
+        }
+    }
+}
+
+// SWAP = false: MMA M = 128 pixels, N = BN output channels (D[pixel][co]).
+// SWAP = true (layers with Cout <= 128): the operands trade places, MMA M =
+// 128 output channels (weights as A), N = 256 pixels (activations as B),
+// D[co][pixel]; every MMA then has N = 256, the only width at which tcgen05
+// reaches its peak rate (the issue cost of an MMA does not shrink with N).
+//
+// PAIR (normal layout only): a cluster of two CTAs on two SMs computes a
+// 256-pixel x BN tile with tcgen05's CTA-pair MMA (M = 256).  Each CTA stages
+// its own 128 pixel rows and HALF of the BN weight rows; the even CTA issues
+// the MMAs, which read both CTAs' shared memory and write each CTA's 128
+// accumulator rows into its own TMEM.  Per SM this stages (128 + BN/2) rows
+// per K block instead of 128 + BN: a third less shared-memory traffic for
+// BN = 256, which is what limits the single-CTA layout on large layers.
+// Both CTAs' loads complete on the even CTA's full barrier; the even CTA's
+// commits arrive on both CTAs' empty / accumulator-full barriers; both CTAs'
+// epilogue warps arrive on the even CTA's accumulator-empty barrier.
+// FUSED: the layer has a residual or upsample replicas (conv_output_t); a
+// separate instantiation, so that plain layers run none of that code.
+template <int BN, int BK, bool FLAT, bool SWAP, bool PAIR, bool FUSED>
+__global__ void __launch_bounds__(cta_threads(BN, SWAP), 1)
+igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const __grid_constant__ YMaps tmY, const IgArgs a) {
+    static_assert(!(PAIR && SWAP), "the CTA-pair mode uses the normal layout");
+    constexpr int kPix = SWAP ? kBMSwap : kBM;  // pixel rows of a tile (per CTA)
+    constexpr int kAcc = SWAP ? kBMSwap : BN;   // accumulator columns of a tile
+    constexpr int kBRows = PAIR ? BN / 2 : BN;  // weight rows this CTA stages
+    constexpr uint32_t kRowBytes = BK * 2;
+    constexpr uint32_t kAStage = kPix * BK * 2;  // activation (pixel) tile
+    constexpr uint32_t kBStage = kBRows * BK * 2;  // weight tile (this CTA's part)
+    constexpr uint32_t kTmemCols = 2 * kAcc;     // two accumulators
+    constexpr uint32_t kIdesc = SWAP ? tc::idesc_bf16_f32(128, kBMSwap)
+                                     : tc::idesc_bf16_f32(PAIR ? 2 * kBM : kBM, BN);
+    constexpr int kGroups = epi_groups(BN, SWAP);
+    constexpr int kCols = kAcc / kGroups;  // accumulator columns per epilogue thread
+    static_assert(SWAP ? (BN == 128 && kCols % 16 == 0) : (kCols % 32 == 0), "epilogue column slices");
+    constexpr uint32_t kOutStage = SWAP ? 16 * kTP : kBM * 64;  // per group: transpose rows / store staging
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = tc::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms need 1024-byte alignment
+    uint8_t *gbase = smem_raw + (base - raw);
+    const int stages = a.stages;
+    const uint32_t sA = base;
+    const uint32_t sB = base + stages * kAStage;
+    const uint32_t sOut = sB + stages * kBStage;  // per epilogue group: 128 rows x 64 B output staging
+    const uint32_t sBar = sOut + kGroups * a.out_bufs * kOutStage;
+    auto full_bar = [&](int s) { return sBar + 8u * s; };
+    auto empty_bar = [&](int s) { return sBar + 8u * (stages + s); };
+    auto tfull_bar = [&](int b) { return sBar + 8u * (2 * stages + b); };
+    auto tempty_bar = [&](int b) { return sBar + 8u * (2 * stages + 2 + b); };
+    uint8_t *gmisc = gbase + (sBar - base) + 8u * (2 * stages + 4);
+    volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(gmisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gmisc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    // Work unit: the CTA, or in pair mode the cluster (CTAs 2u and 2u + 1).
+    const uint32_t rank = PAIR ? tc::cluster_ctarank() : 0u;
+    const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            tc::mbar_init(full_bar(s), 1);
+            tc::mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(tfull_bar(b), 1);
+            tc::mbar_init(tempty_bar(b), PAIR ? 2 * 4 * kGroups : 128 * kGroups);  // pair: one per warp
+        }
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+        tc::tma_prefetch_desc(&tmA);
+        tc::tma_prefetch_desc(&tmB);
+        tc::tma_prefetch_desc(&tmY.m[0]);
+    }
+    if (warp == 1) {
+        if constexpr (PAIR) {
+            tc::tmem_alloc_pair(tc::smem_u32((const void *)tmem_holder), kTmemCols);
+            tc::tmem_relinquish_pair();
+        } else {
+            tc::tmem_alloc(tc::smem_u32((const void *)tmem_holder), kTmemCols);
+            tc::tmem_relinquish();
+        }
+    }
+    // __syncthreads is an aligned barrier: every warp must reach it converged.
+    __syncwarp();
+    tc::fence_before_sync();
+    __syncthreads();
+    if constexpr (PAIR) tc::cluster_sync();  // the peer's barriers are initialised
+    tc::fence_after_sync();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            // pair mode: both CTAs' loads complete on the even CTA's barriers
+            const uint32_t full0 = PAIR ? tc::mapa_shared(full_bar(0), 0) : full_bar(0);
+            for (int tile = unit; tile < a.num_tiles && ok; tile += units) {
+                const int nb = tile % a.tiles_n;
+                // pair mode: this CTA's pixel tile (past tiles_m: an empty
+                // half, loaded as zeros from outside the tensor, never stored)
+                const int mt = PAIR ? (tile / a.tiles_n) * 2 + (int)rank : tile / a.tiles_n;
+                int n = 0, oh0 = 0, ow0 = 0;
+                int m0 = 0;
+                if (FLAT) {
+                    m0 = mt * kPix;
+                } else {
+                    const int tw = mt % a.tiles_w;
+                    const int t2 = mt / a.tiles_w;
+                    oh0 = (t2 % a.tiles_h) * a.bh;
+                    n = t2 / a.tiles_h;
+                    ow0 = tw * a.bw;
+                }
+                int r = 0, s = 0, cb = 0;
+                for (int kb = 0; kb < a.kblocks; ++kb) {
+                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, a.status,
+                                      KSTATUS_TIMEOUT_PRODUCER)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dA = sA + stage * kAStage;
+                    const uint32_t dB = sB + stage * kBStage;
+                    const int kx = (r * a.KW + s) * a.Cin + cb * BK;
+                    if constexpr (PAIR) {
+                        const uint32_t fb = full0 + 8u * stage;
+                        if (rank == 0) tc::mbar_arrive_expect_tx(full_bar(stage), 2u * (a.a_bytes + kBStage));
+                        if (FLAT)
+                            tc::tma_load_2d_pair(dA, &tmA, fb, cb * BK, m0);
+                        else
+                            tc::tma_load_4d_pair(dA, &tmA, fb, cb * BK, ow0 * a.stride - a.pad_w + s,
+                                                 oh0 * a.stride - a.pad_h + r, n);
+                        tc::tma_load_2d_pair(dB, &tmB, fb, kx, nb * BN + (int)rank * kBRows);
+                    } else {
+                        tc::mbar_arrive_expect_tx(full_bar(stage), a.a_bytes + kBStage);
+                        if (FLAT)
+                            tc::tma_load_2d(dA, &tmA, full_bar(stage), cb * BK, m0);
+                        else
+                            tc::tma_load_4d(dA, &tmA, full_bar(stage), cb * BK,
+                                            ow0 * a.stride - a.pad_w + s, oh0 * a.stride - a.pad_h + r, n);
+                        tc::tma_load_2d(dB, &tmB, full_bar(stage), kx, nb * BN);
+                    }
+                    if (++stage == stages) { stage = 0; phase ^= 1u; }
+                    if (++cb == a.cblocks) {
+                        cb = 0;
+                        if (++s == a.KW) { s = 0; ++r; }
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (pair mode: even CTA only)
+        if (lane == 0 && rank == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int lt = 0;
+            for (int tile = unit; tile < a.num_tiles && ok; tile += units, ++lt) {
+                const int buf = lt & 1;
+                const uint32_t use = (uint32_t)(lt >> 1);
+                if (!wait_bounded<PAIR>(tempty_bar(buf), (use & 1u) ^ 1u, abort_flag, a.status,
+                                        KSTATUS_TIMEOUT_MMA))
+                    break;
+                tc::fence_after_sync();
+                const uint32_t d = tmem_base + (uint32_t)(buf * kAcc);
+                for (int kb = 0; kb < a.kblocks; ++kb) {
+                    if (!wait_bounded(full_bar(stage), phase, abort_flag, a.status, KSTATUS_TIMEOUT_MMA)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const uint32_t aS = sA + stage * kAStage;
+                    const uint32_t bS = sB + stage * kBStage;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        const uint64_t pd = tc::smem_desc_kmajor(aS + 32u * k, kRowBytes);  // pixels
+                        const uint64_t wd = tc::smem_desc_kmajor(bS + 32u * k, kRowBytes);  // weights
+                        if (PAIR)
+                            tc::mma_bf16_pair(d, pd, wd, kIdesc, (kb | k) != 0 ? 1u : 0u);
+                        else if (SWAP)
+                            tc::mma_bf16(d, wd, pd, kIdesc, (kb | k) != 0 ? 1u : 0u);
+                        else
+                            tc::mma_bf16(d, pd, wd, kIdesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    // stage free (in both CTAs of a pair) once these MMAs complete
+                    if (PAIR)
+                        tc::mma_commit_pair(empty_bar(stage), 0x3);
+                    else
+                        tc::mma_commit(empty_bar(stage));
+                    if (++stage == stages) { stage = 0; phase ^= 1u; }
+                }
+                if (ok) {  // accumulator ready
+                    if (PAIR)
+                        tc::mma_commit_pair(tfull_bar(buf), 0x3);
+                    else
+                        tc::mma_commit(tfull_bar(buf));
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 2 ..)
+        // tcgen05.ld lets warp w reach TMEM lanes 32 * (w % 4) .. + 31, so every
+        // run of four consecutive warps covers the 128 accumulator rows; warp
+        // group g (warps 2 + 4g .. 5 + 4g) drains columns [g * kCols, (g+1) * kCols).
+        const int q = warp & 3;
+        const int grp = (warp - 2) >> 2;
+        const int row = q * 32 + lane;
+        const int c_base = grp * kCols;
+        const bool issuer = ((warp - 2) & 3) == 0 && lane == 0;  // issues the group's TMA stores
+        const uint32_t sStage = sOut + (uint32_t)(grp * a.out_bufs) * kOutStage;  // this group's staging
+        int oc = 0;  // TMA stores this group has issued (selects the staging buffer)
+        int lt = 0;
+        // pair mode: accumulator-empty arrivals go to the even CTA's barrier
+        const uint32_t tempty0 = PAIR ? tc::mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
+        for (int tile = unit; tile < a.num_tiles; tile += units, ++lt) {
+            const int buf = lt & 1;
+            const uint32_t use = (uint32_t)(lt >> 1);
+            const bool got = wait_bounded(tfull_bar(buf), use & 1u, abort_flag, a.status,
+                                          KSTATUS_TIMEOUT_EPILOGUE);
+            __syncwarp();  // tcgen05.ld below is warp-collective (.sync.aligned)
+            if (!__all_sync(0xffffffffu, got)) break;
+            tc::fence_after_sync();
+            if constexpr (SWAP) {
+                const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kAcc + c_base);
+                uint8_t *tb = gbase + (sOut - base) + grp * a.out_bufs * kOutStage;
+                if (a.out_i8)
+                    epilogue_swapped<kCols, FUSED>(a, tile, ta, tempty_bar(buf), row, grp, c_base, tb,
+                                                   threadIdx.x - 64 - grp * 128);
+                else
+                    epilogue_swapped_bf16<kCols, FUSED>(a, tile, ta, tempty_bar(buf), grp, c_base, tb,
+                                                        threadIdx.x - 64 - grp * 128, q, lane);
+                continue;
+            }
+            // Plain layers pull this thread's whole accumulator slice out of
+            // TMEM and hand the buffer back to the MMA warp at once; FUSED
+            // layers (registers for the residual) read it 32 columns at a time
+            // and hand it back after the last chunk.
+            constexpr int kAccRegs = FUSED ? 32 : kCols;
+            uint32_t acc[kAccRegs];
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c_base);
+            auto release = [&]() {
+                tc::fence_before_sync();
+                if constexpr (PAIR) {
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive_cluster(tempty0 + 8u * buf);
+                } else {
+                    tc::mbar_arrive(tempty_bar(buf));
+                }
+            };
+            if constexpr (!FUSED) {
+#pragma unroll
+                for (int c = 0; c < kCols; c += 32)
+                    tc::tmem_ld_32x32(tbase + (uint32_t)c, *reinterpret_cast<uint32_t(*)[32]>(acc + c));
+                tc::tmem_ld_wait();
+                release();
+            }
+
+            // Output slice: bias, activation, bf16, staged in shared memory
+            // (64-byte swizzle, matching the store's tensor map) and written by
+            // one TMA tensor store per 32 columns.  The box is the tile's
+            // bh x bw pixel rectangle (or 128 flat rows): rows past it are
+            // never stored and pixels outside the image are clipped by TMA.
+            const int nb = tile % a.tiles_n;
+            const int mt = PAIR ? (tile / a.tiles_n) * 2 + (int)rank : tile / a.tiles_n;
+            if (PAIR && mt >= a.tiles_m) {  // the empty half of the last pair tile
+                if constexpr (FUSED) release();
+                continue;
+            }
+            int n = 0, oh0 = 0, ow0 = 0, m0 = 0;
+            if (FLAT) {
+                m0 = mt * kPix;
+            } else {
+                const int tw = mt % a.tiles_w;
+                const int t2 = mt / a.tiles_w;
+                oh0 = (t2 % a.tiles_h) * a.bh;
+                n = t2 / a.tiles_h;
+                ow0 = tw * a.bw;
+            }
+            const uint32_t swz = (uint32_t)((row >> 1) & 3);
+            // residual pixel of this thread's row (-1: none, or outside the image;
+            // pixel counts are below 2^31)
+            int rpix = -1;
+            if (FUSED && a.om.res) {
+                if (FLAT) {
+                    if ((long long)m0 + row < a.M) rpix = m0 + row;
+                } else if (row < a.bw * a.bh) {
+                    const int dh = row / a.bw;
+                    const int oh = oh0 + dh, ow = ow0 + (row - dh * a.bw);
+                    if (oh < a.OH && ow < a.OW) rpix = (n * a.OH + oh) * a.OW + ow;
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < kCols; c += 32) {
+                const int co = nb * BN + c_base + c;
+                const bool live = co < a.Cout;  // the same for the whole group
+                if constexpr (FUSED) {
+                    if (live) {
+                        tc::tmem_ld_32x32(tbase + (uint32_t)c, *reinterpret_cast<uint32_t(*)[32]>(acc));
+                        tc::tmem_ld_wait();
+                    }
+                    if (c + 32 == kCols) release();
+                }
+                if (!live) continue;
+                const uint32_t *av = acc + (FUSED ? 0 : c);  // this chunk's 32 accumulator columns
+                const uint32_t sbuf = sStage + (uint32_t)(oc & (a.out_bufs - 1)) * kOutStage;
+                const uint32_t srow = sbuf + (uint32_t)row * 64u;
+                // the store that last used this staging buffer has read it
+                // (with two buffers that is every store but the latest)
+                if (issuer) {
+                    if (a.out_bufs == 2)
+                        tc::bulk_wait_read1();
+                    else
+                        tc::bulk_wait_read0();
+                }
+                tc::named_bar_sync(1 + grp, 128);
+                if (a.out_i8) {
+                    // int8 output: the accumulator is an exact integer (< 2^24);
+                    // + int32 bias, requantise, saturate.  Rows of 32 bytes,
+                    // stored unswizzled (the int8 store map has no swizzle).
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int cc = co + e;
+                        long long v = (long long)__float2int_rn(__uint_as_float(av[e]));
+                        if (a.bias) v += (long long)__ldg(reinterpret_cast<const int32_t *>(a.bias) + cc);
+                        const int q = requant_i8(v, __ldg(a.mult + cc), a.act);
+                        if ((e & 3) == 0) pk[e >> 2] = 0u;
+                        pk[e >> 2] |= ((uint32_t)(q & 0xff)) << (8 * (e & 3));
+                    }
+                    const uint32_t dst8 = sbuf + (uint32_t)row * 32u;
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst8), "r"(pk[0]), "r"(pk[1]),
+                                 "r"(pk[2]), "r"(pk[3])
+                                 : "memory");
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst8 + 16u), "r"(pk[4]),
+                                 "r"(pk[5]), "r"(pk[6]), "r"(pk[7])
+                                 : "memory");
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(av[8 * j + e]);
+                        if (a.bias && co + 8 * j < a.Cout) {  // Cout % 8 == 0: 8 columns all in or all out
+                            const float *fb = reinterpret_cast<const float *>(a.bias) + co + 8 * j;
+                            const float4 b0 = __ldg(reinterpret_cast<const float4 *>(fb));
+                            const float4 b1 = __ldg(reinterpret_cast<const float4 *>(fb) + 1);
+                            v[0] += b0.x; v[1] += b0.y; v[2] += b0.z; v[3] += b0.w;
+                            v[4] += b1.x; v[5] += b1.y; v[6] += b1.z; v[7] += b1.w;
+                        }
+                        // residual (8 channels, 16 bytes) added after the activation
+                        float rv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                        if (FUSED && rpix >= 0 && co + 8 * j < a.Cout) {
+                            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(
+                                reinterpret_cast<const __nv_bfloat16 *>(a.om.res) + (long long)rpix * a.Cout + co + 8 * j));
+                            const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                rv[2 * e] = __uint_as_float(wd[e] << 16);
+                                rv[2 * e + 1] = __uint_as_float(wd[e] & 0xffff0000u);
+                            }
+                        }
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float2 f = activate2_fast(make_float2(v[2 * e], v[2 * e + 1]), a.act);
+                            if constexpr (FUSED) f = add2(f, make_float2(rv[2 * e], rv[2 * e + 1]));
+                            __nv_bfloat162 h2 = __floats2bfloat162_rn(f.x, f.y);
+                            pk[e] = *reinterpret_cast<uint32_t *>(&h2);
+                        }
+                        const uint32_t dst = srow + ((((uint32_t)j) ^ swz) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pk[0]),
+                                     "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
+                                     : "memory");
+                    }
+                }
+                tc::fence_proxy_async_smem();  // staged values visible to the TMA engine
+                tc::named_bar_sync(1 + grp, 128);
+                if (issuer) {
+                    const int reps = FUSED ? a.om.up * a.om.up : 1;
+                    for (int rp = 0; rp < reps; ++rp) {  // one store per upsample replica
+                        if (FLAT)
+                            tc::tma_store_2d(&tmY.m[rp], sbuf, co, m0);
+                        else
+                            tc::tma_store_4d(&tmY.m[rp], sbuf, co, ow0, oh0, n);
+                    }
+                    tc::bulk_commit();
+                }
+                ++oc;
+            }
+        }
+        // The staging buffers must outlive the stores' reads of them; the
+        // global writes themselves complete before the grid does.
+        if (issuer) tc::bulk_wait_read0();
+    }
+
+    // Warps 0 and 1 ran their loops on lane 0 only: reconverge each warp
+    // before the block barrier, so that the barrier really waits for every
+    // role (TMEM is freed only after the epilogue's last tcgen05.ld).
+    __syncwarp();
+    tc::fence_before_sync();
+    __syncthreads();
+    // pair mode: neither CTA leaves (or frees TMEM) while the other may still
+    // use its shared memory or TMEM
+    if constexpr (PAIR) tc::cluster_sync();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        if constexpr (PAIR)
+            tc::tmem_dealloc_pair(tmem_base, kTmemCols);
+        else
+            tc::tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+}  // namespace

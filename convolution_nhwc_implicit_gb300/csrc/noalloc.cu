@@ -79,6 +79,7 @@ extern "C" int conv_run_i8_noalloc(const conv_shape_t *shape, int stride, int pa
     p.s = *shape;
     p.stride = stride; p.pad_h = pad_h; p.pad_w = pad_w; p.groups = groups;
     p.dtype = CONV_I8; p.act = act; p.oh = oh; p.ow = ow;
+    p.y_c = shape->c_out; p.y_coff = 0; p.up = 1; p.has_res = 0;  // the plain layer output
     p.algo = CONV_ALGO_DIRECT;
     if (!direct_supported(&p)) return CONV_ERR_UNSUPPORTED;
     if (shape->n == 0) return CONV_OK;
@@ -107,5 +108,5 @@ extern "C" int conv_run_i8_noalloc(const conv_shape_t *shape, int stride, int pa
         fill_multipliers<<<(n + 255) / 256, 256, 0, st>>>(chunk, off, n);
         if (cudaGetLastError() != cudaSuccess) return CONV_ERR_CUDA;
     }
-    return launch_direct(&p, x, w, bias, y, st) == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+    return launch_direct(&p, x, w, bias, nullptr, y, st) == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }

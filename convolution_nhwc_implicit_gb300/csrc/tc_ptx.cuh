@@ -245,6 +245,24 @@ __device__ __forceinline__ void tmem_ld_32x16(uint32_t taddr, uint32_t (&r)[16])
           "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
+// 16 TMEM lanes x 8 consecutive 32-bit columns: thread t gets r[0], r[1] =
+// lane (base + t/4), columns 2(t%4) and 2(t%4)+1, and r[2], r[3] = lane
+// (base + 8 + t/4), the same columns (the layout of an m16n8 accumulator
+// fragment).
+__device__ __forceinline__ void tmem_ld_16x256(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+}
+// Four 8x8 b16 matrices stored transposed: register i of thread t holds
+// elements (t/4, 2(t%4)) and (t/4, 2(t%4)+1) of matrix i; thread t gives the
+// shared-memory address of row t%8 of matrix t/8, which receives column t%8
+// of the matrix (16 bytes).
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r0),
+                 "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor (sm_100 family) of a K-major operand tile

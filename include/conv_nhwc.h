@@ -59,7 +59,7 @@
 extern "C" {
 #endif
 
-#define CONV_NHWC_ABI_VERSION 1
+#define CONV_NHWC_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define CONV_API __attribute__((visibility("default")))
@@ -137,12 +137,64 @@ CONV_API int conv_plan_create_ex(const conv_shape_t *shape, int stride, int pad_
                         const conv_quant_t *quant, conv_algo_t algo,
                         conv_plan_t **out_plan);
 
+/* ---------------------------------------------------------------------------
+ * Output placement and residual fusion.
+ *
+ * Two fused-epilogue options from the "YOLOv4, optimized for Wormhole" page,
+ * section 9 (custom Tensix kernels):
+ *   - K2, Mish + residual add: the layer adds a skip tensor after its
+ *     activation and writes the result once:
+ *       y = act(acc + b[co]) + r[n,oh,ow,co]      (then rounded to y's type)
+ *   - K4, upsample + concat: the layer writes straight into a channel slice
+ *     of the next layer's concatenated NHWC buffer, optionally repeating
+ *     every output pixel over the 2x2 block a 2x nearest-neighbour upsample
+ *     would give it:
+ *       y[n, u*oh+dy, u*ow+dx, y_channel_offset + co] = value(n, oh, ow, co)
+ *       for dy, dx in [0, u),  u = upsample.
+ * y is then a [N][u*OH][u*OW][y_channels] buffer, of which the layer writes
+ * channels [y_channel_offset, y_channel_offset + c_out) and nothing else.
+ *
+ *   y_channels       channels per pixel of y; 0 means c_out
+ *   y_channel_offset first channel of the layer's slice (>= 0,
+ *                    y_channel_offset + c_out <= y_channels)
+ *   upsample         1 or 2
+ *   residual         0, or 1: conv_run_fused takes r, a dense
+ *                    [N][OH][OW][c_out] tensor of the layer's dtype
+ *                    (CONV_F32 or CONV_BF16; int8 layers return
+ *                    CONV_ERR_UNSUPPORTED)
+ * y_channels * esize and y_channel_offset * esize must be multiples of 16
+ * bytes (CONV_ERR_MISALIGNED).  Other values: CONV_ERR_INVALID_ARG.
+ * Depthwise layers with any of these options run on the direct kernel. */
+typedef struct {
+    int32_t y_channels;
+    int32_t y_channel_offset;
+    int32_t upsample;
+    int32_t residual;
+} conv_output_t;
+
+/* As conv_plan_create_ex with output options (`out` NULL: the plain layer,
+ * identical to conv_plan_create_ex). */
+CONV_API int conv_plan_create_fused(const conv_shape_t *shape, int stride, int pad_h, int pad_w,
+                                    int groups, conv_dtype_t dtype, conv_act_t act,
+                                    const conv_quant_t *quant, const conv_output_t *out,
+                                    conv_algo_t algo, conv_plan_t **out_plan);
+
+/* As conv_run, with the residual r (a device pointer, 16-byte aligned, not
+ * overlapping y; required if and only if the plan was created with
+ * residual = 1, else CONV_ERR_NULL_ARG / CONV_ERR_INVALID_ARG).  y is the
+ * [N][u*OH][u*OW][y_channels] buffer of the plan's output options and must
+ * not overlap x, w, bias or r. */
+CONV_API int conv_run_fused(const conv_plan_t *plan, const void *x, const void *w, const void *bias,
+                            const void *residual, void *y, void *stream);
+
 /* Enqueues the layer on `stream` (a cudaStream_t; NULL = legacy default
  * stream).  x, w, y are device pointers, bias a device pointer or NULL; all
  * 16-byte aligned.  y must not overlap x, w or bias.  Asynchronous: errors
  * of the kernel itself surface through conv_plan_check_device_status. */
 CONV_API int conv_run(const conv_plan_t *plan, const void *x, const void *w, const void *bias,
              void *y, void *stream);
+/* (conv_run on a plan with output options is conv_run_fused without a
+ * residual.) */
 
 /* Frees the plan and its device buffers.  NULL-safe.  The caller must make
  * sure no conv_run of this plan is still executing on the GPU. */

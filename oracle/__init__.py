@@ -212,3 +212,32 @@ def conv_i8_points(x, w, b, M, points, stride=1, pad_h=0, pad_w=0, groups=1,
     if rc:
         raise ValueError("oracle_conv_i8_points rejected the arguments")
     return vals
+
+
+def conv_residual_f64(x, w, b, r, stride=1, pad_h=0, pad_w=0, groups=1, act="none", threads=0):
+    """Convolution, activation, then a residual (skip) tensor added once:
+    y = act(conv(x, w) + b) + r, in double ("YOLOv4, optimized for Wormhole",
+    section 9, K2 "Mish + residual add": Mish first, then the add, one
+    write).  r is NHWC with the layer's output shape."""
+    y = conv_f64(x, w, b, stride, pad_h, pad_w, groups, act, threads)
+    r = np.asarray(r, dtype=np.float64)
+    if r.shape != y.shape:
+        raise ValueError(f"residual shape {r.shape} differs from the output shape {y.shape}")
+    return y + r
+
+
+def place_output(y, y_channels, y_channel_offset=0, upsample=1, fill=np.nan):
+    """Where a layer's output lands in the next layer's buffer ("YOLOv4,
+    optimized for Wormhole", section 9, K4 "upsample + concat": rows repeated
+    for a 2x nearest-neighbour upsample, written into the concatenated
+    layout): out[n, u*oh+dy, u*ow+dx, off+co] = y[n, oh, ow, co] for dy, dx
+    in [0, u); every other element of out is ``fill``."""
+    y = np.asarray(y)
+    N, OH, OW, C = y.shape
+    if y_channel_offset < 0 or y_channel_offset + C > y_channels or upsample < 1:
+        raise ValueError("slice outside the output buffer")
+    out = np.full((N, OH * upsample, OW * upsample, y_channels), fill,
+                  dtype=np.result_type(y.dtype, np.asarray(fill).dtype))
+    rep = np.repeat(np.repeat(y, upsample, axis=1), upsample, axis=2)
+    out[..., y_channel_offset:y_channel_offset + C] = rep
+    return out

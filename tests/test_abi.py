@@ -55,7 +55,7 @@ def test_status_strings(lib):
     for c, name in codes.items():
         assert cl.status_str(c) == "CONV_ERR_" + name
     assert cl.status_str(-1234) == "CONV_ERR_UNKNOWN"
-    assert cl.abi_version() == 1
+    assert cl.abi_version() == 2
 
 
 def _create(lib, shape, stride=1, ph=0, pw=0, groups=1, dtype=1, act=0, quant=None, algo=0):
@@ -137,3 +137,30 @@ def test_package_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(cl, "_lib", None)
     with pytest.raises(ImportError):
         cl.load_library()
+
+
+@pytest.mark.parametrize("dtype,out,expect", [
+    (1, (0, 0, 3, 0), -9),        # upsample must be 1 or 2
+    (1, (0, 0, 1, 2), -9),        # residual is 0 or 1
+    (1, (32, 24, 1, 0), -9),      # slice past y's channels (24 + 16 > 32)
+    (1, (32, -8, 1, 0), -9),      # negative offset
+    (1, (32, 4, 1, 0), -4),       # bf16 offset of 8 bytes: not a 16-byte multiple
+    (1, (36, 0, 1, 0), -4),       # bf16 pixel pitch of 72 bytes
+    (0, (32, 4, 1, 0), None),     # fp32 offset 4 = 16 bytes: valid, the call goes on to CUDA
+    (2, (0, 0, 1, 1), -3),        # int8 with a residual is not offered
+])
+def test_output_options_are_validated_before_cuda(lib, dtype, out, expect):
+    import convolution_nhwc_implicit_gb300 as cl
+    s = cl._Shape(1, 8, 8, 16, 16, 3, 3)
+    quant = _quant([0.01] * 16) if dtype == 2 else None
+    o = cl._Output(*out)
+    h = ctypes.c_void_p(12345)
+    rc = lib.conv_plan_create_fused(ctypes.byref(s), 1, 1, 1, 1, dtype, 0, quant, ctypes.byref(o), 0,
+                                    ctypes.byref(h))
+    if expect is None:  # valid options: the CUDA step fails without a GPU (or succeeds with one)
+        assert rc in (0, -6, -3)
+        if rc == 0:
+            lib.conv_plan_destroy(h)
+    else:
+        assert rc == expect
+        assert h.value is None

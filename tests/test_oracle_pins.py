@@ -342,3 +342,41 @@ def test_oracle_rejects_bad_shapes():
         oracle.conv_f64(x, np.zeros((4, 5, 5, 4)), None)           # no output fits
     with pytest.raises(ValueError):
         oracle.requant_multipliers(0.05, 0.0, [1.0])
+
+
+# ---------------------------------------------------------------- K2 / K4 options
+
+def test_residual_is_added_after_the_activation():
+    # 1..9 with an all-ones 3x3 kernel, pad 1 (the hand-worked golden case):
+    # [[12,21,16],[27,45,33],[24,39,28]]; bias -20, ReLU, residual -1.
+    x = np.arange(1, 10, dtype=np.float64).reshape(1, 3, 3, 1)
+    w = np.ones((1, 3, 3, 1))
+    b = np.array([-20.0])
+    r = np.full((1, 3, 3, 1), -1.0)
+    y = oracle.conv_residual_f64(x, w, b, r, 1, 1, 1, 1, "relu")
+    want = np.array([[-1, 0, -1], [6, 24, 12], [3, 18, 7]], dtype=np.float64)
+    assert np.array_equal(y[0, :, :, 0], want)
+    # ... which is not relu(conv + b + r): the order of the two steps shows
+    assert not np.array_equal(y, oracle.conv_f64(x, w, b - 1.0, 1, 1, 1, 1, "relu"))
+
+
+def test_residual_with_mish_matches_the_definition():
+    rng = np.random.default_rng(7)
+    x = rng.uniform(-1, 1, (1, 5, 4, 3))
+    w = rng.normal(0, 0.5, (4, 3, 3, 3))
+    r = rng.normal(0, 1, (1, 5, 4, 4))
+    y = oracle.conv_residual_f64(x, w, None, r, 1, 1, 1, 1, "mish")
+    v = oracle.conv_f64(x, w, None, 1, 1, 1, 1, "none")
+    ref = v * np.tanh(np.log1p(np.exp(v))) + r
+    assert np.allclose(y, ref, rtol=0, atol=1e-13)
+
+
+def test_place_output_concat_and_upsample():
+    y = np.array([[[[1.0], [2.0]]]])  # 1 x 1 x 2 x 1
+    out = oracle.place_output(y, y_channels=3, y_channel_offset=1, upsample=2, fill=-9.0)
+    assert out.shape == (1, 2, 4, 3)
+    assert np.array_equal(out[0, :, :, 1], [[1, 1, 2, 2], [1, 1, 2, 2]])
+    assert np.all(out[..., 0] == -9.0) and np.all(out[..., 2] == -9.0)
+    # no upsampling, no offset: the output itself
+    z = np.arange(24.0).reshape(1, 2, 3, 4)
+    assert np.array_equal(oracle.place_output(z, 4), z)
