@@ -261,9 +261,92 @@ def run_ours(args, rank, world, device):
                    "launch": "CUDA graph replay of the step (events inside the graph)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roofline, "layers": layer_rows, "e2e": e2e,
-        "gpu_launches": nl * args.steps, "clocks": clk, "wall_s_timed_region": round(wall, 4),
+        "next_rows": measure_next_rows(dev, peaks) if rank == 0 and not args.no_next_rows else None,
+        "gpu_launches": sum(p.launches for p in plans) * args.steps, "clocks": clk,
+        "wall_s_timed_region": round(wall, 4),
     }
     return out
+
+
+def measure_next_rows(dev, peaks, reps=30):
+    """The adjacent rows built beyond the five layer sets (the residual-add
+    epilogue, concat + 2x upsample output placement, the SPP block), each
+    timed like a layer of the main step: one call captured as a CUDA graph
+    between two events, replayed `reps` times with the L2 flushed before
+    every replay; the mean event time is reported with its roofline."""
+    import torch
+    import convolution_nhwc_implicit_gb300 as cl
+    from conv_workloads import LayerSpec, alg_bytes, make_layer
+
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20)
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True, external=True)
+        e1 = torch.cuda.Event(enable_timing=True, external=True)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            st = torch.cuda.current_stream(dev)
+            e0.record(st)
+            fn()
+            e1.record(st)
+        ts = []
+        for _ in range(reps):
+            flush.fill_(1)
+            g.replay()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        return float(np.mean(ts))
+
+    def roof(flops, nbytes, us):
+        ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+        if flops / nbytes >= ridge:
+            a = flops / (us * 1e-6) / 1e12
+            return {"bound": "tensor", "achieved": round(a, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": round(a / peaks["bf16_tflops"], 4)}
+        a = nbytes / (us * 1e-6) / 1e9
+        return {"bound": "hbm", "achieved": round(a, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(a / peaks["hbm_gbs"], 4)}
+
+    rows = []
+    g = torch.Generator("cpu").manual_seed(5)
+    # 1. residual add: the batch-8 256->256 3x3 layer with a skip tensor
+    s = LayerSpec("conv3x3_256to256_80_residual", 8, 80, 80, 256, 256, 3, 3, 1, 1, 1, dtype="bf16",
+                  act="mish", x_dist=("normal", 1.0))
+    d = make_layer(s, g)
+    x, w, b = d.x.to(dev), d.w.to(dev), d.b.to(dev)
+    r = torch.randn(8, 80, 80, 256, generator=g).to(torch.bfloat16).to(dev)
+    y = torch.empty(8, 80, 80, 256, dtype=torch.bfloat16, device=dev)
+    pf = cl.Plan(8, 80, 80, 256, 256, 3, 3, 1, 1, 1, 1, "bf16", "mish", out=dict(residual=True))
+    pp = cl.Plan(8, 80, 80, 256, 256, 3, 3, 1, 1, 1, 1, "bf16", "mish")
+    us = timed(lambda: pf.run(x, w, b, y, residual=r))
+    us_plain = timed(lambda: pp.run(x, w, b, y))
+    rows.append(dict({"row": "residual add (K2)", "layer": s.name, "kernel": pf.describe(), "us": round(us, 2),
+                      "plain_us": round(us_plain, 2)},
+                     **roof(flops_of(s), alg_bytes(s) + r.numel() * 2, us)))
+    # 2. concat + 2x upsample: YOLOv4 neck 1x1 512->256 at 20x20 (batch 8) written
+    #    upsampled into channels 256..511 of a 40x40x512 concat buffer
+    s = LayerSpec("pw1x1_512to256_20_up2_concat", 8, 20, 20, 512, 256, 1, 1, dtype="bf16", act="mish",
+                  x_dist=("normal", 1.0))
+    d = make_layer(s, g)
+    x, w, b = d.x.to(dev), d.w.to(dev), d.b.to(dev)
+    ycat = torch.empty(8, 40, 40, 512, dtype=torch.bfloat16, device=dev)
+    pc = cl.Plan(8, 20, 20, 512, 256, 1, 1, 1, 0, 0, 1, "bf16", "mish",
+                 out=dict(y_channels=512, y_channel_offset=256, upsample=2))
+    us = timed(lambda: pc.run(x, w, b, ycat))
+    nbytes = alg_bytes(s) + 3 * 8 * 20 * 20 * 256 * 2  # the output is written four times
+    rows.append(dict({"row": "concat + 2x upsample (K4)", "layer": s.name, "kernel": pc.describe(),
+                      "us": round(us, 2)}, **roof(flops_of(s), nbytes, us)))
+    # 3. SPP: 8 x 20 x 20 x 512 bf16 -> [mp5 | mp9 | mp13 | x] (2048 channels)
+    xs = torch.randn(8, 20, 20, 512, generator=g).to(torch.bfloat16).to(dev)
+    ys = torch.empty(8, 20, 20, 2048, dtype=torch.bfloat16, device=dev)
+    us = timed(lambda: cl.spp(xs, ys))
+    nbytes = xs.numel() * 2 + ys.numel() * 2
+    rows.append(dict({"row": "SPP max pools 5/9/13 (K3)", "layer": "spp_20x20x512_b8", "kernel": "spp cascaded 5x5",
+                      "us": round(us, 2)}, **roof(0.0, nbytes, us)))
+    return rows
 
 
 def run_e2e(args, layers, plans, dev, stream, total_flops, world):
@@ -415,6 +498,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-next-rows", action="store_true", help="skip timing the residual / concat / SPP rows")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

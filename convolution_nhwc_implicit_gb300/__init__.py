@@ -18,7 +18,7 @@ import ctypes
 import os
 
 __all__ = ["Plan", "ConvError", "conv2d_nhwc", "library_path", "load_library", "DTYPES", "ACTS",
-           "ALGOS", "status_str", "abi_version", "run_i8_noalloc", "NOALLOC_MAX_COUT"]
+           "ALGOS", "status_str", "abi_version", "run_i8_noalloc", "NOALLOC_MAX_COUT", "spp"]
 
 # Largest c_out conv_run_i8_noalloc accepts (its fixed scratch array holds
 # that many requantisation multipliers).
@@ -90,6 +90,8 @@ def load_library():
     lib.conv_plan_output_shape.restype = c_int
     lib.conv_plan_algo.argtypes = [c_void_p]
     lib.conv_plan_algo.restype = c_int
+    lib.conv_plan_launches.argtypes = [c_void_p]
+    lib.conv_plan_launches.restype = c_int
     lib.conv_plan_describe.argtypes = [c_void_p]
     lib.conv_plan_describe.restype = ctypes.c_char_p
     lib.conv_plan_check_device_status.argtypes = [c_void_p, c_void_p]
@@ -102,6 +104,9 @@ def load_library():
                                         ctypes.POINTER(_Quant), c_void_p, c_void_p, c_void_p, c_void_p,
                                         c_void_p]
     lib.conv_run_i8_noalloc.restype = c_int
+    lib.conv_spp_run.argtypes = [c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
+                                 c_int, c_void_p]
+    lib.conv_spp_run.restype = c_int
     _lib = lib
     return lib
 
@@ -190,6 +195,11 @@ class Plan:
     def algo(self) -> str:
         return ALGO_NAMES[self._lib.conv_plan_algo(self._handle)]
 
+    @property
+    def launches(self) -> int:
+        """Kernels one run() enqueues."""
+        return self._lib.conv_plan_launches(self._handle)
+
     def describe(self) -> str:
         return self._lib.conv_plan_describe(self._handle).decode()
 
@@ -257,3 +267,21 @@ def run_i8_noalloc(x, w, b, y, stride=1, pad=(0, 0), groups=1, act="none", quant
     if rc != 0:
         raise ConvError("conv_run_i8_noalloc", rc)
     return y
+
+
+def spp(x, y, y_channels=None, off5=None, off9=None, off13=None, off_x=-1, stream=None):
+    """SPP block (conv_spp_run): the 5x5, 9x9 and 13x13 max pools of x (NHWC,
+    torch CUDA tensor) written into channel slices of y.  Defaults: y has
+    4*C channels laid out [mp5 | mp9 | mp13 | x]."""
+    n, h, w, c = x.shape
+    y_channels = y_channels or 4 * c
+    off5 = 0 if off5 is None else off5
+    off9 = c if off9 is None else off9
+    off13 = 2 * c if off13 is None else off13
+    if off_x is None:
+        off_x = 3 * c
+    dt = {"torch.float32": 0, "torch.bfloat16": 1, "torch.int8": 2}[str(x.dtype)]
+    rc = load_library().conv_spp_run(n, h, w, c, dt, _ptr(x), _ptr(y), y_channels, off5, off9, off13, off_x,
+                                     _stream_handle(stream))
+    if rc != 0:
+        raise ConvError("conv_spp_run", rc)

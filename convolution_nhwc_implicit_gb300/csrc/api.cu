@@ -278,6 +278,12 @@ int conv_plan_algo(const conv_plan_t *plan) {
 
 const char *conv_plan_describe(const conv_plan_t *plan) { return plan ? plan->desc : ""; }
 
+int conv_plan_launches(const conv_plan_t *plan) {
+    if (!plan) return CONV_ERR_NULL_ARG;
+    if (plan->s.n == 0) return 0;
+    return (plan->algo == CONV_ALGO_IGEMM && plan->ig.prep) ? 2 : 1;
+}
+
 int conv_run_fused(const conv_plan_t *plan, const void *x, const void *w, const void *bias, const void *residual,
                    void *y, void *stream) {
     if (!plan) return CONV_ERR_NULL_ARG;

@@ -187,6 +187,25 @@ CONV_API int conv_plan_create_fused(const conv_shape_t *shape, int stride, int p
 CONV_API int conv_run_fused(const conv_plan_t *plan, const void *x, const void *w, const void *bias,
                             const void *residual, void *y, void *stream);
 
+/* ---------------------------------------------------------------------------
+ * SPP block ("YOLOv4, optimized for Wormhole", section 9, K3): the max pools
+ * of x over 5x5, 9x9 and 13x13 windows, stride 1, output the size of x,
+ * positions outside the image never winning the max:
+ *   mpK[n,h,w,c] = max { x[n,i,j,c] : |i-h| <= K/2, |j-w| <= K/2, in the image }
+ * each written to its own channel slice of y, a [N][H][W][y_channels]
+ * buffer (the next layer's concatenated layout):
+ *   y[n,h,w,off5+c] = mp5, y[n,h,w,off9+c] = mp9, y[n,h,w,off13+c] = mp13,
+ *   and, when off_x >= 0, y[n,h,w,off_x+c] = x[n,h,w,c].
+ * x [N][H][W][C] and y are device pointers of dtype (F32, BF16 or I8), 16-byte
+ * aligned, not overlapping.  C * esize, y_channels * esize and every offset *
+ * esize must be multiples of 16 bytes (CONV_ERR_MISALIGNED); the slices must
+ * lie inside y and not overlap one another (CONV_ERR_INVALID_ARG).  Results
+ * are exact (bit-identical to a direct evaluation of each window).
+ * Asynchronous on `stream`; allocates nothing. */
+CONV_API int conv_spp_run(int32_t n, int32_t h, int32_t w, int32_t c, conv_dtype_t dtype, const void *x,
+                          void *y, int32_t y_channels, int32_t off5, int32_t off9, int32_t off13,
+                          int32_t off_x, void *stream);
+
 /* Enqueues the layer on `stream` (a cudaStream_t; NULL = legacy default
  * stream).  x, w, y are device pointers, bias a device pointer or NULL; all
  * 16-byte aligned.  y must not overlap x, w or bias.  Asynchronous: errors
@@ -205,6 +224,10 @@ CONV_API int conv_plan_output_shape(const conv_plan_t *plan, int *oh, int *ow);
 
 /* The kernel family (conv_algo_t) the plan runs, or a negative error. */
 CONV_API int conv_plan_algo(const conv_plan_t *plan);
+
+/* Number of kernels conv_run enqueues for this plan (the tensor-core path of
+ * int8 and small-Cin layers adds its widening pre-pass), or a negative error. */
+CONV_API int conv_plan_launches(const conv_plan_t *plan);
 
 /* A short human-readable description of the kernel and tiling chosen. */
 CONV_API const char *conv_plan_describe(const conv_plan_t *plan);

@@ -77,6 +77,8 @@ def _load():
             lib.oracle_conv_i8_points.restype = i
             lib.oracle_max_threads.argtypes = [i]
             lib.oracle_max_threads.restype = i
+            lib.oracle_maxpool_same.argtypes = [p, p] + [i] * 6
+            lib.oracle_maxpool_same.restype = i
             _lib = lib
     return _lib
 
@@ -241,3 +243,21 @@ def place_output(y, y_channels, y_channel_offset=0, upsample=1, fill=np.nan):
     rep = np.repeat(np.repeat(y, upsample, axis=1), upsample, axis=2)
     out[..., y_channel_offset:y_channel_offset + C] = rep
     return out
+
+
+def maxpool_same(x, k, threads=0):
+    """k x k max pool, stride 1, output the size of the input, positions
+    outside the image left out of the max (the pools of the YOLOv4 SPP block,
+    "YOLOv4, optimized for Wormhole", section 9, K3).  Direct evaluation
+    over each window in oracle.c.  x NHWC; returns float64 (exact)."""
+    xd = np.ascontiguousarray(x, dtype=np.float64)
+    N, H, W, C = xd.shape
+    y = np.empty_like(xd)
+    if _load().oracle_maxpool_same(_ptr(xd), _ptr(y), N, H, W, C, int(k), threads):
+        raise ValueError("oracle_maxpool_same rejected the arguments")
+    return y
+
+
+def spp(x, threads=0):
+    """The SPP block's three pools of x: (mp5, mp9, mp13)."""
+    return tuple(maxpool_same(x, k, threads) for k in (5, 9, 13))

@@ -330,3 +330,42 @@ int oracle_max_threads(int nthreads)
     return 1;
 #endif
 }
+
+/*
+ * Max pooling with stride 1 and an output the size of the input: a k x k
+ * window (k odd) centred on every pixel, positions outside the image left out
+ * of the max (they never win it).  These are the three pools (k = 5, 9, 13)
+ * of the YOLOv4 SPP block ("YOLOv4, optimized for Wormhole", section 9, K3).
+ * Evaluated directly over the whole window -- not as the cascade of smaller
+ * windows the fast kernel uses, so that the cascade identity is checked
+ * rather than assumed.  x, y NHWC, C channels; exact for any input values.
+ */
+int oracle_maxpool_same(const double *x, double *y, int N, int H, int W, int C, int k, int nthreads)
+{
+    if (!x || !y || N < 0 || H < 1 || W < 1 || C < 1 || k < 1 || (k % 2) == 0)
+        return -1;
+    set_threads(nthreads);
+    const int r = k / 2;
+    const long long rows = (long long)N * H;
+#pragma omp parallel for schedule(static)
+    for (long long nh = 0; nh < rows; ++nh) {
+        const int n = (int)(nh / H), h = (int)(nh % H);
+        for (int w = 0; w < W; ++w)
+            for (int c = 0; c < C; ++c) {
+                double m = -INFINITY;
+                for (int i = h - r; i <= h + r; ++i) {
+                    if (i < 0 || i >= H)
+                        continue;
+                    for (int j = w - r; j <= w + r; ++j) {
+                        if (j < 0 || j >= W)
+                            continue;
+                        const double v = x[(((long long)n * H + i) * W + j) * C + c];
+                        if (v > m)
+                            m = v;
+                    }
+                }
+                y[(((long long)n * H + h) * W + w) * C + c] = m;
+            }
+    }
+    return 0;
+}

@@ -164,3 +164,18 @@ def test_output_options_are_validated_before_cuda(lib, dtype, out, expect):
     else:
         assert rc == expect
         assert h.value is None
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((1, 8, 8, 16, 1, 64, 0, 16, 32, 48), 0),     # valid (n = 0 below: no CUDA needed)
+    ((1, 8, 8, 16, 1, 64, 0, 8, 32, 48), -9),     # mp5 and mp9 slices overlap
+    ((1, 8, 8, 16, 1, 64, 0, 16, 56, -1), -9),    # mp13 slice past y's 64 channels
+    ((1, 8, 8, 16, 1, 64, 4, 24, 40, -1), -4),    # offset of 8 bytes
+    ((1, 8, 8, 12, 1, 64, 0, 16, 32, -1), -4),    # C of 24 bytes
+    ((1, 8, 8, 16, 1, 64, -1, 16, 32, 48), -9),   # the three pools are always written
+    ((1, 8, 8, 16, 7, 64, 0, 16, 32, 48), -9),    # bad dtype
+])
+def test_spp_arguments_are_validated_before_cuda(lib, args, expect):
+    n, h, w, c, dt, cy, o5, o9, o13, ox = args
+    rc = lib.conv_spp_run(0, h, w, c, dt, None, None, cy, o5, o9, o13, ox, None)
+    assert rc == expect

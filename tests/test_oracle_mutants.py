@@ -31,6 +31,8 @@ MUTANTS = {
                  "return v * fmin(fmax(v + 2.0, 0.0), 2.0) / 2.0;"),
     "relu_as_abs": ("return v > 0.0 ? v : 0.0;", "return fabs(v);"),
     "stride_ignored_w": ("int iw = ow * stride - pad_w + s;", "int iw = ow - pad_w + s;"),
+    "maxpool_zero_padding": ("double m = -INFINITY;", "double m = 0.0;"),
+    "maxpool_window_short": ("for (int j = w - r; j <= w + r; ++j) {", "for (int j = w - r; j < w + r; ++j) {"),
 }
 
 

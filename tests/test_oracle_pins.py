@@ -380,3 +380,43 @@ def test_place_output_concat_and_upsample():
     # no upsampling, no offset: the output itself
     z = np.arange(24.0).reshape(1, 2, 3, 4)
     assert np.array_equal(oracle.place_output(z, 4), z)
+
+
+# ---------------------------------------------------------------- SPP max pools (K3)
+
+def _maxpool_numpy(x, k):
+    # independent restatement: pad with -inf and take the max of all k*k shifts
+    r = k // 2
+    N, H, W, C = x.shape
+    p = np.full((N, H + 2 * r, W + 2 * r, C), -np.inf)
+    p[:, r:r + H, r:r + W] = x
+    out = np.full(x.shape, -np.inf)
+    for i in range(k):
+        for j in range(k):
+            out = np.maximum(out, p[:, i:i + H, j:j + W])
+    return out
+
+
+@pytest.mark.parametrize("k", [1, 3, 5, 9, 13])
+def test_maxpool_same_matches_shifted_maximum(k):
+    rng = np.random.default_rng(k)
+    x = rng.normal(0, 1, (2, 7, 11, 3))
+    assert np.array_equal(oracle.maxpool_same(x, k), _maxpool_numpy(x, k))
+
+
+def test_maxpool_same_hand_case_and_negative_edges():
+    # 1 x 3 x 3, all values negative: padding must never win the max
+    x = -np.arange(1, 10, dtype=np.float64).reshape(1, 3, 3, 1)
+    y = oracle.maxpool_same(x, 3)[0, :, :, 0]
+    assert np.array_equal(y, [[-1, -1, -2], [-1, -1, -2], [-4, -4, -5]])
+    # a window wider than the image covers it all
+    assert np.all(oracle.maxpool_same(x, 13) == -1)
+
+
+def test_spp_cascade_identity_holds_for_the_oracle():
+    # mp9 = mp5(mp5), mp13 = mp5(mp5(mp5)): the identity the fast kernel uses
+    rng = np.random.default_rng(3)
+    x = rng.integers(-128, 128, (1, 12, 9, 4)).astype(np.float64)
+    p5, p9, p13 = oracle.spp(x)
+    assert np.array_equal(p9, oracle.maxpool_same(p5, 5))
+    assert np.array_equal(p13, oracle.maxpool_same(p9, 5))
