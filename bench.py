@@ -392,16 +392,39 @@ def run_e2e(args, layers, plans, dev, stream, total_flops, world):
             "ms_per_step": round(ms / k, 4)}
 
 
+# Source files that define each kernel family (a change to any of them voids
+# the DRAM traffic captured for that family).
+_FAMILY_SOURCES = {
+    "igemm": ["k_igemm.cu", "k_igemm_kernel.cuh", "k_prep.cu", "tc_ptx.cuh", "epilogue.cuh", "conv_internal.h"],
+    "dw3x3": ["k_dw3x3.cu", "tc_ptx.cuh", "epilogue.cuh", "conv_internal.h"],
+    "direct": ["k_direct.cu", "epilogue.cuh", "conv_internal.h"],
+}
+
+
+def kernel_sources_sha1(kernel_desc):
+    """sha1 of the source files of the kernel family a plan description names."""
+    import hashlib
+    fam = next((f for f in _FAMILY_SOURCES if kernel_desc.startswith(f)), None)
+    if fam is None:
+        return None
+    h = hashlib.sha1()
+    for name in _FAMILY_SOURCES[fam]:
+        with open(os.path.join(ROOT, "convolution_nhwc_implicit_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
 def _traffic_for(layer_name, kernel_desc):
     """DRAM bytes per launch of this kernel from the committed ncu summary
-    (profiles/dram_traffic.json), if it was captured for this exact kernel."""
+    (profiles/dram_traffic.json), if it was captured for this exact kernel
+    configuration and its sources have not changed since; else None."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     e = d.get(layer_name)
-    if not e or e.get("kernel") != kernel_desc:
+    if not e or e.get("kernel") != kernel_desc or e.get("sources_sha1") != kernel_sources_sha1(kernel_desc):
         return None
     return e.get("bytes_per_launch")
 
