@@ -57,13 +57,24 @@ def flops_of(spec):
     return 2.0 * macs(spec)
 
 
+def compute_peak(spec, peaks):
+    """The compute roof of a layer's own arithmetic: bf16 layers and the int8
+    layers (which this library contracts as exact bf16 MMAs) take the measured
+    bf16 tensor peak; fp32 layers (FFMA, never TF32) the FFMA peak, SMs x 128
+    lanes x 2 flops x the maximum SM clock.  Returns (TFLOP/s, roof name)."""
+    if spec.dtype == "f32":
+        return peaks["fp32_ffma_tflops"], "alu"
+    return peaks["bf16_tflops"], "tensor"
+
+
 def layer_bound(spec, peaks):
     """Which roof binds a layer: compare its arithmetic intensity with the
-    ridge (bf16 peak / HBM bandwidth)."""
+    ridge (its compute peak / HBM bandwidth)."""
     from conv_workloads import alg_bytes
     ai = flops_of(spec) / alg_bytes(spec)
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    return ("tensor" if ai >= ridge else "hbm"), ai
+    pk, roof = compute_peak(spec, peaks)
+    ridge = pk * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    return (roof if ai >= ridge else "hbm"), ai
 
 
 # ---------------------------------------------------------------- clocks
@@ -148,6 +159,10 @@ def run_ours(args, rank, world, device):
     peaks, peaks_src = load_peaks()
     torch.cuda.set_device(device)
     dev = torch.device("cuda", device)
+    # FFMA peak of the fp32 layers: SMs x 128 FP32 lanes x 2 flops x max SM clock
+    props = torch.cuda.get_device_properties(dev)
+    sm_mhz = float(peaks.get("sm_max_mhz") or 2070.0)
+    peaks["fp32_ffma_tflops"] = round(props.multi_processor_count * 128 * 2 * sm_mhz * 1e6 / 1e12, 1)
     layers = generate(args.workload)
     plans, X, Wt, B, Y = [], [], [], [], []
     for d in layers:
@@ -212,6 +227,14 @@ def run_ours(args, rank, world, device):
     wall = time.perf_counter() - t0
     clocks.mark("t_end")
     clk = clocks.stop()
+    # warm-L2 figures (outside the timed region): replays back to back with
+    # no flush, so each layer's inputs are whatever L2 kept from the last replay
+    warm_rows = []
+    for k in range(20):
+        graph.replay()
+        torch.cuda.synchronize()
+        warm_rows.append([ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(nl)])
+    warm = np.median(np.array(warm_rows), axis=0)
     for p in plans:
         p.check_device_status()
     my_ms = float(step_ms.sum())
@@ -227,16 +250,17 @@ def run_ours(args, rank, world, device):
     layer_rows = []
     for i, d in enumerate(layers):
         s = d.spec
-        us = float(per_layer[:, i].mean() * 1e3)
+        us = float(np.median(per_layer[:, i]) * 1e3)
         bound, ai = layer_bound(s, peaks)
         fl = flops_of(s)
         by = alg_bytes(s)
-        if bound == "tensor":
-            ach, pk, unit = fl / (us * 1e-6) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+        if bound != "hbm":
+            ach, pk, unit = fl / (us * 1e-6) / 1e12, compute_peak(s, peaks)[0], "TFLOP/s"
         else:
             ach, pk, unit = by / (us * 1e-6) / 1e9, peaks["hbm_gbs"], "GB/s"
         layer_rows.append({
             "layer": s.name, "kernel": plans[i].describe(), "us": round(us, 2),
+            "us_mean": round(float(per_layer[:, i].mean() * 1e3), 2), "us_warm_l2": round(float(warm[i]), 2),
             "tflops": round(fl / (us * 1e-6) / 1e12, 1), "gbs": round(by / (us * 1e-6) / 1e9, 1),
             "ai_flop_per_byte": round(ai, 1), "bound": bound,
             "achieved": round(ach, 1), "peak": pk, "unit": unit, "frac": round(ach / pk, 4),
@@ -246,7 +270,30 @@ def run_ours(args, rank, world, device):
     traffic = _traffic_for(layers[dom].spec.name, plans[dom].describe())
     roofline = {"bound": dr["bound"], "achieved": dr["achieved"], "peak": dr["peak"], "unit": dr["unit"],
                 "frac": dr["frac"], "traffic": traffic, "kernel": layers[dom].spec.name,
-                "peak_source": f"{peaks_src} ({'bf16 burst' if dr['bound'] == 'tensor' else 'HBM copy'})"}
+                "peak_source": {"tensor": f"{peaks_src} (bf16 burst)", "hbm": f"{peaks_src} (HBM copy)",
+                                "alu": "derived: SMs x 128 FP32 lanes x 2 x max SM clock"}[dr["bound"]]}
+
+    # ---- int8 context: the tensor cores' int8 rate as torch exposes it (these
+    # layers themselves run as exact bf16 MMAs, so their roof is the bf16 peak)
+    int8_probe = None
+    if any(d.spec.dtype == "i8" for d in layers):
+        try:
+            a8 = torch.randint(-128, 128, (8192, 8192), dtype=torch.int8, device=dev)
+            b8 = torch.randint(-128, 128, (8192, 8192), dtype=torch.int8, device=dev).t()
+            best = None
+            for _ in range(10):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                torch._int_mm(a8, b8)
+                e1.record()
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1)
+                best = ms if best is None else min(best, ms)
+            int8_probe = {"int8_tops": round(2 * 8192 ** 3 / (best * 1e-3) / 1e12, 1),
+                          "how": "torch._int_mm 8192^3, best of 10"}
+            del a8, b8
+        except Exception as e:  # no int8 GEMM in this torch build
+            int8_probe = {"unavailable": str(e)[:120]}
 
     # ---- end to end through the same API, from pinned host memory
     e2e = run_e2e(args, layers, plans, dev, stream, total_flops, world)
@@ -261,6 +308,9 @@ def run_ours(args, rank, world, device):
                    "launch": "CUDA graph replay of the step (events inside the graph)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roofline, "layers": layer_rows, "e2e": e2e,
+        "peaks": {"bf16_tflops": peaks["bf16_tflops"], "hbm_gbs": peaks["hbm_gbs"],
+                  "fp32_ffma_tflops": peaks["fp32_ffma_tflops"], "source": peaks_src,
+                  "int8_probe": int8_probe},
         "next_rows": measure_next_rows(dev, peaks) if rank == 0 and not args.no_next_rows else None,
         "gpu_launches": sum(p.launches for p in plans) * args.steps, "clocks": clk,
         "wall_s_timed_region": round(wall, 4),
@@ -346,6 +396,33 @@ def measure_next_rows(dev, peaks, reps=30):
     nbytes = xs.numel() * 2 + ys.numel() * 2
     rows.append(dict({"row": "SPP max pools 5/9/13 (K3)", "layer": "spp_20x20x512_b8", "kernel": "spp cascaded 5x5",
                       "us": round(us, 2)}, **roof(0.0, nbytes, us)))
+    # 4. fused depthwise -> pointwise pair: the KWS DS-CNN block (1x25x5x64,
+    #    fp32, ReLU / ReLU), beside the same two layers run as two plans
+    xk = torch.empty(1, 25, 5, 64).uniform_(-1, 1, generator=g).to(dev)
+    wd = (torch.randn(64, 3, 3, 1, generator=g) * (2 / 9) ** 0.5).to(dev)
+    bd = (torch.randn(64, generator=g) * 0.01).to(dev)
+    wp = (torch.randn(64, 1, 1, 64, generator=g) * (2 / 64) ** 0.5).to(dev)
+    bp = (torch.randn(64, generator=g) * 0.01).to(dev)
+    yk = torch.empty(1, 25, 5, 64, device=dev)
+    zk = torch.empty(1, 25, 5, 64, device=dev)
+    pf = cl.DwpwPlan(1, 25, 5, 64, 64, 1, 1, "f32", "relu", "relu")
+    p1 = cl.Plan(1, 25, 5, 64, 64, 3, 3, 1, 1, 1, 64, "f32", "relu")
+    p2 = cl.Plan(1, 25, 5, 64, 64, 1, 1, 1, 0, 0, 1, "f32", "relu")
+    us = timed(lambda: pf.run(xk, wd, bd, wp, bp, yk))
+
+    def two():
+        p1.run(xk, wd, bd, zk)
+        p2.run(zk, wp, bp, yk)
+    us_two = timed(two)
+    fl = 2.0 * 125 * 64 * (9 + 64)
+    nbytes = 4 * (125 * 64 * 2 + 64 * 9 + 64 * 64 + 128)
+    ach = nbytes / (us * 1e-6) / 1e9  # far below the FFMA ridge: HBM (latency) bound
+    rows.append({"row": "fused dw3x3 -> pw1x1 (DS-CNN block)", "layer": "kws_ds_block_25x5x64_f32",
+                 "kernel": pf.describe(), "us": round(us, 2), "plain_us": round(us_two, 2),
+                 "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                 "frac": round(ach / peaks["hbm_gbs"], 4),
+                 "tflops": round(fl / (us * 1e-6) / 1e12, 3),
+                 "note": "plain_us: the depthwise and pointwise plans run one after the other"})
     return rows
 
 

@@ -18,7 +18,7 @@ import ctypes
 import os
 
 __all__ = ["Plan", "ConvError", "conv2d_nhwc", "library_path", "load_library", "DTYPES", "ACTS",
-           "ALGOS", "status_str", "abi_version", "run_i8_noalloc", "NOALLOC_MAX_COUT", "spp"]
+           "ALGOS", "status_str", "abi_version", "run_i8_noalloc", "NOALLOC_MAX_COUT", "spp", "DwpwPlan"]
 
 # Largest c_out conv_run_i8_noalloc accepts (its fixed scratch array holds
 # that many requantisation multipliers).
@@ -30,7 +30,7 @@ _LIB_PATH = os.path.join(_HERE, "libconv_nhwc.so")
 DTYPES = {"f32": 0, "bf16": 1, "i8": 2}
 ACTS = {"none": 0, "relu": 1, "mish": 2}
 ALGOS = {"auto": 0, "direct": 1, "depthwise": 2, "igemm": 3, "igemm_swapped": 4, "igemm_n256": 5,
-         "igemm_n128": 6, "igemm_n64": 7, "igemm_pair": 8}
+         "igemm_n128": 6, "igemm_n64": 7, "igemm_pair": 8, "dwpw": 9}
 ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 
 
@@ -104,6 +104,10 @@ def load_library():
                                         ctypes.POINTER(_Quant), c_void_p, c_void_p, c_void_p, c_void_p,
                                         c_void_p]
     lib.conv_run_i8_noalloc.restype = c_int
+    lib.conv_plan_create_dwpw.argtypes = [ctypes.POINTER(_Shape), c_int, c_int, c_int, c_int, c_int, pp]
+    lib.conv_plan_create_dwpw.restype = c_int
+    lib.conv_run_dwpw.argtypes = [c_void_p] * 8
+    lib.conv_run_dwpw.restype = c_int
     lib.conv_spp_run.argtypes = [c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
                                  c_int, c_void_p]
     lib.conv_spp_run.restype = c_int
@@ -285,3 +289,33 @@ def spp(x, y, y_channels=None, off5=None, off9=None, off13=None, off_x=-1, strea
                                      _stream_handle(stream))
     if rc != 0:
         raise ConvError("conv_spp_run", rc)
+
+
+class DwpwPlan(Plan):
+    """A fused depthwise 3x3 -> pointwise 1x1 pair (conv_plan_create_dwpw):
+    y = act_pw(pw(round(act_dw(dw(x) + b_dw))) + b_pw), the intermediate kept
+    on chip."""
+
+    def __init__(self, n, h, w, c, c_out, stride=1, pad=1, dtype="f32", act_dw="relu", act_pw="relu"):
+        lib = load_library()
+        self._lib = lib
+        self._handle = ctypes.c_void_p()
+        self.shape = (n, h, w, c, c_out, 3, 3)
+        self.stride, self.pad_h, self.pad_w, self.groups = stride, pad, pad, 1
+        self.dtype, self.act, self.act_pw = dtype, act_dw, act_pw
+        self.out = dict(y_channels=c_out, y_channel_offset=0, upsample=1, residual=False)
+        shape = _Shape(n, h, w, c, c_out, 3, 3)
+        rc = lib.conv_plan_create_dwpw(ctypes.byref(shape), stride, pad, DTYPES[dtype], ACTS[act_dw], ACTS[act_pw],
+                                       ctypes.byref(self._handle))
+        if rc != 0:
+            raise ConvError("conv_plan_create_dwpw", rc)
+        oh, ow = ctypes.c_int(), ctypes.c_int()
+        lib.conv_plan_output_shape(self._handle, ctypes.byref(oh), ctypes.byref(ow))
+        self.oh, self.ow = oh.value, ow.value
+
+    def run(self, x, w_dw, b_dw, w_pw, b_pw, y, stream=None) -> None:  # noqa: D401
+        """Enqueue the fused pair on `stream` (default: torch's current stream)."""
+        rc = self._lib.conv_run_dwpw(self._handle, _ptr(x), _ptr(w_dw), _ptr(b_dw), _ptr(w_pw), _ptr(b_pw),
+                                     _ptr(y), _stream_handle(stream))
+        if rc != 0:
+            raise ConvError("conv_run_dwpw", rc)

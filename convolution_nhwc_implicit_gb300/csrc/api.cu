@@ -242,6 +242,86 @@ int conv_plan_create_fused(const conv_shape_t *shape, int stride, int pad_h, int
     return CONV_OK;
 }
 
+int conv_plan_create_dwpw(const conv_shape_t *shape, int stride, int pad, conv_dtype_t dtype, conv_act_t act_dw,
+                          conv_act_t act_pw, conv_plan_t **out_plan) {
+    if (!out_plan) return CONV_ERR_NULL_ARG;
+    *out_plan = nullptr;
+    if (!shape) return CONV_ERR_NULL_ARG;
+    if ((int)act_pw < CONV_ACT_NONE || (int)act_pw > CONV_ACT_MISH) return CONV_ERR_INVALID_ARG;
+    if (shape->k_h != 3 || shape->k_w != 3) return CONV_ERR_INVALID_SHAPE;
+    if ((int)dtype == CONV_I8) return CONV_ERR_UNSUPPORTED;
+    // the depthwise layer validates the input, stride, pad and dtype
+    conv_shape_t dws = *shape;
+    dws.c_out = shape->c_in;
+    int oh = 0, ow = 0;
+    int rc = validate(&dws, stride, pad, pad, shape->c_in, dtype, act_dw, nullptr, &oh, &ow);
+    if (rc != CONV_OK) return rc;
+    if (shape->c_out < 1) return CONV_ERR_INVALID_SHAPE;
+    if (shape->c_in % 4 != 0) return CONV_ERR_UNSUPPORTED;
+    if ((long long)shape->n * oh * ow * shape->c_out >= (1ll << 40)) return CONV_ERR_UNSUPPORTED;
+
+    conv_plan *p = new (std::nothrow) conv_plan();
+    if (!p) return CONV_ERR_OOM;
+    p->s = *shape;
+    p->stride = stride; p->pad_h = pad; p->pad_w = pad; p->groups = 1;
+    p->dtype = dtype; p->act = act_dw; p->act2 = act_pw; p->oh = oh; p->ow = ow;
+    p->y_c = shape->c_out; p->y_coff = 0; p->up = 1; p->has_res = 0;
+    cudaDeviceProp prop;
+    if (cudaGetDevice(&p->device) != cudaSuccess || cudaGetDeviceProperties(&prop, p->device) != cudaSuccess) {
+        delete p;
+        return CONV_ERR_CUDA;
+    }
+    if (prop.major != 10 || prop.minor != 3) {
+        delete p;
+        return CONV_ERR_UNSUPPORTED;
+    }
+    p->num_sms = prop.multiProcessorCount;
+    if (!dwpw_supported(p)) {
+        delete p;
+        return CONV_ERR_UNSUPPORTED;
+    }
+    p->algo = CONV_ALGO_DWPW;
+    if (cudaMalloc(&p->d_status, sizeof(int)) != cudaSuccess) {
+        delete p;
+        return CONV_ERR_OOM;
+    }
+    if (cudaMemset(p->d_status, 0, sizeof(int)) != cudaSuccess) {
+        conv_plan_destroy(p);
+        return CONV_ERR_CUDA;
+    }
+    rc = dwpw_configure(p);
+    if (rc != CONV_OK) {
+        conv_plan_destroy(p);
+        return rc;
+    }
+    snprintf(p->desc, sizeof(p->desc), "dw3x3+pw1x1 %s fused tile=%dx%d halo=%dx%d co/cta=%d ctas=%lld",
+             dtype == CONV_F32 ? "f32" : "bf16", p->dwpw.th, p->dwpw.tw, p->dwpw.hin, p->dwpw.win,
+             p->dwpw.cochunk, (long long)p->dwpw.tiles_w * p->dwpw.tiles_h * shape->n * p->dwpw.chunks);
+    *out_plan = p;
+    return CONV_OK;
+}
+
+int conv_run_dwpw(const conv_plan_t *plan, const void *x, const void *w_dw, const void *b_dw, const void *w_pw,
+                  const void *b_pw, void *y, void *stream) {
+    if (!plan) return CONV_ERR_NULL_ARG;
+    const conv_plan *p = plan;
+    if (p->algo != CONV_ALGO_DWPW) return CONV_ERR_INVALID_ARG;
+    if (p->s.n == 0) return CONV_OK;
+    if (!x || !w_dw || !w_pw || !y) return CONV_ERR_NULL_ARG;
+    if (!aligned16(x) || !aligned16(w_dw) || !aligned16(w_pw) || !aligned16(y) || (b_dw && !aligned16(b_dw)) ||
+        (b_pw && !aligned16(b_pw)))
+        return CONV_ERR_MISALIGNED;
+    const size_t es = (size_t)conv_esize(p->dtype);
+    const size_t C = (size_t)p->s.c_in, Co = (size_t)p->s.c_out;
+    const size_t xb = (size_t)p->s.n * p->s.h * p->s.w * C * es;
+    const size_t yb = (size_t)p->s.n * p->oh * p->ow * Co * es;
+    if (overlaps(y, yb, x, xb) || overlaps(y, yb, w_dw, C * 9 * es) || overlaps(y, yb, w_pw, Co * C * es) ||
+        overlaps(y, yb, b_dw, b_dw ? C * 4 : 0) || overlaps(y, yb, b_pw, b_pw ? Co * 4 : 0))
+        return CONV_ERR_ALIASING;
+    return launch_dwpw(p, x, w_dw, b_dw, w_pw, b_pw, y, (cudaStream_t)stream) == cudaSuccess ? CONV_OK
+                                                                                             : CONV_ERR_CUDA;
+}
+
 int conv_plan_create_ex(const conv_shape_t *shape, int stride, int pad_h, int pad_w, int groups,
                         conv_dtype_t dtype, conv_act_t act, const conv_quant_t *quant, conv_algo_t algo,
                         conv_plan_t **out_plan) {
@@ -288,6 +368,7 @@ int conv_run_fused(const conv_plan_t *plan, const void *x, const void *w, const 
                    void *y, void *stream) {
     if (!plan) return CONV_ERR_NULL_ARG;
     const conv_plan *p = plan;
+    if (p->algo == CONV_ALGO_DWPW) return CONV_ERR_INVALID_ARG;  // runs through conv_run_dwpw
     if (p->has_res && !residual) return CONV_ERR_NULL_ARG;
     if (!p->has_res && residual) return CONV_ERR_INVALID_ARG;
     if (p->s.n == 0) return CONV_OK;  // empty batch: nothing to compute

@@ -54,6 +54,15 @@ struct DwGeom {
     long long blocks;  // persistent CTAs
 };
 
+struct DwpwGeom {
+    int th, tw;        // output pixels of a CTA tile
+    int hin, win;      // its input halo
+    int cochunk;       // pointwise output channels per CTA (multiple of 4)
+    int chunks;        // ceil(Cout / cochunk)
+    int tiles_w, tiles_h;
+    int smem;          // dynamic shared memory bytes
+};
+
 struct conv_plan {
     conv_shape_t s;
     int stride, pad_h, pad_w, groups;
@@ -69,6 +78,8 @@ struct conv_plan {
     int cin_p;         // channels of those copies
     IgemmGeom ig;
     DwGeom dw;
+    DwpwGeom dwpw;
+    conv_act_t act2;   // fused depthwise -> pointwise plans: the pointwise activation
     int dct, dpt;      // direct kernel: channels / pixels per thread of the smem variant (dct 0: generic)
     // Output options (conv_output_t): y has y_c channels per pixel, the layer
     // writes channels [y_coff, y_coff + c_out) of a (up*OH) x (up*OW) grid,
@@ -88,6 +99,12 @@ cudaError_t launch_dw3x3(const conv_plan *p, const void *x, const void *w, const
 // Returns a CONV_* status (tensor-map encoding can fail on the host).
 int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *bias, const void *res,
                  void *y, cudaStream_t st);
+
+// Fused depthwise 3x3 -> pointwise pair (conv_plan_create_dwpw).
+cudaError_t launch_dwpw(const conv_plan *p, const void *x, const void *wdw, const void *bdw, const void *wpw,
+                        const void *bpw, void *y, cudaStream_t st);
+bool dwpw_supported(const conv_plan *p);
+int dwpw_configure(conv_plan *p);  // CONV_* status
 
 // Widens int8 to bf16 / pads channels into the plan's d_xprep, d_wprep.
 cudaError_t launch_prep(const conv_plan *p, const void *x, const void *w, cudaStream_t st);

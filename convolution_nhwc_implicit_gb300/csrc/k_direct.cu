@@ -189,6 +189,8 @@ direct_conv_smem(DirectArgs a, int chunks_per_group, const T *__restrict__ x, co
     __syncthreads();
 
     const int g0 = g * a.cin_g;
+    // fp32 rows that start on 16-byte boundaries: vector loads of the channels
+    const bool vec4 = sizeof(T) == 4 && (a.Cin % 4) == 0 && (g0 % 4) == 0 && (a.cin_g % 8) == 0;
     long long pix[PT];
     int ihb[PT], iwb[PT], nn[PT];
     bool pv[PT];
@@ -221,13 +223,10 @@ direct_conv_smem(DirectArgs a, int chunks_per_group, const T *__restrict__ x, co
                 xp[i] = x + (((long long)nn[i] * a.H + (ok[i] ? ih : 0)) * a.W + (ok[i] ? iw : 0)) * a.Cin + g0;
             }
             const float *wrow = wsm + (r * a.KW + s) * a.cin_g * CT;
-            for (int ci = 0; ci < a.cin_g; ++ci, wrow += CT) {
-                float xv[PT];
-#pragma unroll
-                for (int i = 0; i < PT; ++i) xv[i] = ok[i] ? Elem<T>::to_f(__ldg(xp[i] + ci)) : 0.0f;
+            auto fma_ci = [&](const float (&xv)[PT], const float *wr) {
 #pragma unroll
                 for (int j = 0; j < CT; j += 4) {
-                    const float4 w4 = *reinterpret_cast<const float4 *>(wrow + j);
+                    const float4 w4 = *reinterpret_cast<const float4 *>(wr + j);
 #pragma unroll
                     for (int i = 0; i < PT; ++i) {
                         acc[i][j] = __fmaf_rn(xv[i], w4.x, acc[i][j]);
@@ -236,6 +235,37 @@ direct_conv_smem(DirectArgs a, int chunks_per_group, const T *__restrict__ x, co
                         acc[i][j + 3] = __fmaf_rn(xv[i], w4.w, acc[i][j + 3]);
                     }
                 }
+            };
+            int ci = 0;
+            if (vec4) {
+                // fp32 channels in 16-byte chunks, two chunks in flight per pixel:
+                // the input loads no longer serialise on their latency
+                for (; ci + 8 <= a.cin_g; ci += 8) {
+                    float4 q0[PT], q1[PT];
+#pragma unroll
+                    for (int i = 0; i < PT; ++i) {
+                        const float4 *p4 = reinterpret_cast<const float4 *>(xp[i] + ci);
+                        q0[i] = ok[i] ? __ldg(p4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        q1[i] = ok[i] ? __ldg(p4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        float xv[PT];
+#pragma unroll
+                        for (int i = 0; i < PT; ++i) {
+                            const float4 &q = e < 4 ? q0[i] : q1[i];
+                            const int k = e & 3;
+                            xv[i] = k == 0 ? q.x : (k == 1 ? q.y : (k == 2 ? q.z : q.w));
+                        }
+                        fma_ci(xv, wrow + (ci + e) * CT);
+                    }
+                }
+            }
+            for (; ci < a.cin_g; ++ci) {
+                float xv[PT];
+#pragma unroll
+                for (int i = 0; i < PT; ++i) xv[i] = ok[i] ? Elem<T>::to_f(__ldg(xp[i] + ci)) : 0.0f;
+                fma_ci(xv, wrow + ci * CT);
             }
         }
     }

@@ -101,6 +101,9 @@ typedef enum {
     CONV_ALGO_IGEMM_N128 = 6,    /* MMA M = 128 pixels, N = 128 output channels */
     CONV_ALGO_IGEMM_N64 = 7,     /* MMA M = 128 pixels, N = 64 output channels  */
     CONV_ALGO_IGEMM_PAIR = 8,    /* CTA-pair MMA on two SMs: M = 256 pixels, N = 256 */
+    /* (reported by conv_plan_algo for plans of conv_plan_create_dwpw; not a
+     * family conv_plan_create_ex can force) */
+    CONV_ALGO_DWPW = 9,          /* fused depthwise 3x3 -> pointwise 1x1 pair */
 } conv_algo_t;
 
 enum {
@@ -205,6 +208,28 @@ CONV_API int conv_run_fused(const conv_plan_t *plan, const void *x, const void *
 CONV_API int conv_spp_run(int32_t n, int32_t h, int32_t w, int32_t c, conv_dtype_t dtype, const void *x,
                           void *y, int32_t y_channels, int32_t off5, int32_t off9, int32_t off13,
                           int32_t off_x, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Fused depthwise-separable pair (the DS-CNN block): a depthwise 3x3
+ * convolution, its bias and activation, then a 1x1 pointwise convolution,
+ * its bias and activation, in one kernel with the intermediate kept in
+ * shared memory ("nanoinfer", "What is still slow": depthwise convolution is
+ * the gap and each layer boundary is a trip through memory):
+ *   z[n,oh,ow,c]  = round( act_dw( b_dw[c] + sum_{r,s<3}
+ *                         x[n, oh*stride-pad+r, ow*stride-pad+s, c] * w_dw[c,r,s,0] ) )
+ *   y[n,oh,ow,co] = act_pw( b_pw[co] + sum_{c} z[n,oh,ow,c] * w_pw[co,0,0,c] )
+ * where round() rounds z to the layer's type (nearest-even bf16; nothing for
+ * fp32), so the pair computes what the two layers run one after the other
+ * compute.  shape: n, h, w of x, c_in = channels of x and z (<= 512, a
+ * multiple of 4), c_out = channels of y; k_h and k_w must be 3.  dtype F32
+ * or BF16 (fp32 arithmetic; I8 is CONV_ERR_UNSUPPORTED).  pad applies to both
+ * axes.  Layouts: x NHWC, w_dw [c_in][3][3][1], w_pw [c_out][1][1][c_in],
+ * b_dw [c_in] and b_pw [c_out] fp32 or NULL, y NHWC [N][OH][OW][c_out].
+ * The plan runs only through conv_run_dwpw (conv_run: CONV_ERR_INVALID_ARG). */
+CONV_API int conv_plan_create_dwpw(const conv_shape_t *shape, int stride, int pad, conv_dtype_t dtype,
+                                   conv_act_t act_dw, conv_act_t act_pw, conv_plan_t **out_plan);
+CONV_API int conv_run_dwpw(const conv_plan_t *plan, const void *x, const void *w_dw, const void *b_dw,
+                           const void *w_pw, const void *b_pw, void *y, void *stream);
 
 /* Enqueues the layer on `stream` (a cudaStream_t; NULL = legacy default
  * stream).  x, w, y are device pointers, bias a device pointer or NULL; all

@@ -261,3 +261,18 @@ def maxpool_same(x, k, threads=0):
 def spp(x, threads=0):
     """The SPP block's three pools of x: (mp5, mp9, mp13)."""
     return tuple(maxpool_same(x, k, threads) for k in (5, 9, 13))
+
+
+def dwpw_f64(x, w_dw, b_dw, w_pw, b_pw, stride=1, pad=1, act_dw="none", act_pw="none", round_to=None,
+             threads=0):
+    """The depthwise-separable pair run one layer after the other, in double:
+    z = act_dw(depthwise 3x3 (x, w_dw) + b_dw), rounded to the layer type
+    (``round_to`` a callable on float64 arrays, e.g. rounding to bf16; None
+    for fp32), then y = act_pw(1x1 (z, w_pw) + b_pw).  w_dw [C,3,3,1],
+    w_pw [Cout,1,1,C].  (The fused kernel keeps z on chip; the result is the
+    same pair of layers.)"""
+    C = np.asarray(x).shape[3]
+    z = conv_f64(x, w_dw, b_dw, stride, pad, pad, C, act_dw, threads)
+    if round_to is not None:
+        z = np.asarray(round_to(z), dtype=np.float64)
+    return conv_f64(z, w_pw, b_pw, 1, 0, 0, 1, act_pw, threads)

@@ -179,3 +179,19 @@ def test_spp_arguments_are_validated_before_cuda(lib, args, expect):
     n, h, w, c, dt, cy, o5, o9, o13, ox = args
     rc = lib.conv_spp_run(0, h, w, c, dt, None, None, cy, o5, o9, o13, ox, None)
     assert rc == expect
+
+
+@pytest.mark.parametrize("shape,kw,expect", [
+    ((1, 8, 8, 16, 16, 5, 5), {}, -2),            # the depthwise kernel is 3x3
+    ((1, 8, 8, 16, 16, 3, 3), {"dtype": 2}, -3),  # int8 pair not offered
+    ((1, 8, 8, 16, 16, 3, 3), {"act_pw": 7}, -9), # bad activation
+    ((1, 8, 8, 16, 16, 3, 3), {"stride": 0}, -2), # validated like the depthwise layer
+])
+def test_dwpw_plan_validation_before_cuda(lib, shape, kw, expect):
+    import convolution_nhwc_implicit_gb300 as cl
+    s = cl._Shape(*shape)
+    h = ctypes.c_void_p(12345)
+    rc = lib.conv_plan_create_dwpw(ctypes.byref(s), kw.get("stride", 1), 1, kw.get("dtype", 0), 1,
+                                   kw.get("act_pw", 1), ctypes.byref(h))
+    assert rc == expect
+    assert h.value is None

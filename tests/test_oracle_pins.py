@@ -420,3 +420,22 @@ def test_spp_cascade_identity_holds_for_the_oracle():
     p5, p9, p13 = oracle.spp(x)
     assert np.array_equal(p9, oracle.maxpool_same(p5, 5))
     assert np.array_equal(p13, oracle.maxpool_same(p9, 5))
+
+
+# ---------------------------------------------------------------- fused dw -> pw pair
+
+def test_dwpw_pair_matches_torch_depthwise_then_pointwise():
+    import torch.nn.functional as F
+    rng = np.random.default_rng(9)
+    x = rng.uniform(-1, 1, (2, 9, 7, 8))
+    wd = rng.normal(0, 0.5, (8, 3, 3, 1))
+    bd = rng.normal(0, 0.1, 8)
+    wp = rng.normal(0, 0.3, (5, 1, 1, 8))
+    bp = rng.normal(0, 0.1, 5)
+    for stride in (1, 2):
+        y = oracle.dwpw_f64(x, wd, bd, wp, bp, stride, 1, "relu", "mish")
+        t = torch.from_numpy(x).permute(0, 3, 1, 2)
+        z = F.relu(F.conv2d(t, torch.from_numpy(wd).permute(0, 3, 1, 2), torch.from_numpy(bd), stride, 1,
+                            groups=8))
+        r = F.mish(F.conv2d(z, torch.from_numpy(wp).permute(0, 3, 1, 2), torch.from_numpy(bp)))
+        assert np.allclose(y, r.permute(0, 2, 3, 1).numpy(), rtol=0, atol=1e-12)
