@@ -30,7 +30,7 @@ _LIB_PATH = os.path.join(_HERE, "libconv_nhwc.so")
 DTYPES = {"f32": 0, "bf16": 1, "i8": 2}
 ACTS = {"none": 0, "relu": 1, "mish": 2}
 ALGOS = {"auto": 0, "direct": 1, "depthwise": 2, "igemm": 3, "igemm_swapped": 4, "igemm_n256": 5,
-         "igemm_n128": 6, "igemm_n64": 7, "igemm_pair": 8, "dwpw": 9}
+         "igemm_n128": 6, "igemm_n64": 7, "igemm_pair": 8, "dwpw": 9, "igemm_pair128": 10}
 ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 
 

@@ -136,7 +136,8 @@ int conv_plan_create_fused(const conv_shape_t *shape, int stride, int pad_h, int
     if (!out_plan) return CONV_ERR_NULL_ARG;
     *out_plan = nullptr;
     if (!shape) return CONV_ERR_NULL_ARG;
-    if ((int)algo < CONV_ALGO_AUTO || (int)algo > CONV_ALGO_IGEMM_PAIR) return CONV_ERR_INVALID_ARG;
+    if ((int)algo < CONV_ALGO_AUTO || ((int)algo > CONV_ALGO_IGEMM_PAIR && algo != CONV_ALGO_IGEMM_PAIR128))
+        return CONV_ERR_INVALID_ARG;
     int oh = 0, ow = 0;
     int rc = validate(shape, stride, pad_h, pad_w, groups, dtype, act, quant, &oh, &ow);
     if (rc != CONV_OK) return rc;
@@ -219,8 +220,10 @@ int conv_plan_create_fused(const conv_shape_t *shape, int stride, int pad_h, int
     }
 
     if (chosen == CONV_ALGO_IGEMM) {
-        // tile layout: 0 = estimated fastest, else swapped / N256 / N128 / N64 / pair
-        rc = igemm_configure(p, algo >= CONV_ALGO_IGEMM_SWAPPED ? (int)algo - CONV_ALGO_IGEMM_SWAPPED + 1 : 0);
+        // tile layout: 0 = estimated fastest, else swapped / N256 / N128 / N64 / pair / pair N128
+        rc = igemm_configure(p, algo == CONV_ALGO_IGEMM_PAIR128
+                                    ? 6
+                                    : (algo >= CONV_ALGO_IGEMM_SWAPPED ? (int)algo - CONV_ALGO_IGEMM_SWAPPED + 1 : 0));
         if (rc != CONV_OK) { conv_plan_destroy(p); return rc; }
     } else if (chosen == CONV_ALGO_DEPTHWISE) {
         rc = dw3x3_configure(p);

@@ -119,8 +119,8 @@ bool igemm_supported(const conv_plan *p);
 // upsample replicas), compiled in its own translation unit.
 void *igemm_select_fused(int bn, int bk, bool flat, bool swap, bool pair);
 // Fills p->ig and sets kernel attributes; CONV_* status.  layout 0 picks
-// the tile layout by estimated time; 1..5 force swapped, N256, N128, N64,
-// CTA pair.
+// the tile layout by estimated time; 1..6 force swapped, N256, N128, N64,
+// CTA pair (N = 256), CTA pair (N = 128).
 int igemm_configure(conv_plan *p, int layout);
 
 // Host-side argument checks shared by the entry points (api.cu).

@@ -56,20 +56,23 @@ void *kernel_ptr_swap(bool flat) {
     return flat ? kernel_ptr<128, BK, true, true>() : kernel_ptr<128, BK, false, true>();
 }
 
-template <int BK>
+template <int BN, int BK>
 void *kernel_ptr_pair(bool flat) {
-    return flat ? kernel_ptr<256, BK, true, false, true>() : kernel_ptr<256, BK, false, false, true>();
+    return flat ? kernel_ptr<BN, BK, true, false, true>() : kernel_ptr<BN, BK, false, false, true>();
+}
+
+template <int BN>
+void *kernel_ptr_pair_bk(int bk, bool flat) {
+    switch (bk) {
+    case 64: return kernel_ptr_pair<BN, 64>(flat);
+    case 32: return kernel_ptr_pair<BN, 32>(flat);
+    default: return kernel_ptr_pair<BN, 16>(flat);
+    }
 }
 
 void *select_kernel(int bn, int bk, bool flat, bool swap, bool pair, bool fused) {
     if (fused) return igemm_select_fused(bn, bk, flat, swap, pair);
-    if (pair) {
-        switch (bk) {
-        case 64: return kernel_ptr_pair<64>(flat);
-        case 32: return kernel_ptr_pair<32>(flat);
-        default: return kernel_ptr_pair<16>(flat);
-        }
-    }
+    if (pair) return bn == 128 ? kernel_ptr_pair_bk<128>(bk, flat) : kernel_ptr_pair_bk<256>(bk, flat);
     if (swap) {
         switch (bk) {
         case 64: return kernel_ptr_swap<64>(flat);
@@ -168,13 +171,13 @@ int igemm_configure(conv_plan *p, int layout) {
     const long long K = (long long)p->s.k_h * g.kw * cin;
     const long long epi_c = p->dtype == CONV_I8 ? 10 : (p->act == CONV_ACT_MISH ? 16 : 6);
     long long best_cost = -1, best_tiles = 0;
-    for (int cand = 0; cand < 5; ++cand) {
+    for (int cand = 0; cand < 6; ++cand) {
         const bool swap = cand == 0;
-        const bool pair = cand == 4;
+        const bool pair = cand == 4 || cand == 5;
         if (swap && p->s.c_out > 128) continue;
         if (pair && p->num_sms < 2) continue;
         if (layout != 0 && layout != cand + 1) continue;
-        const int bn = swap ? 128 : (cand == 1 || pair ? 256 : (cand == 2 ? 128 : 64));
+        const int bn = swap ? 128 : (cand == 1 || cand == 4 ? 256 : (cand == 2 || cand == 5 ? 128 : 64));
         const int P = swap ? kBMSwap : kBM;
         int bw = P, bh = 1, tw = 1, th = 1;
         long long tiles_m;
@@ -276,7 +279,7 @@ int igemm_configure(conv_plan *p, int layout) {
              g.flat ? "flat" : "spatial",
              g.swap ? " swapped" : (g.pair ? " cta-pair" : ""),
              g.swap ? "M=128co N=256px"
-                    : (g.pair ? "M=256px N=256co"
+                    : (g.pair ? (g.bn == 256 ? "M=256px N=256co" : "M=256px N=128co")
                               : (g.bn == 256 ? "M=128px N=256co" : (g.bn == 128 ? "M=128px N=128co" : "M=128px N=64co"))),
              g.bk, g.bh, g.bw, g.stages, g.out_bufs, g.num_tiles, g.grid);
     return CONV_OK;

@@ -27,7 +27,7 @@ void *fused_bk(int bk, bool flat) {
 }  // namespace
 
 void *igemm_select_fused(int bn, int bk, bool flat, bool swap, bool pair) {
-    if (pair) return fused_bk<256, false, true>(bk, flat);
+    if (pair) return bn == 128 ? fused_bk<128, false, true>(bk, flat) : fused_bk<256, false, true>(bk, flat);
     if (swap) return fused_bk<128, true, false>(bk, flat);
     switch (bn) {
     case 256: return fused_bk<256, false, false>(bk, flat);

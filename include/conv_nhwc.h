@@ -104,6 +104,7 @@ typedef enum {
     /* (reported by conv_plan_algo for plans of conv_plan_create_dwpw; not a
      * family conv_plan_create_ex can force) */
     CONV_ALGO_DWPW = 9,          /* fused depthwise 3x3 -> pointwise 1x1 pair */
+    CONV_ALGO_IGEMM_PAIR128 = 10, /* CTA-pair MMA: M = 256 pixels, N = 128 output channels */
 } conv_algo_t;
 
 enum {

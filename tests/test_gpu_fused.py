@@ -73,7 +73,7 @@ def run_fused(spec, out, algo="auto", seed=0):
     return plan
 
 
-LAYOUTS = ["igemm", "igemm_swapped", "igemm_n256", "igemm_n128", "igemm_n64", "igemm_pair"]
+LAYOUTS = ["igemm", "igemm_swapped", "igemm_n256", "igemm_n128", "igemm_n64", "igemm_pair", "igemm_pair128"]
 
 IGEMM_FUSED = [
     (L("res_3x3_64to64", 1, 13, 11, 64, 64, 3, 3, 1, 1, 1), dict(residual=True)),

@@ -68,13 +68,15 @@ IGEMM = [
 # Every case runs with the layout the plan picks and with each forced tile
 # layout: swapped (c_out <= 128 only), N = 256, 128 and 64, and the CTA pair.
 _LAYOUT_DESC = {"igemm_swapped": "swapped", "igemm_n256": "M=128px N=256co", "igemm_n128": "N=128co",
-                "igemm_n64": "N=64co", "igemm_pair": "cta-pair"}
+                "igemm_n64": "N=64co", "igemm_pair": "cta-pair M=256px N=256co",
+                "igemm_pair128": "cta-pair M=256px N=128co"}
 
 
 def with_layouts(specs):
     out = []
     for spec in specs:
-        for lay in ["igemm", "igemm_swapped", "igemm_n256", "igemm_n128", "igemm_n64", "igemm_pair"]:
+        for lay in ["igemm", "igemm_swapped", "igemm_n256", "igemm_n128", "igemm_n64", "igemm_pair",
+                    "igemm_pair128"]:
             if lay == "igemm_swapped" and spec.cout > 128:
                 continue
             out.append(pytest.param(spec, lay, id=f"{spec.name}-{lay}"))
