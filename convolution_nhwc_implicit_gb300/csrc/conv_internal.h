@@ -31,6 +31,7 @@ struct IgemmGeom {
     int kblocks;   // k_h * k_w * cblocks: K blocks per tile
     int stages;    // shared-memory pipeline depth
     int out_bufs;  // epilogue output staging buffers per group (1 or 2)
+    int wres;      // 1: all weights resident in shared memory (one N block, loaded once per CTA)
     int grid;      // persistent CTAs
     int smem;      // dynamic shared memory bytes
     int in_i8;     // operands are int8 (converted to bf16 on chip)

@@ -228,7 +228,7 @@ int igemm_configure(conv_plan *p, int layout) {
     const int P = g.swap ? kBMSwap : kBM;  // pixels per tile (per CTA)
     g.num_tiles = g.tiles_n * (g.pair ? (g.tiles_m + 1) / 2 : g.tiles_m);  // work units
 
-    const int stage_bytes = (P + (g.pair ? g.bn / 2 : g.bn)) * g.bk * 2;
+    int stage_bytes = (P + (g.pair ? g.bn / 2 : g.bn)) * g.bk * 2;
     // Epilogue staging: swapped mode, 16 transpose rows per group; normal
     // mode, 128 rows x 64 B per group and buffer.  Two buffers per group let
     // a group fill one while the TMA store of the other is still reading it;
@@ -240,11 +240,23 @@ int igemm_configure(conv_plan *p, int layout) {
     g.out_bufs = 1;
     if (!g.swap && g.kblocks < 16 && (227 * 1024 - 1024 - 256 - 2 * one_buf) / stage_bytes >= 4) g.out_bufs = 2;
     const int out_bytes = one_buf * g.out_bufs;
-    const int budget = 227 * 1024 - 1024 - 256 - out_bytes;
+    // Resident weights: a single N block whose K blocks all fit beside at
+    // least four activation stages is loaded once per CTA; the ring then
+    // moves activations only (fewer TMA rows per K block).
+    const int wblock = (g.swap ? 128 : g.bn) * g.bk * 2;  // one K block of weights
+    const int act_stage = P * g.bk * 2;
+    const long long wall = (long long)g.kblocks * wblock;
+    g.wres = 0;
+    if (!g.pair && g.tiles_n == 1 &&
+        (227LL * 1024 - 1024 - 512 - out_bytes - wall) / act_stage >= 4) {
+        g.wres = 1;
+        stage_bytes = act_stage;
+    }
+    const int budget = 227 * 1024 - 1024 - 512 - out_bytes - (g.wres ? (int)wall : 0);
     g.stages = budget / stage_bytes;
     if (g.stages > 8) g.stages = 8;
     if (g.stages < 2) return CONV_ERR_UNSUPPORTED;
-    g.smem = 1024 + g.stages * stage_bytes + out_bytes + 8 * (2 * g.stages + 4) + 16;
+    g.smem = 1024 + g.stages * stage_bytes + (g.wres ? (int)wall : 0) + out_bytes + 8 * (2 * g.stages + 5) + 16;
     // Ask for more than half of an SM's shared memory so that no two CTAs of
     // this persistent kernel share an SM: each CTA then owns its TMEM
     // columns (at most 512) without waiting for another to free them.
@@ -273,7 +285,7 @@ int igemm_configure(conv_plan *p, int layout) {
         g.grid = g.num_tiles < p->num_sms ? g.num_tiles : p->num_sms;
     }
     snprintf(p->desc, sizeof(p->desc),
-             "igemm_%s_tcgen05 %s%s %s BK=%d tile=%dx%d stages=%d out_bufs=%d tiles=%d grid=%d",
+             "igemm_%s_tcgen05 %s%s %s BK=%d tile=%dx%d stages=%d%s out_bufs=%d tiles=%d grid=%d",
              p->dtype == CONV_I8 ? (g.fold ? "i8-as-bf16-kwfold" : "i8-as-bf16")
                                  : (g.fold ? "bf16-cpad-kwfold" : (g.prep ? "bf16-cpad" : "bf16")),
              g.flat ? "flat" : "spatial",
@@ -281,7 +293,7 @@ int igemm_configure(conv_plan *p, int layout) {
              g.swap ? "M=128co N=256px"
                     : (g.pair ? (g.bn == 256 ? "M=256px N=256co" : "M=256px N=128co")
                               : (g.bn == 256 ? "M=128px N=256co" : (g.bn == 128 ? "M=128px N=128co" : "M=128px N=64co"))),
-             g.bk, g.bh, g.bw, g.stages, g.out_bufs, g.num_tiles, g.grid);
+             g.bk, g.bh, g.bw, g.stages, g.wres ? " resident-weights" : "", g.out_bufs, g.num_tiles, g.grid);
     return CONV_OK;
 }
 
@@ -380,6 +392,7 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
     a.out_i8 = p->dtype == CONV_I8 ? 1 : 0;
     a.mult = p->d_mult;
     a.out_bufs = g.out_bufs;
+    a.wres = g.wres;
     a.om.Cy = p->y_c; a.om.c_off = p->y_coff; a.om.up = p->up;
     a.om.OH = p->oh; a.om.OW = p->ow; a.om.Cout = p->s.c_out;
     a.om.res = res;

@@ -72,6 +72,8 @@ struct IgArgs {
     int out_i8;          // 1: int8 output, requantised with mult[co]
     const float *mult;   // int8: requantisation multipliers M[co]
     int out_bufs;        // normal mode: output staging buffers per epilogue group (1 or 2)
+    int wres;            // 1: the layer's whole weight tensor (one N block) is loaded once per
+                         //    CTA and stays in shared memory; the ring then holds activations only
     OutMap om;           // output placement (concat slice, 2x upsample) and residual
     int *status;
 };
@@ -359,15 +361,17 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms need 1024-byte alignment
     uint8_t *gbase = smem_raw + (base - raw);
     const int stages = a.stages;
+    const bool wres = !PAIR && a.wres;  // resident weights: one B slot per K block
     const uint32_t sA = base;
     const uint32_t sB = base + stages * kAStage;
-    const uint32_t sOut = sB + stages * kBStage;  // per epilogue group: 128 rows x 64 B output staging
+    const uint32_t sOut = sB + (wres ? a.kblocks : stages) * kBStage;  // then 128 rows x 64 B per group
     const uint32_t sBar = sOut + kGroups * a.out_bufs * kOutStage;
     auto full_bar = [&](int s) { return sBar + 8u * s; };
     auto empty_bar = [&](int s) { return sBar + 8u * (stages + s); };
     auto tfull_bar = [&](int b) { return sBar + 8u * (2 * stages + b); };
     auto tempty_bar = [&](int b) { return sBar + 8u * (2 * stages + 2 + b); };
-    uint8_t *gmisc = gbase + (sBar - base) + 8u * (2 * stages + 4);
+    const uint32_t wres_bar = sBar + 8u * (2 * stages + 4);  // the resident weights have landed
+    uint8_t *gmisc = gbase + (sBar - base) + 8u * (2 * stages + 5);
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(gmisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gmisc + 4);
 
@@ -387,6 +391,7 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             tc::mbar_init(tfull_bar(b), 1);
             tc::mbar_init(tempty_bar(b), PAIR ? 2 * 4 * kGroups : 128 * kGroups);  // pair: one per warp
         }
+        tc::mbar_init(wres_bar, 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
         tc::tma_prefetch_desc(&tmA);
@@ -418,6 +423,18 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             bool ok = true;
             // pair mode: both CTAs' loads complete on the even CTA's barriers
             const uint32_t full0 = PAIR ? tc::mapa_shared(full_bar(0), 0) : full_bar(0);
+            if (wres && a.num_tiles > (int)blockIdx.x) {
+                // every K block of the (single) N block of weights, once
+                tc::mbar_arrive_expect_tx(wres_bar, (uint32_t)a.kblocks * kBStage);
+                int r = 0, s = 0, cb = 0;
+                for (int kb = 0; kb < a.kblocks; ++kb) {
+                    tc::tma_load_2d(sB + kb * kBStage, &tmB, wres_bar, (r * a.KW + s) * a.Cin + cb * BK, 0);
+                    if (++cb == a.cblocks) {
+                        cb = 0;
+                        if (++s == a.KW) { s = 0; ++r; }
+                    }
+                }
+            }
             for (int tile = unit; tile < a.num_tiles && ok; tile += units) {
                 const int nb = tile % a.tiles_n;
                 // pair mode: this CTA's pixel tile (past tiles_m: an empty
@@ -454,13 +471,13 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                                  oh0 * a.stride - a.pad_h + r, n);
                         tc::tma_load_2d_pair(dB, &tmB, fb, kx, nb * BN + (int)rank * kBRows);
                     } else {
-                        tc::mbar_arrive_expect_tx(full_bar(stage), a.a_bytes + kBStage);
+                        tc::mbar_arrive_expect_tx(full_bar(stage), a.a_bytes + (wres ? 0u : kBStage));
                         if (FLAT)
                             tc::tma_load_2d(dA, &tmA, full_bar(stage), cb * BK, m0);
                         else
                             tc::tma_load_4d(dA, &tmA, full_bar(stage), cb * BK,
                                             ow0 * a.stride - a.pad_w + s, oh0 * a.stride - a.pad_h + r, n);
-                        tc::tma_load_2d(dB, &tmB, full_bar(stage), kx, nb * BN);
+                        if (!wres) tc::tma_load_2d(dB, &tmB, full_bar(stage), kx, nb * BN);
                     }
                     if (++stage == stages) { stage = 0; phase ^= 1u; }
                     if (++cb == a.cblocks) {
@@ -477,6 +494,10 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             uint32_t phase = 0;
             bool ok = true;
             int lt = 0;
+            if (wres && a.num_tiles > (int)blockIdx.x) {  // the resident weights are in shared memory
+                ok = wait_bounded(wres_bar, 0u, abort_flag, a.status, KSTATUS_TIMEOUT_MMA);
+                tc::fence_after_sync();
+            }
             for (int tile = unit; tile < a.num_tiles && ok; tile += units, ++lt) {
                 const int buf = lt & 1;
                 const uint32_t use = (uint32_t)(lt >> 1);
@@ -492,7 +513,7 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     }
                     tc::fence_after_sync();
                     const uint32_t aS = sA + stage * kAStage;
-                    const uint32_t bS = sB + stage * kBStage;
+                    const uint32_t bS = sB + (wres ? kb : stage) * kBStage;
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
                         const uint64_t pd = tc::smem_desc_kmajor(aS + 32u * k, kRowBytes);  // pixels
