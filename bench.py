@@ -180,27 +180,35 @@ def run_ours(args, rank, world, device):
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
     nl = len(layers)
 
-    def step(ev=None):
+    def step():
         st = torch.cuda.current_stream(dev)  # the capture stream while capturing
         for i in range(nl):
-            if ev is not None:
-                ev[i].record(st)
             plans[i].run(X[i], Wt[i], B[i], Y[i], st)
-        if ev is not None:
-            ev[nl].record(st)
 
-    # One step is captured as a CUDA graph (the five launches and a timing
-    # event before each), so replaying it enqueues the whole step at once and
-    # the GPU never waits on the host between layers.
+    def capture(fn, with_events=False):
+        """fn captured as a CUDA graph (optionally between two timing events,
+        external=True so each replay re-records them)."""
+        evs = None
+        if with_events:
+            evs = (torch.cuda.Event(enable_timing=True, external=True),
+                   torch.cuda.Event(enable_timing=True, external=True))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            st = torch.cuda.current_stream(dev)
+            if evs:
+                evs[0].record(st)
+            fn()
+            if evs:
+                evs[1].record(st)
+        return g, evs
+
+    # The step (the layers back to back, nothing between them: consecutive
+    # launches overlap through programmatic dependent launch) is captured as
+    # one CUDA graph and replayed, so the GPU never waits on the host.
     for _ in range(2):
         step()
     torch.cuda.synchronize()
-    # external=True: recorded inside the capture as event-record nodes, so
-    # each replay re-records them and they can be timed.
-    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(nl + 1)]
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        step(ev)
+    graph, _ = capture(step)
     torch.cuda.synchronize()
 
     clocks = ClockSampler(device)
@@ -213,28 +221,40 @@ def run_ours(args, rank, world, device):
         torch.distributed.barrier()
     torch.cuda.synchronize()
 
-    per_layer = np.zeros((args.steps, nl))
-    step_ms = np.zeros(args.steps)
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     clocks.mark("t_start")
     t0 = time.perf_counter()
     for k in range(args.steps):
-        flush.fill_(k & 0xFF)
+        flush.fill_(k & 0xFF)          # outside the events: L2 holds none of the step's inputs
+        e0[k].record(stream)
         graph.replay()
-        torch.cuda.synchronize()
-        for i in range(nl):
-            per_layer[k, i] = ev[i].elapsed_time(ev[i + 1])
-        step_ms[k] = ev[0].elapsed_time(ev[nl])
+        e1[k].record(stream)
+    torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     clocks.mark("t_end")
     clk = clocks.stop()
-    # warm-L2 figures (outside the timed region): replays back to back with
-    # no flush, so each layer's inputs are whatever L2 kept from the last replay
-    warm_rows = []
-    for k in range(20):
-        graph.replay()
-        torch.cuda.synchronize()
-        warm_rows.append([ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(nl)])
-    warm = np.median(np.array(warm_rows), axis=0)
+    step_ms = np.array([e0[k].elapsed_time(e1[k]) for k in range(args.steps)])
+
+    # Per-layer figures (outside the timed region): each layer alone as a
+    # graph between two events, cold (L2 flushed before each replay) and warm.
+    reps = min(args.steps, 50)
+    per_layer = np.zeros((reps, nl))
+    warm = np.zeros(nl)
+    for i in range(nl):
+        gi, (ea, eb) = capture(lambda i=i: plans[i].run(X[i], Wt[i], B[i], Y[i], torch.cuda.current_stream(dev)),
+                               with_events=True)
+        for r in range(reps):
+            flush.fill_(r & 0xFF)
+            gi.replay()
+            torch.cuda.synchronize()
+            per_layer[r, i] = ea.elapsed_time(eb)
+        ws = []
+        for r in range(20):
+            gi.replay()
+            torch.cuda.synchronize()
+            ws.append(ea.elapsed_time(eb) * 1e3)
+        warm[i] = float(np.median(ws))
     for p in plans:
         p.check_device_status()
     my_ms = float(step_ms.sum())
@@ -305,7 +325,8 @@ def run_ours(args, rank, world, device):
         "data": "synthetic",
         "config": {"workload": args.workload, "layers": len(layers),
                    "batch_per_gpu": layers[0].spec.n, "l2": "flushed before every step (outside the events)",
-                   "launch": "CUDA graph replay of the step (events inside the graph)",
+                   "launch": "CUDA graph replay of the step, events around each replay; per-layer figures "
+                             "from each layer's own graph",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roofline, "layers": layer_rows, "e2e": e2e,
         "peaks": {"bf16_tflops": peaks["bf16_tflops"], "hbm_gbs": peaks["hbm_gbs"],

@@ -96,6 +96,29 @@ int conv_check_run_pointers(conv_dtype_t dtype, const conv_shape_t *s, int group
     return CONV_OK;
 }
 
+cudaError_t conv_launch(const void *kernel, dim3 grid, dim3 block, void **args, size_t smem, cudaStream_t st,
+                        int cluster_x) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    int na = 1;
+    if (cluster_x > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)cluster_x;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        na = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelExC(&cfg, kernel, args);
+}
+
 int conv_grant_smem(const void *k, int device, int need) {
     int optin = 0;
     cudaFuncAttributes fa;

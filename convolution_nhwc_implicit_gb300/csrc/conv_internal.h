@@ -92,6 +92,15 @@ struct conv_plan {
 // Element size of a conv_dtype_t.
 static inline int conv_esize(conv_dtype_t t) { return t == CONV_F32 ? 4 : (t == CONV_BF16 ? 2 : 1); }
 
+// Every kernel of the library is launched with programmatic stream
+// serialisation: it may be scheduled while the previous kernel on the stream
+// drains, and waits (griddepcontrol.wait, pdl_wait) until that kernel has
+// completed and its writes are visible before its first global access, so
+// the launch latency and the kernel's set-up overlap the previous kernel's
+// tail.  cluster_x > 1 launches clusters of that many CTAs along x.
+cudaError_t conv_launch(const void *kernel, dim3 grid, dim3 block, void **args, size_t smem, cudaStream_t st,
+                        int cluster_x = 1);
+
 // Launchers (stream-ordered, no allocation, no synchronisation).
 cudaError_t launch_direct(const conv_plan *p, const void *x, const void *w, const void *bias,
                           const void *res, void *y, cudaStream_t st);

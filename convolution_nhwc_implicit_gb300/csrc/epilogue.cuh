@@ -91,6 +91,13 @@ __device__ __forceinline__ float activate(float v, int act) {
     return v;
 }
 
+// Programmatic dependent launch (see conv_launch): let the next kernel on
+// the stream be scheduled, and wait for the previous one to complete (with
+// its writes visible) before touching global memory.  Both are no-ops for a
+// kernel launched without the attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Where a layer's output goes and what is added to it (the conv_output_t
 // options): output pixel (n, oh, ow), channel co lands at element
 //   base(n, oh, ow) + rep(dy, dx) + co   for dy, dx in [0, up)

@@ -38,6 +38,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
 direct_conv_float(DirectArgs a, const T *__restrict__ x, const T *__restrict__ w,
                   const float *__restrict__ bias, T *__restrict__ y) {
+    pdl_trigger();  // see conv_launch
+    pdl_wait();
     const T *res = reinterpret_cast<const T *>(a.om.res);
     long long pix = (long long)blockIdx.x * kThreads + threadIdx.x;
     if (pix >= a.npix) return;
@@ -93,6 +95,8 @@ __global__ void __launch_bounds__(kThreads)
 direct_conv_i8(DirectArgs a, const int8_t *__restrict__ x, const int8_t *__restrict__ w,
                const int32_t *__restrict__ bias, const float *__restrict__ mult,
                int8_t *__restrict__ y) {
+    pdl_trigger();  // see conv_launch
+    pdl_wait();
     long long pix = (long long)blockIdx.x * kThreads + threadIdx.x;
     if (pix >= a.npix) return;
     const int g = blockIdx.y / a.chunks_per_group;
@@ -173,6 +177,8 @@ template <typename T, int CT, int PT>
 __global__ void __launch_bounds__(kDThreads)
 direct_conv_smem(DirectArgs a, int chunks_per_group, const T *__restrict__ x, const T *__restrict__ w,
                  const float *__restrict__ bias, T *__restrict__ y) {
+    pdl_trigger();  // see conv_launch
+    pdl_wait();
     extern __shared__ __align__(16) float wsm[];  // [K][CT]
     const int K = a.KH * a.KW * a.cin_g;
     const int g = blockIdx.y / chunks_per_group;
@@ -348,7 +354,7 @@ cudaError_t launch_smem(const conv_plan *p, DirectArgs a, const void *x, const v
               (unsigned)(p->groups * chunks));
     void *k = smem_kernel<T>(ct, pt);
     void *args[] = {&a, (void *)&chunks, (void *)&x, (void *)&w, (void *)&bias, &y};
-    return cudaLaunchKernel(k, grid, dim3(kDThreads), args, (size_t)K * ct * sizeof(float), st);
+    return conv_launch(k, grid, dim3(kDThreads), args, (size_t)K * ct * sizeof(float), st);
 }
 
 }  // namespace
@@ -390,26 +396,22 @@ cudaError_t launch_direct(const conv_plan *p, const void *x, const void *w, cons
     DirectArgs a = make_args(p);
     a.om.res = res;
     dim3 grid((unsigned)((a.npix + kThreads - 1) / kThreads), (unsigned)(p->groups * a.chunks_per_group));
+    const float *mult = p->d_mult;
     switch (p->dtype) {
-    case CONV_F32:
+    case CONV_F32: {
         if (p->dct > 0) return launch_smem<float>(p, a, x, w, bias, y, st);
-        direct_conv_float<float><<<grid, kThreads, 0, st>>>(
-            a, (const float *)x, (const float *)w, (const float *)bias, (float *)y);
-        break;
-    case CONV_BF16:
-        if (p->dct > 0) return launch_smem<__nv_bfloat16>(p, a, x, w, bias, y, st);
-        direct_conv_float<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
-            a, (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)w, (const float *)bias,
-            (__nv_bfloat16 *)y);
-        break;
-    case CONV_I8:
-        if (a.cin_g % 4 == 0)
-            direct_conv_i8<true><<<grid, kThreads, 0, st>>>(
-                a, (const int8_t *)x, (const int8_t *)w, (const int32_t *)bias, p->d_mult, (int8_t *)y);
-        else
-            direct_conv_i8<false><<<grid, kThreads, 0, st>>>(
-                a, (const int8_t *)x, (const int8_t *)w, (const int32_t *)bias, p->d_mult, (int8_t *)y);
-        break;
+        void *args[] = {&a, (void *)&x, (void *)&w, (void *)&bias, &y};
+        return conv_launch((const void *)&direct_conv_float<float>, grid, dim3(kThreads), args, 0, st);
     }
-    return cudaGetLastError();
+    case CONV_BF16: {
+        if (p->dct > 0) return launch_smem<__nv_bfloat16>(p, a, x, w, bias, y, st);
+        void *args[] = {&a, (void *)&x, (void *)&w, (void *)&bias, &y};
+        return conv_launch((const void *)&direct_conv_float<__nv_bfloat16>, grid, dim3(kThreads), args, 0, st);
+    }
+    default: {
+        void *args[] = {&a, (void *)&x, (void *)&w, (void *)&bias, (void *)&mult, &y};
+        const void *k = a.cin_g % 4 == 0 ? (const void *)&direct_conv_i8<true> : (const void *)&direct_conv_i8<false>;
+        return conv_launch(k, grid, dim3(kThreads), args, 0, st);
+    }
+    }
 }

@@ -147,6 +147,8 @@ __device__ __forceinline__ void issue_halo(const CUtensorMap *tm, const DwArgs &
 template <typename T, int S>
 __global__ void __launch_bounds__(256, 2)
 dw3x3_float_kernel(const __grid_constant__ CUtensorMap tmX, const T *__restrict__ w, const DwArgs a) {
+    pdl_trigger();  // see conv_launch
+    pdl_wait();
     using Tr = DwT<T>;
     using Vec = typename Tr::Vec;
     constexpr int VB = sizeof(Vec);
@@ -304,6 +306,8 @@ template <int CBV, int TW, int TH>
 __global__ void __launch_bounds__(CBV * TW / 2, (CBV * TW / 2) <= 128 ? 4 : 2)
 dw3x3_bf16_rows_kernel(const __grid_constant__ CUtensorMap tmX, const __nv_bfloat16 *__restrict__ w,
                        const DwArgs a) {
+    pdl_trigger();  // see conv_launch
+    pdl_wait();
     constexpr int kWin = TW + 2, kHin = TH + 2;
     constexpr uint32_t kPix = CBV * 8;  // bytes of one halo pixel: CBV vectors of 4 bf16
     constexpr uint32_t kHalo = kHin * kWin * kPix;
@@ -434,6 +438,8 @@ dw3x3_bf16_rows_kernel(const __grid_constant__ CUtensorMap tmX, const __nv_bfloa
 template <int S>
 __global__ void __launch_bounds__(256, 2)
 dw3x3_i8_kernel(const __grid_constant__ CUtensorMap tmX, const int8_t *__restrict__ w, const DwArgs a) {
+    pdl_trigger();  // see conv_launch
+    pdl_wait();
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t bars[2];
     const int stride = S ? S : a.stride;
@@ -734,5 +740,5 @@ cudaError_t launch_dw3x3(const conv_plan *p, const void *x, const void *w, const
     a.status = p->d_status;
     void *k = g.kind == 1 ? select_rows(g.cbv, g.tw, g.th) : select(p->dtype, p->stride);
     void *args[] = {&tm, &w, &a};
-    return cudaLaunchKernel(k, dim3((unsigned)g.blocks), dim3(g.threads), args, (size_t)g.smem, st);
+    return conv_launch(k, dim3((unsigned)g.blocks), dim3(g.threads), args, (size_t)g.smem, st);
 }

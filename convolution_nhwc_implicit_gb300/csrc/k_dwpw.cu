@@ -54,6 +54,8 @@ __global__ void __launch_bounds__(kThreads) dwpw_kernel(const T *__restrict__ x,
                                                         const float *__restrict__ bdw, const T *__restrict__ wpw,
                                                         const float *__restrict__ bpw, T *__restrict__ y,
                                                         const DwpwArgs a) {
+    pdl_trigger();  // see conv_launch
+    pdl_wait();
     extern __shared__ __align__(16) float sm[];
     float *xs = sm;                                   // [hin][win][C]
     float *zs = xs + a.hin * a.win * a.C;             // [th*tw][zp]
@@ -187,13 +189,7 @@ cudaError_t launch_dwpw(const conv_plan *p, const void *x, const void *wdw, cons
     a.tiles_w = g.tiles_w; a.tiles_h = g.tiles_h; a.zp = p->s.c_in + 1;
     a.act_dw = (int)p->act; a.act_pw = (int)p->act2;
     dim3 grid((unsigned)((long long)g.tiles_w * g.tiles_h * p->s.n), (unsigned)g.chunks);
-    if (p->dtype == CONV_F32)
-        dwpw_kernel<float><<<grid, kThreads, (size_t)g.smem, st>>>(
-            (const float *)x, (const float *)wdw, (const float *)bdw, (const float *)wpw, (const float *)bpw,
-            (float *)y, a);
-    else
-        dwpw_kernel<__nv_bfloat16><<<grid, kThreads, (size_t)g.smem, st>>>(
-            (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)wdw, (const float *)bdw, (const __nv_bfloat16 *)wpw,
-            (const float *)bpw, (__nv_bfloat16 *)y, a);
-    return cudaGetLastError();
+    void *args[] = {(void *)&x, (void *)&wdw, (void *)&bdw, (void *)&wpw, (void *)&bpw, &y, &a};
+    const void *k = p->dtype == CONV_F32 ? (const void *)&dwpw_kernel<float> : (const void *)&dwpw_kernel<__nv_bfloat16>;
+    return conv_launch(k, grid, dim3(kThreads), args, (size_t)g.smem, st);
 }

@@ -400,21 +400,7 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
 
     void *k = select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0, g.pair != 0, igemm_fused(p));
     void *args[] = {&tmA, &tmB, &tmY, &a};
-    cudaError_t e;
-    if (g.pair) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(g.grid);
-        cfg.blockDim = dim3(cta_threads(g.bn, false));
-        cfg.dynamicSmemBytes = (size_t)g.smem;
-        cfg.stream = st;
-        cudaLaunchAttribute attr;
-        attr.id = cudaLaunchAttributeClusterDimension;
-        attr.val.clusterDim.x = 2; attr.val.clusterDim.y = 1; attr.val.clusterDim.z = 1;
-        cfg.attrs = &attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelExC(&cfg, k, args);
-    } else {
-        e = cudaLaunchKernel(k, dim3(g.grid), dim3(cta_threads(g.bn, g.swap != 0)), args, (size_t)g.smem, st);
-    }
+    const cudaError_t e = conv_launch(k, dim3(g.grid), dim3(cta_threads(g.bn, g.swap != 0)), args, (size_t)g.smem, st,
+                                      g.pair ? 2 : 1);
     return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }

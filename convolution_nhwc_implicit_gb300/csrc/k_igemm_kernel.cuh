@@ -414,6 +414,10 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     if constexpr (PAIR) tc::cluster_sync();  // the peer's barriers are initialised
     tc::fence_after_sync();
     const uint32_t tmem_base = *tmem_holder;
+    // set-up done: let the next kernel be scheduled, and wait for the
+    // previous one's writes before the first global access
+    pdl_trigger();
+    pdl_wait();
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer

@@ -19,6 +19,7 @@
 #include <stdint.h>
 
 #include "conv_internal.h"
+#include "epilogue.cuh"
 
 namespace {
 
@@ -104,6 +105,8 @@ __device__ __forceinline__ void prep_one(const PrepJob &j, Idx i) {
 // Both operands in one launch: threads [0, nx) prepare x, the rest w.
 template <typename Tin, typename Idx>
 __global__ void __launch_bounds__(kThreads) prep_kernel(const PrepJob jx, const PrepJob jw, Idx nx, Idx nw) {
+    convk::pdl_trigger();
+    convk::pdl_wait();
     const Idx i = (Idx)blockIdx.x * kThreads + threadIdx.x;
     if (i < nx)
         prep_one<Tin, Idx>(jx, i);
@@ -117,11 +120,15 @@ cudaError_t prep(const PrepJob &jx, const PrepJob &jw, cudaStream_t st) {
     const long long n = nx + nw;
     if (n == 0) return cudaSuccess;
     const unsigned blocks = (unsigned)((n + kThreads - 1) / kThreads);
-    if (n + kThreads < (1ll << 32))
-        prep_kernel<Tin, uint32_t><<<blocks, kThreads, 0, st>>>(jx, jw, (uint32_t)nx, (uint32_t)nw);
-    else
-        prep_kernel<Tin, uint64_t><<<blocks, kThreads, 0, st>>>(jx, jw, (uint64_t)nx, (uint64_t)nw);
-    return cudaGetLastError();
+    PrepJob a = jx, b = jw;
+    if (n + kThreads < (1ll << 32)) {
+        uint32_t ux = (uint32_t)nx, uw = (uint32_t)nw;
+        void *args[] = {&a, &b, &ux, &uw};
+        return conv_launch((const void *)&prep_kernel<Tin, uint32_t>, dim3(blocks), dim3(kThreads), args, 0, st);
+    }
+    uint64_t ux = (uint64_t)nx, uw = (uint64_t)nw;
+    void *args[] = {&a, &b, &ux, &uw};
+    return conv_launch((const void *)&prep_kernel<Tin, uint64_t>, dim3(blocks), dim3(kThreads), args, 0, st);
 }
 
 }  // namespace

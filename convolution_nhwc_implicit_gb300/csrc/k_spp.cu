@@ -17,6 +17,9 @@
 #include <stdint.h>
 
 #include "conv_internal.h"
+#include "epilogue.cuh"
+
+using namespace convk;
 
 namespace {
 
@@ -99,6 +102,8 @@ __device__ __forceinline__ void store_tile(const uint4 *buf, int org, uint4 *y, 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) spp_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ y,
                                                        const SppArgs a) {
+    pdl_trigger();  // see conv_launch
+    pdl_wait();
     extern __shared__ __align__(16) uint4 sm[];
     uint4 *A = sm;
     uint4 *B = sm + kR * kP * a.cbv;
@@ -195,7 +200,7 @@ extern "C" int conv_spp_run(int32_t n, int32_t h, int32_t w, int32_t c, conv_dty
     const uint4 *xv = static_cast<const uint4 *>(x);
     uint4 *yv = static_cast<uint4 *>(y);
     void *args[] = {(void *)&xv, (void *)&yv, (void *)&a};
-    const cudaError_t e = cudaLaunchKernel(k, dim3((unsigned)tiles, (unsigned)cblocks), dim3(kThreads), args, smem,
-                                           (cudaStream_t)stream);
+    const cudaError_t e = conv_launch(k, dim3((unsigned)tiles, (unsigned)cblocks), dim3(kThreads), args, smem,
+                                      (cudaStream_t)stream);
     return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
