@@ -176,6 +176,17 @@ def run_ours(args, rank, world, device):
         B.append(None if d.b is None else d.b.to(dev))
         Y.append(torch.empty(p.output_shape, dtype=d.x.dtype, device=dev))
     stream = torch.cuda.current_stream(dev)
+    if args.profile_pass:
+        # For a profiler's launch list: `warmup` eager passes over the layers,
+        # then one more, each layer's launches in order, no graphs, no timing.
+        for _ in range(args.warmup + 1):
+            for i in range(len(layers)):
+                plans[i].run(X[i], Wt[i], B[i], Y[i], stream)
+        torch.cuda.synchronize()
+        return {"profile_pass": args.workload, "passes": args.warmup + 1,
+                "launches_per_pass": sum(p.launches for p in plans),
+                "layers": [{"layer": d.spec.name, "kernel": p.describe(), "launches": p.launches}
+                           for d, p in zip(layers, plans)]}
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20)
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
     nl = len(layers)
@@ -287,7 +298,7 @@ def run_ours(args, rank, world, device):
         })
     dom = max(range(nl), key=lambda i: per_layer[:, i].mean())
     dr = layer_rows[dom]
-    traffic = _traffic_for(layers[dom].spec.name, plans[dom].describe())
+    traffic = _traffic_for(args.workload, layers[dom].spec.name, plans[dom].describe())
     roofline = {"bound": dr["bound"], "achieved": dr["achieved"], "peak": dr["peak"], "unit": dr["unit"],
                 "frac": dr["frac"], "traffic": traffic, "kernel": layers[dom].spec.name,
                 "peak_source": {"tensor": f"{peaks_src} (bf16 burst)", "hbm": f"{peaks_src} (HBM copy)",
@@ -494,6 +505,7 @@ def run_e2e(args, layers, plans, dev, stream, total_flops, world):
 # the DRAM traffic captured for that family).
 _FAMILY_SOURCES = {
     "igemm": ["k_igemm.cu", "k_igemm_kernel.cuh", "k_prep.cu", "tc_ptx.cuh", "epilogue.cuh", "conv_internal.h"],
+    "dw3x3+pw1x1": ["k_dwpw.cu", "epilogue.cuh", "conv_internal.h"],
     "dw3x3": ["k_dw3x3.cu", "tc_ptx.cuh", "epilogue.cuh", "conv_internal.h"],
     "direct": ["k_direct.cu", "epilogue.cuh", "conv_internal.h"],
 }
@@ -512,7 +524,7 @@ def kernel_sources_sha1(kernel_desc):
     return h.hexdigest()
 
 
-def _traffic_for(layer_name, kernel_desc):
+def _traffic_for(workload, layer_name, kernel_desc):
     """DRAM bytes per launch of this kernel from the committed ncu summary
     (profiles/dram_traffic.json), if it was captured for this exact kernel
     configuration and its sources have not changed since; else None."""
@@ -521,7 +533,7 @@ def _traffic_for(layer_name, kernel_desc):
         return None
     with open(p) as f:
         d = json.load(f)
-    e = d.get(layer_name)
+    e = d.get(workload, {}).get(layer_name)
     if not e or e.get("kernel") != kernel_desc or e.get("sources_sha1") != kernel_sources_sha1(kernel_desc):
         return None
     return e.get("bytes_per_launch")
@@ -620,6 +632,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next-rows", action="store_true", help="skip timing the residual / concat / SPP rows")
+    ap.add_argument("--profile-pass", action="store_true",
+                    help="run the layers eagerly (warmup + 1 passes, in order) for a profiler and print their "
+                         "plans; no timing")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -639,7 +654,7 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     out = run_ours(args, rank, world, local)
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not args.profile_pass:
         from conv_workloads import generate
         out["cpu_baseline"] = cpu_baseline(generate(args.workload))
     if rank == 0:
