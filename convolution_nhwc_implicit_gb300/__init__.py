@@ -32,6 +32,14 @@ ACTS = {"none": 0, "relu": 1, "mish": 2}
 ALGOS = {"auto": 0, "direct": 1, "depthwise": 2, "igemm": 3, "igemm_swapped": 4, "igemm_n256": 5,
          "igemm_n128": 6, "igemm_n64": 7, "igemm_pair": 8, "dwpw": 9, "igemm_pair128": 10}
 ALGO_NAMES = {v: k for k, v in ALGOS.items()}
+# Staging flags of the tensor-core family (CONV_ALGO_STAGE_*), written as a
+# suffix of the algo name: "igemm+halo", "igemm_n64+taps".
+STAGING = {"taps": 0x100, "halo": 0x200}
+
+
+def _algo_code(algo: str) -> int:
+    name, _, stage = algo.partition("+")
+    return ALGOS[name] | (STAGING[stage] if stage else 0)
 
 
 class ConvError(RuntimeError):
@@ -172,7 +180,7 @@ class Plan:
             op = ctypes.pointer(_Output(int(o["y_channels"]), int(o["y_channel_offset"]), int(o["upsample"]),
                                         int(bool(o["residual"]))))
         rc = lib.conv_plan_create_fused(ctypes.byref(shape), stride, pad_h, pad_w, groups, DTYPES[dtype],
-                                        ACTS[act], qp, op, ALGOS[algo], ctypes.byref(self._handle))
+                                        ACTS[act], qp, op, _algo_code(algo), ctypes.byref(self._handle))
         if rc != 0:
             raise ConvError("conv_plan_create", rc)
         oh, ow = ctypes.c_int(), ctypes.c_int()

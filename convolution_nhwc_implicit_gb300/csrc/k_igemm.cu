@@ -32,58 +32,33 @@ CUtensorMapSwizzle swizzle_for(int bk) {
     return bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : (bk == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
 }
 
-template <int BN, int BK, bool FLAT, bool SWAP, bool PAIR = false>
-void *kernel_ptr() {
-    return reinterpret_cast<void *>(&igemm_bf16_kernel<BN, BK, FLAT, SWAP, PAIR, false>);
+// The plain (no output options) variant for the tile mode: flat, spatial with
+// per-tap boxes, or spatial with halo staging.
+template <int BN, int BK, bool SWAP, bool PAIR>
+void *kernel_ptr(bool flat, bool halo) {
+    if (flat) return reinterpret_cast<void *>(&igemm_bf16_kernel<BN, BK, true, SWAP, PAIR, false, false>);
+    if (halo) return reinterpret_cast<void *>(&igemm_bf16_kernel<BN, BK, false, SWAP, PAIR, false, true>);
+    return reinterpret_cast<void *>(&igemm_bf16_kernel<BN, BK, false, SWAP, PAIR, false, false>);
 }
 
-template <int BN, int BK>
-void *kernel_ptr_flat(bool flat) {
-    return flat ? kernel_ptr<BN, BK, true, false>() : kernel_ptr<BN, BK, false, false>();
-}
-
-template <int BN>
-void *kernel_ptr_bk(int bk, bool flat) {
+template <int BN, bool SWAP, bool PAIR>
+void *kernel_ptr_bk(int bk, bool flat, bool halo) {
     switch (bk) {
-    case 64: return kernel_ptr_flat<BN, 64>(flat);
-    case 32: return kernel_ptr_flat<BN, 32>(flat);
-    default: return kernel_ptr_flat<BN, 16>(flat);
+    case 64: return kernel_ptr<BN, 64, SWAP, PAIR>(flat, halo);
+    case 32: return kernel_ptr<BN, 32, SWAP, PAIR>(flat, halo);
+    default: return kernel_ptr<BN, 16, SWAP, PAIR>(flat, halo);
     }
 }
 
-template <int BK>
-void *kernel_ptr_swap(bool flat) {
-    return flat ? kernel_ptr<128, BK, true, true>() : kernel_ptr<128, BK, false, true>();
-}
-
-template <int BN, int BK>
-void *kernel_ptr_pair(bool flat) {
-    return flat ? kernel_ptr<BN, BK, true, false, true>() : kernel_ptr<BN, BK, false, false, true>();
-}
-
-template <int BN>
-void *kernel_ptr_pair_bk(int bk, bool flat) {
-    switch (bk) {
-    case 64: return kernel_ptr_pair<BN, 64>(flat);
-    case 32: return kernel_ptr_pair<BN, 32>(flat);
-    default: return kernel_ptr_pair<BN, 16>(flat);
-    }
-}
-
-void *select_kernel(int bn, int bk, bool flat, bool swap, bool pair, bool fused) {
-    if (fused) return igemm_select_fused(bn, bk, flat, swap, pair);
-    if (pair) return bn == 128 ? kernel_ptr_pair_bk<128>(bk, flat) : kernel_ptr_pair_bk<256>(bk, flat);
-    if (swap) {
-        switch (bk) {
-        case 64: return kernel_ptr_swap<64>(flat);
-        case 32: return kernel_ptr_swap<32>(flat);
-        default: return kernel_ptr_swap<16>(flat);
-        }
-    }
+void *select_kernel(int bn, int bk, bool flat, bool swap, bool pair, bool fused, bool halo) {
+    if (fused) return igemm_select_fused(bn, bk, flat, swap, pair, halo);
+    if (pair) return bn == 128 ? kernel_ptr_bk<128, false, true>(bk, flat, halo)
+                               : kernel_ptr_bk<256, false, true>(bk, flat, halo);
+    if (swap) return kernel_ptr_bk<128, true, false>(bk, flat, halo);
     switch (bn) {
-    case 256: return kernel_ptr_bk<256>(bk, flat);
-    case 128: return kernel_ptr_bk<128>(bk, flat);
-    default: return kernel_ptr_bk<64>(bk, flat);
+    case 256: return kernel_ptr_bk<256, false, false>(bk, flat, halo);
+    case 128: return kernel_ptr_bk<128, false, false>(bk, flat, halo);
+    default: return kernel_ptr_bk<64, false, false>(bk, flat, halo);
     }
 }
 
@@ -129,7 +104,7 @@ bool igemm_supported(const conv_plan *p) {
     return true;
 }
 
-int igemm_configure(conv_plan *p, int layout) {
+int igemm_configure(conv_plan *p, int layout, int staging) {
     IgemmGeom &g = p->ig;
     const int S = p->stride;
     g.in_i8 = 0;
@@ -142,8 +117,6 @@ int igemm_configure(conv_plan *p, int layout) {
     g.wx = g.fold ? p->s.w + 2 * p->pad_w - p->s.k_w + 1 : p->s.w;
     // (a flat tile's pixels have no (oh, ow) structure for the upsample replicas)
     g.flat = (p->s.k_h == 1 && g.kw == 1 && S == 1 && p->pad_h == 0 && g.padw == 0 && p->up == 1) ? 1 : 0;
-    g.bk = cin % 64 == 0 ? 64 : (cin % 32 == 0 ? 32 : 16);
-    g.cblocks = cin / g.bk;
     if (g.prep) {
         // plan-owned bf16 copies of x and w (channels padded to `cin`)
         const size_t xb = (size_t)p->s.n * p->s.h * g.wx * cin * 2;
@@ -152,25 +125,40 @@ int igemm_configure(conv_plan *p, int layout) {
         if (xb && cudaMalloc(&p->d_xprep, xb) != cudaSuccess) return CONV_ERR_OOM;
         if (cudaMalloc(&p->d_wprep, wb) != cudaSuccess) return CONV_ERR_OOM;
     }
-    g.kblocks = p->s.k_h * g.kw * g.cblocks;
 
-    // Candidate layouts: swapped (Cout <= 128) with 256-pixel tiles; normal
-    // with 128-pixel tiles and BN in {256, 128, 64}; the CTA pair with
-    // 2 x 128-pixel tiles and BN = 256.  Each is scored by an estimate of
-    // its time: waves x (per-tile cost + fixed cost), the per-tile cost
-    // (per SM) being the largest of
-    //   MMA issue   128 cycles per K=16 step whatever N is (so N = 256 is
-    //               the only full-rate width),
-    //   shared memory  the staged operand bytes are written once by TMA and
-    //               read once by the MMAs: 2 * (pixel rows + weight rows
-    //               staged) * K * 2 bytes at 128 B/cycle,
+    // Candidates: the tile layout (swapped, Cout <= 128, with 256-pixel
+    // tiles; normal with 128-pixel tiles and BN in {256, 128, 64}; the CTA
+    // pair with 2 x 128-pixel tiles and BN in {256, 128}) x the staging
+    // (per-tap boxes, or halo staging for stride-1 spatial layers with
+    // k_h = 3) x, in spatial mode, the tile's bh x bw shape.  The channel
+    // block BK is the largest of 64, 32, 16 dividing Cin (measured: smaller
+    // blocks never won, even where they let the weights stay resident)
+    // unless it leaves no room for two stages.
+    // Each candidate is scored by an estimate of its time, waves x (per-tile
+    // cost + a fixed cost), the per-tile cost (per SM) being the largest of
+    //   MMA issue   128 cycles per K = 16 step whatever N is (N = 256 is the
+    //               only full-rate width; measured),
+    //   TMA issue   ~2 cycles per staged operand row (a pixel's or an output
+    //               channel's BK channels), whatever its length,
+    //   ring latency  a freed stage is refilled ~2000 cycles later: with S
+    //               stages each stage's MMAs are spaced at least 2000 / (S - 1),
     //   epilogue    accumulator lanes x columns (wasted lanes included)
     //               x cycles per value / 128 lanes per cycle per SM,
     // with the epilogue costing ~16 cycles per value with Mish (two MUFU
     // operations), ~10 for an int8 requantisation and ~6 otherwise.
     const long long K = (long long)p->s.k_h * g.kw * cin;
     const long long epi_c = p->dtype == CONV_I8 ? 10 : (p->act == CONV_ACT_MISH ? 16 : 6);
-    long long best_cost = -1, best_tiles = 0;
+    const int smem_cap = 227 * 1024 - 1024 - 512;  // minus the alignment slack and the barriers
+    const bool halo_ok = !g.flat && S == 1 && p->s.k_h == 3;  // (the halo variants' tap count)
+    if (staging == 2 && !halo_ok) return CONV_ERR_UNSUPPORTED;
+    struct Cand {
+        int swap, pair, bn, bk, halo, bw, bh, tw, th, wres, stages, out_bufs;
+        long long tiles_m, tiles_n, units, rows;
+        uint32_t a_stage;
+    };
+    Cand best{};
+    long long best_cost = -1;
+    const int bk_max = cin % 64 == 0 ? 64 : (cin % 32 == 0 ? 32 : 16);
     for (int cand = 0; cand < 6; ++cand) {
         const bool swap = cand == 0;
         const bool pair = cand == 4 || cand == 5;
@@ -179,90 +167,140 @@ int igemm_configure(conv_plan *p, int layout) {
         if (layout != 0 && layout != cand + 1) continue;
         const int bn = swap ? 128 : (cand == 1 || cand == 4 ? 256 : (cand == 2 || cand == 5 ? 128 : 64));
         const int P = swap ? kBMSwap : kBM;
-        int bw = P, bh = 1, tw = 1, th = 1;
-        long long tiles_m;
-        if (g.flat) {
-            const long long M = (long long)p->s.n * p->s.h * g.wx;
-            tiles_m = (M + P - 1) / P;
-        } else {
-            // Smallest number of bh x bw rectangles covering the output; among
-            // equal counts, the widest (longest contiguous NHWC runs).
-            long long best = -1;
-            for (int cw = 1; cw <= P && cw <= p->ow * 2; ++cw) {
-                if (cw * S > 256) break;
-                int ch = P / cw;
-                if (ch > p->oh) ch = p->oh;
-                while (ch * S > 256) --ch;
-                if (ch < 1) continue;
-                const long long ctw = (p->ow + cw - 1) / cw, cth = (p->oh + ch - 1) / ch;
-                const long long t = ctw * cth * p->s.n;
-                if (best < 0 || t < best || (t == best && cw > bw)) {
-                    best = t; bw = cw; bh = ch; tw = (int)ctw; th = (int)cth;
+        const int bnc = swap ? 128 : (pair ? bn / 2 : bn);  // weight rows a CTA stages per K block
+        // (a smaller channel block only where the largest leaves no room for
+        // two ring stages of this layout and staging)
+        for (int bk = bk_max, fits = 0; bk >= 16 && !fits; bk /= 2) {
+            const long long cblocks = cin / bk;
+            const long long wblocks = (long long)p->s.k_h * g.kw * cblocks;
+            for (int halo = 0; halo <= (halo_ok ? 1 : 0); ++halo) {
+                if ((staging == 1 && halo) || (staging == 2 && !halo)) continue;
+                // tile shapes: flat (one); per-tap spatial (the fewest tiles,
+                // then the widest); halo (bw a multiple of 8, bh x bw <= P)
+                int shapes[40][2];
+                int nshapes = 0;
+                if (g.flat) {
+                    shapes[nshapes][0] = P; shapes[nshapes][1] = 1; ++nshapes;
+                } else if (!halo) {
+                    long long bt = -1;
+                    int bw = P, bh = 1;
+                    for (int cw = 1; cw <= P && cw <= p->ow * 2; ++cw) {
+                        if (cw * S > 256) break;
+                        int ch = P / cw;
+                        if (ch > p->oh) ch = p->oh;
+                        while (ch * S > 256) --ch;
+                        if (ch < 1) continue;
+                        const long long t = (long long)((p->ow + cw - 1) / cw) * ((p->oh + ch - 1) / ch) * p->s.n;
+                        if (bt < 0 || t < bt || (t == bt && cw > bw)) { bt = t; bw = cw; bh = ch; }
+                        if (cw >= p->ow) break;
+                    }
+                    shapes[nshapes][0] = bw; shapes[nshapes][1] = bh; ++nshapes;
+                } else {
+                    for (int cw = 8; cw <= P && cw <= 256 && nshapes < 40; cw += 8) {
+                        int ch = P / cw;
+                        if (ch > p->oh) ch = p->oh;
+                        if (ch + p->s.k_h - 1 > 256) continue;
+                        shapes[nshapes][0] = cw; shapes[nshapes][1] = ch; ++nshapes;
+                        if (cw >= p->ow) break;  // wider tiles only waste more columns
+                    }
                 }
-                if (cw >= p->ow) break;
+                for (int si = 0; si < nshapes; ++si) {
+                    Cand c{};
+                    c.swap = swap; c.pair = pair; c.bn = bn; c.bk = bk; c.halo = halo;
+                    c.bw = shapes[si][0]; c.bh = shapes[si][1];
+                    if (g.flat) {
+                        const long long M = (long long)p->s.n * p->s.h * g.wx;
+                        c.tiles_m = (M + P - 1) / P;
+                        c.tw = 1; c.th = 1;
+                    } else {
+                        c.tw = (p->ow + c.bw - 1) / c.bw;
+                        c.th = (p->oh + c.bh - 1) / c.bh;
+                        c.tiles_m = (long long)c.tw * c.th * p->s.n;
+                    }
+                    c.tiles_n = swap ? 1 : (p->s.c_out + bn - 1) / bn;
+                    c.units = (pair ? (c.tiles_m + 1) / 2 : c.tiles_m) * c.tiles_n;
+                    // Shared memory: ring stages, resident weights, epilogue
+                    // staging.  A halo stage holds the box's (bh + k_h - 1) x bw
+                    // pixel rows and, when bh x bw < P, the P - bh x bw rows the
+                    // last tap's MMAs read past them (stale, never stored).
+                    const int hrows = c.bh + p->s.k_h - 1;
+                    const int box_rows = halo ? hrows * c.bw : P;  // pixel rows TMA writes per stage
+                    const int read_rows = halo ? (p->s.k_h - 1) * c.bw + P : P;
+                    const int a_rows = box_rows > read_rows ? box_rows : read_rows;
+                    c.a_stage = (uint32_t)(((long long)a_rows * bk * 2 + 1023) / 1024 * 1024);
+                    const long long ring_kb = halo ? (long long)g.kw * cblocks : wblocks;  // stages per tile
+                    const long long wblock = (long long)bnc * bk * 2;
+                    const int one_buf = swap ? 4 * 16 * kTP : epi_groups(bn, false) * kBM * 64;
+                    c.out_bufs = 1;
+                    if (!swap && wblocks < 16 && (smem_cap - 2 * one_buf) / ((long long)c.a_stage + wblock) >= 4)
+                        c.out_bufs = 2;
+                    const long long out_bytes = (long long)one_buf * c.out_bufs;
+                    const long long wall = wblocks * wblock;
+                    const int min_stages = halo ? 3 : 4;
+                    c.wres = (c.tiles_n == 1 && (smem_cap - out_bytes - wall) / (long long)c.a_stage >= min_stages)
+                                 ? 1 : 0;
+                    const int taps = halo ? 3 : 1;  // weight blocks a stage carries
+                    const long long stage_bytes = c.a_stage + (c.wres ? 0 : taps * wblock);
+                    long long st = (smem_cap - out_bytes - (c.wres ? wall : 0)) / stage_bytes;
+                    if (st > 8) st = 8;
+                    if (st < 2) continue;
+                    c.stages = (int)st;
+                    fits = 1;
+                    // the estimate
+                    const long long slots = pair ? p->num_sms / 2 : p->num_sms;
+                    const long long waves = (c.units + slots - 1) / slots;
+                    const long long t_mma = K / 16 * 128;
+                    c.rows = ring_kb * box_rows + (c.wres ? 0 : wblocks * bnc);  // staged rows per tile
+                    const long long t_tma = 2 * c.rows;
+                    const long long t_epi = 128LL * (swap ? P : bn) * epi_c / 128;
+                    // a stage is refilled ~2000 cycles after its MMAs free it, which
+                    // the MMAs of the other stages must cover
+                    const long long m_stage = (long long)taps * (bk / 16) * 128;
+                    long long per_stage = 2000 / (c.stages - 1);
+                    if (per_stage < m_stage) per_stage = m_stage;
+                    const long long t_ring = ring_kb * per_stage;
+                    long long t_tile = t_mma > t_tma ? t_mma : t_tma;
+                    if (t_epi > t_tile) t_tile = t_epi;
+                    if (t_ring > t_tile) t_tile = t_ring;
+                    const long long cost = waves * (t_tile + 500);
+                    // ties: more work units (more SMs busy), then fewer staged
+                    // rows, then the narrower N tile
+                    const bool better =
+                        best_cost < 0 || cost < best_cost ||
+                        (cost == best_cost &&
+                         (c.units > best.units ||
+                          (c.units == best.units && (c.rows < best.rows || (c.rows == best.rows && bn < best.bn)))));
+                    if (better) {
+                        best_cost = cost;
+                        best = c;
+                    }
+                }
             }
-            tiles_m = best;
-        }
-        const long long tiles_n = swap ? 1 : (p->s.c_out + bn - 1) / bn;
-        // pair mode: a unit of work is a pair tile on two SMs
-        const long long tiles = (pair ? (tiles_m + 1) / 2 : tiles_m) * tiles_n;
-        const long long slots = pair ? p->num_sms / 2 : p->num_sms;
-        const long long waves = (tiles + slots - 1) / slots;
-        const long long t_mma = K / 16 * 128;
-        const long long t_smem = (P + (pair ? bn / 2 : bn)) * K / 32;
-        const long long t_epi = 128LL * (swap ? P : bn) * epi_c / 128;
-        long long t_tile = t_mma > t_smem ? t_mma : t_smem;
-        if (t_epi > t_tile) t_tile = t_epi;
-        const long long cost = waves * (t_tile + 500);
-        // ties: more tiles (more SMs busy), then the narrower N tile
-        if (best_cost < 0 || cost < best_cost || (cost == best_cost && tiles > best_tiles) ||
-            (cost == best_cost && tiles == best_tiles && bn < g.bn)) {
-            best_cost = cost;
-            best_tiles = tiles;
-            g.swap = swap ? 1 : 0; g.pair = pair ? 1 : 0; g.bn = bn; g.tiles_n = (int)tiles_n;
-            g.tiles_m = (int)tiles_m;
-            g.bw = bw; g.bh = bh; g.tiles_w = tw; g.tiles_h = th;
         }
     }
-    if (best_cost < 0) return CONV_ERR_UNSUPPORTED;  // forced swapped layout with c_out > 128
-    const int P = g.swap ? kBMSwap : kBM;  // pixels per tile (per CTA)
-    g.num_tiles = g.tiles_n * (g.pair ? (g.tiles_m + 1) / 2 : g.tiles_m);  // work units
-
-    int stage_bytes = (P + (g.pair ? g.bn / 2 : g.bn)) * g.bk * 2;
-    // Epilogue staging: swapped mode, 16 transpose rows per group; normal
-    // mode, 128 rows x 64 B per group and buffer.  Two buffers per group let
-    // a group fill one while the TMA store of the other is still reading it;
-    // they are used when the operand ring keeps at least 4 stages.
-    // Short-K layers (few K blocks per tile) are limited by the epilogue and
-    // take the second buffer; long-K layers keep the shared memory for
-    // operand stages.
-    const int one_buf = g.swap ? 4 * 16 * kTP : epi_groups(g.bn, false) * kBM * 64;
-    g.out_bufs = 1;
-    if (!g.swap && g.kblocks < 16 && (227 * 1024 - 1024 - 256 - 2 * one_buf) / stage_bytes >= 4) g.out_bufs = 2;
-    const int out_bytes = one_buf * g.out_bufs;
-    // Resident weights: a single N block whose K blocks all fit beside at
-    // least four activation stages is loaded once per CTA; the ring then
-    // moves activations only (fewer TMA rows per K block).
-    const int wblock = (g.swap ? 128 : g.bn) * g.bk * 2;  // one K block of weights
-    const int act_stage = P * g.bk * 2;
-    const long long wall = (long long)g.kblocks * wblock;
-    g.wres = 0;
-    if (!g.pair && g.tiles_n == 1 &&
-        (227LL * 1024 - 1024 - 512 - out_bytes - wall) / act_stage >= 4) {
-        g.wres = 1;
-        stage_bytes = act_stage;
+    if (best_cost < 0) return CONV_ERR_UNSUPPORTED;  // e.g. a forced swapped layout with c_out > 128
+    g.swap = best.swap; g.pair = best.pair; g.bn = best.bn; g.bk = best.bk; g.halo = best.halo;
+    g.cblocks = cin / g.bk;
+    const int wblocks = p->s.k_h * g.kw * g.cblocks;
+    g.tiles_n = (int)best.tiles_n; g.tiles_m = (int)best.tiles_m;
+    g.bw = best.bw; g.bh = best.bh; g.tiles_w = best.tw; g.tiles_h = best.th;
+    g.wres = best.wres; g.stages = best.stages; g.out_bufs = best.out_bufs;
+    g.a_stage = (int)best.a_stage;
+    g.kblocks = g.halo ? g.kw * g.cblocks : wblocks;
+    g.num_tiles = (int)best.units;  // work units
+    {
+        const int bnc = g.swap ? 128 : (g.pair ? g.bn / 2 : g.bn);
+        const int wblock = bnc * g.bk * 2;
+        const int one_buf = g.swap ? 4 * 16 * kTP : epi_groups(g.bn, false) * kBM * 64;
+        const int weights = g.wres ? wblocks * wblock : g.stages * (g.halo ? 3 : 1) * wblock;
+        g.smem = 1024 + g.stages * g.a_stage + weights + one_buf * g.out_bufs + 8 * (2 * g.stages + 5) + 16;
     }
-    const int budget = 227 * 1024 - 1024 - 512 - out_bytes - (g.wres ? (int)wall : 0);
-    g.stages = budget / stage_bytes;
-    if (g.stages > 8) g.stages = 8;
-    if (g.stages < 2) return CONV_ERR_UNSUPPORTED;
-    g.smem = 1024 + g.stages * stage_bytes + (g.wres ? (int)wall : 0) + out_bytes + 8 * (2 * g.stages + 5) + 16;
     // Ask for more than half of an SM's shared memory so that no two CTAs of
     // this persistent kernel share an SM: each CTA then owns its TMEM
     // columns (at most 512) without waiting for another to free them.
     if (g.smem < 116 * 1024) g.smem = 116 * 1024;
     if (!tensor_map_encoder()) return CONV_ERR_CUDA;
-    void *kern = select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0, g.pair != 0, igemm_fused(p));
+    void *kern = select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0, g.pair != 0, igemm_fused(p), g.halo != 0);
     const int rc = conv_grant_smem(kern, p->device, g.smem);
     if (rc != CONV_OK) return rc;
     if (g.pair) {
@@ -285,7 +323,7 @@ int igemm_configure(conv_plan *p, int layout) {
         g.grid = g.num_tiles < p->num_sms ? g.num_tiles : p->num_sms;
     }
     snprintf(p->desc, sizeof(p->desc),
-             "igemm_%s_tcgen05 %s%s %s BK=%d tile=%dx%d stages=%d%s out_bufs=%d tiles=%d grid=%d",
+             "igemm_%s_tcgen05 %s%s %s BK=%d tile=%dx%d%s stages=%d%s out_bufs=%d tiles=%d grid=%d",
              p->dtype == CONV_I8 ? (g.fold ? "i8-as-bf16-kwfold" : "i8-as-bf16")
                                  : (g.fold ? "bf16-cpad-kwfold" : (g.prep ? "bf16-cpad" : "bf16")),
              g.flat ? "flat" : "spatial",
@@ -293,7 +331,8 @@ int igemm_configure(conv_plan *p, int layout) {
              g.swap ? "M=128co N=256px"
                     : (g.pair ? (g.bn == 256 ? "M=256px N=256co" : "M=256px N=128co")
                               : (g.bn == 256 ? "M=128px N=256co" : (g.bn == 128 ? "M=128px N=128co" : "M=128px N=64co"))),
-             g.bk, g.bh, g.bw, g.stages, g.wres ? " resident-weights" : "", g.out_bufs, g.num_tiles, g.grid);
+             g.bk, g.bh, g.bw, g.halo ? " halo" : "", g.stages, g.wres ? " resident-weights" : "", g.out_bufs,
+             g.num_tiles, g.grid);
     return CONV_OK;
 }
 
@@ -324,7 +363,9 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
                                     (cuuint64_t)p->s.n};
         const cuuint64_t strides[3] = {(cuuint64_t)cin * 2, (cuuint64_t)g.wx * cin * 2,
                                        (cuuint64_t)p->s.h * g.wx * cin * 2};
-        const cuuint32_t box[4] = {(cuuint32_t)g.bk, (cuuint32_t)(g.bw * S), (cuuint32_t)(g.bh * S), 1};
+        // halo staging: the bh + k_h - 1 input rows under the tile (stride 1)
+        const cuuint32_t box_h = g.halo ? (cuuint32_t)(g.bh + p->s.k_h - 1) : (cuuint32_t)(g.bh * S);
+        const cuuint32_t box[4] = {(cuuint32_t)g.bk, (cuuint32_t)(g.bw * S), box_h, 1};
         const cuuint32_t estr[4] = {1, (cuuint32_t)S, (cuuint32_t)S, 1};
         rc = encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(x), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(g.bk), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -384,7 +425,11 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
     a.num_tiles = g.num_tiles; a.cblocks = g.cblocks; a.kblocks = g.kblocks; a.stages = g.stages;
     a.tiles_m = g.tiles_m;
     a.M = (long long)p->s.n * p->s.h * g.wx;
-    a.a_bytes = (uint32_t)((g.flat ? (g.swap ? kBMSwap : kBM) : g.bw * g.bh) * g.bk * 2);
+    a.a_bytes = (uint32_t)((g.flat ? (g.swap ? kBMSwap : kBM) : g.bw * (g.halo ? g.bh + p->s.k_h - 1 : g.bh)) *
+                           g.bk * 2);
+    a.a_stage = (uint32_t)g.a_stage;
+    a.halo = g.halo;
+    a.wblocks = p->s.k_h * g.kw * g.cblocks;
     a.flat = g.flat;
     a.act = (int)p->act;
     a.bias = bias;
@@ -398,7 +443,7 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
     a.om.res = res;
     a.status = p->d_status;
 
-    void *k = select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0, g.pair != 0, igemm_fused(p));
+    void *k = select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0, g.pair != 0, igemm_fused(p), g.halo != 0);
     void *args[] = {&tmA, &tmB, &tmY, &a};
     const cudaError_t e = conv_launch(k, dim3(g.grid), dim3(cta_threads(g.bn, g.swap != 0)), args, (size_t)g.smem, st,
                                       g.pair ? 2 : 1);

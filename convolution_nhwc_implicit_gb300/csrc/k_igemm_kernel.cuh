@@ -62,6 +62,10 @@ __host__ __device__ constexpr int cta_threads(int bn, bool swap) { return 64 + 1
 struct IgArgs {
     int H, W, Cin, Cout, KH, KW, stride, pad_h, pad_w, OH, OW;
     int bw, bh, tiles_w, tiles_h, tiles_n, num_tiles, cblocks, kblocks, stages;
+    int wblocks;         // weight K blocks of the layer: KH * KW * cblocks
+    int halo;            // 1: halo staging (see the kernel's comment); a ring stage is then
+                         //    the K block (s, cb), kblocks = KW * cblocks
+    uint32_t a_stage;    // bytes of one activation stage of the ring (a multiple of 1024)
     int tiles_m;         // pixel tiles (pair mode: each CTA of a pair takes one of two)
     long long M;         // flat mode: rows of x viewed as [N*H*W, Cin]
     int flat;
@@ -72,8 +76,9 @@ struct IgArgs {
     int out_i8;          // 1: int8 output, requantised with mult[co]
     const float *mult;   // int8: requantisation multipliers M[co]
     int out_bufs;        // normal mode: output staging buffers per epilogue group (1 or 2)
-    int wres;            // 1: the layer's whole weight tensor (one N block) is loaded once per
-                         //    CTA and stays in shared memory; the ring then holds activations only
+    int wres;            // 1: the layer's whole weight tensor (one N block; in pair mode this
+                         //    CTA's half of it) is loaded once per CTA and stays in shared
+                         //    memory; the ring then holds activations only
     OutMap om;           // output placement (concat slice, 2x upsample) and residual
     int *status;
 };
@@ -337,17 +342,34 @@ __device__ __forceinline__ void epilogue_swapped_bf16(const IgArgs &a, int tile,
 // epilogue warps arrive on the even CTA's accumulator-empty barrier.
 // FUSED: the layer has a residual or upsample replicas (conv_output_t); a
 // separate instantiation, so that plain layers run none of that code.
-template <int BN, int BK, bool FLAT, bool SWAP, bool PAIR, bool FUSED>
+//
+// HALO (stride-1 spatial 3 x k_w layers, tile width bw a multiple of 8):
+// taps (r, s) and (r + 1, s) read the same input pixels shifted by one
+// output row.  So an activation slot holds, for one column shift s and
+// channel block cb, the (bh + 2) x bw input pixels under the tile (one TMA
+// box at (cb * BK, ow0 - pad_w + s, oh0 - pad_h, n)), and the MMAs of the
+// three taps (r, s) read it from pixel row r * bw on.  An 8-row group of the
+// K-major swizzled operand is 8 consecutive pixels of one tile row, so every
+// tap's operand starts on a swizzle-atom boundary (r * bw rows) with the
+// usual 8-row group stride.  (When bh x bw is below the MMA's 128 or 256
+// pixel rows, the slot has room for the rows the last tap reads past the
+// box; they are stale and their outputs are never stored.)  Per tile this
+// stages k_w * (bh + 2) * bw pixel rows instead of 3 * k_w * bh * bw (480
+// instead of 1152 for a 3x3 layer and an 8 x 16 tile).  A stage carries the
+// box and, unless they are resident, the three taps' weight blocks: one
+// barrier wait per twelve MMAs (measured: splitting the weights into a ring
+// of their own, for a deeper ring, was slower).
+template <int BN, int BK, bool FLAT, bool SWAP, bool PAIR, bool FUSED, bool HALO = false>
 __global__ void __launch_bounds__(cta_threads(BN, SWAP), 1)
 igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ YMaps tmY, const IgArgs a) {
     static_assert(!(PAIR && SWAP), "the CTA-pair mode uses the normal layout");
+    static_assert(!(HALO && FLAT), "halo staging is for spatial tiles");
     constexpr int kPix = SWAP ? kBMSwap : kBM;  // pixel rows of a tile (per CTA)
     constexpr int kAcc = SWAP ? kBMSwap : BN;   // accumulator columns of a tile
     constexpr int kBRows = PAIR ? BN / 2 : BN;  // weight rows this CTA stages
     constexpr uint32_t kRowBytes = BK * 2;
-    constexpr uint32_t kAStage = kPix * BK * 2;  // activation (pixel) tile
-    constexpr uint32_t kBStage = kBRows * BK * 2;  // weight tile (this CTA's part)
+    constexpr uint32_t kBStage = kBRows * BK * 2;  // one weight K block (this CTA's part)
     constexpr uint32_t kTmemCols = 2 * kAcc;     // two accumulators
     constexpr uint32_t kIdesc = SWAP ? tc::idesc_bf16_f32(128, kBMSwap)
                                      : tc::idesc_bf16_f32(PAIR ? 2 * kBM : kBM, BN);
@@ -361,10 +383,16 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms need 1024-byte alignment
     uint8_t *gbase = smem_raw + (base - raw);
     const int stages = a.stages;
-    const bool wres = !PAIR && a.wres;  // resident weights: one B slot per K block
+    const bool wres = a.wres != 0;           // resident weights: one B slot per weight K block
+    constexpr int kHaloTaps = 3;             // halo staging: k_h (3) taps per activation slot
+    // activation (pixel) part of a stage; weight part (none if resident)
+    // Shared memory: the ring's activation (pixel) parts, then the weights
+    // (the ring's weight parts: one block per stage, three with halo staging;
+    // or the resident blocks), the epilogue staging and the barriers.
+    const uint32_t aStage = HALO ? a.a_stage : (uint32_t)(kPix * BK * 2);
     const uint32_t sA = base;
-    const uint32_t sB = base + stages * kAStage;
-    const uint32_t sOut = sB + (wres ? a.kblocks : stages) * kBStage;  // then 128 rows x 64 B per group
+    const uint32_t sB = base + stages * aStage;
+    const uint32_t sOut = sB + (wres ? (uint32_t)a.wblocks * kBStage : stages * (HALO ? kHaloTaps : 1) * kBStage);
     const uint32_t sBar = sOut + kGroups * a.out_bufs * kOutStage;
     auto full_bar = [&](int s) { return sBar + 8u * s; };
     auto empty_bar = [&](int s) { return sBar + 8u * (stages + s); };
@@ -427,12 +455,18 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             bool ok = true;
             // pair mode: both CTAs' loads complete on the even CTA's barriers
             const uint32_t full0 = PAIR ? tc::mapa_shared(full_bar(0), 0) : full_bar(0);
-            if (wres && a.num_tiles > (int)blockIdx.x) {
-                // every K block of the (single) N block of weights, once
-                tc::mbar_arrive_expect_tx(wres_bar, (uint32_t)a.kblocks * kBStage);
+            if (wres && unit < a.num_tiles) {
+                // every K block of the (single) N block of weights, once; pair
+                // mode: each CTA its half, both completing on the even CTA's barrier
+                const uint32_t wbar = PAIR ? tc::mapa_shared(wres_bar, 0) : wres_bar;
+                if (rank == 0) tc::mbar_arrive_expect_tx(wres_bar, (PAIR ? 2u : 1u) * (uint32_t)a.wblocks * kBStage);
                 int r = 0, s = 0, cb = 0;
-                for (int kb = 0; kb < a.kblocks; ++kb) {
-                    tc::tma_load_2d(sB + kb * kBStage, &tmB, wres_bar, (r * a.KW + s) * a.Cin + cb * BK, 0);
+                for (int kb = 0; kb < a.wblocks; ++kb) {
+                    const int kx = (r * a.KW + s) * a.Cin + cb * BK;
+                    if constexpr (PAIR)
+                        tc::tma_load_2d_pair(sB + kb * kBStage, &tmB, wbar, kx, (int)rank * kBRows);
+                    else
+                        tc::tma_load_2d(sB + kb * kBStage, &tmB, wres_bar, kx, 0);
                     if (++cb == a.cblocks) {
                         cb = 0;
                         if (++s == a.KW) { s = 0; ++r; }
@@ -455,6 +489,39 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     n = t2 / a.tiles_h;
                     ow0 = tw * a.bw;
                 }
+                if constexpr (HALO) {
+                    // K blocks (s, cb), cb fastest: a stage holds the halo box and
+                    // (unless resident) the weight blocks of taps r = 0 .. 2
+                    int s = 0, cb = 0;
+                    for (int kb = 0; kb < a.kblocks; ++kb) {
+                        if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, a.status,
+                                          KSTATUS_TIMEOUT_PRODUCER)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t dB = sB + stage * (kHaloTaps * kBStage);
+                        const uint32_t bytes = a.a_bytes + (wres ? 0u : kHaloTaps * kBStage);
+                        const uint32_t fb = PAIR ? full0 + 8u * stage : full_bar(stage);
+                        if (!PAIR || rank == 0) tc::mbar_arrive_expect_tx(full_bar(stage), (PAIR ? 2u : 1u) * bytes);
+                        const int c1 = ow0 - a.pad_w + s, c2 = oh0 - a.pad_h;
+                        if (PAIR) tc::tma_load_4d_pair(sA + stage * aStage, &tmA, fb, cb * BK, c1, c2, n);
+                        else tc::tma_load_4d(sA + stage * aStage, &tmA, fb, cb * BK, c1, c2, n);
+                        if (!wres) {
+#pragma unroll
+                            for (int t = 0; t < kHaloTaps; ++t) {
+                                const int kx = (t * a.KW + s) * a.Cin + cb * BK;
+                                if (PAIR)
+                                    tc::tma_load_2d_pair(dB + t * kBStage, &tmB, fb, kx, nb * BN + (int)rank * kBRows);
+                                else
+                                    tc::tma_load_2d(dB + t * kBStage, &tmB, fb, kx, nb * BN);
+                            }
+                        }
+                        if (++stage == stages) { stage = 0; phase ^= 1u; }
+                        if (++cb == a.cblocks) { cb = 0; ++s; }
+                    }
+                    continue;
+                }
+                // K block order: (r, s, cb), cb fastest
                 int r = 0, s = 0, cb = 0;
                 for (int kb = 0; kb < a.kblocks; ++kb) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, a.status,
@@ -462,26 +529,23 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         ok = false;
                         break;
                     }
-                    const uint32_t dA = sA + stage * kAStage;
+                    const uint32_t dA = sA + stage * aStage;
                     const uint32_t dB = sB + stage * kBStage;
-                    const int kx = (r * a.KW + s) * a.Cin + cb * BK;
-                    if constexpr (PAIR) {
-                        const uint32_t fb = full0 + 8u * stage;
-                        if (rank == 0) tc::mbar_arrive_expect_tx(full_bar(stage), 2u * (a.a_bytes + kBStage));
-                        if (FLAT)
-                            tc::tma_load_2d_pair(dA, &tmA, fb, cb * BK, m0);
-                        else
-                            tc::tma_load_4d_pair(dA, &tmA, fb, cb * BK, ow0 * a.stride - a.pad_w + s,
-                                                 oh0 * a.stride - a.pad_h + r, n);
-                        tc::tma_load_2d_pair(dB, &tmB, fb, kx, nb * BN + (int)rank * kBRows);
+                    const uint32_t bytes = a.a_bytes + (wres ? 0u : kBStage);
+                    const uint32_t fb = PAIR ? full0 + 8u * stage : full_bar(stage);
+                    if (!PAIR || rank == 0) tc::mbar_arrive_expect_tx(full_bar(stage), (PAIR ? 2u : 1u) * bytes);
+                    if (FLAT) {
+                        if (PAIR) tc::tma_load_2d_pair(dA, &tmA, fb, cb * BK, m0);
+                        else tc::tma_load_2d(dA, &tmA, fb, cb * BK, m0);
                     } else {
-                        tc::mbar_arrive_expect_tx(full_bar(stage), a.a_bytes + (wres ? 0u : kBStage));
-                        if (FLAT)
-                            tc::tma_load_2d(dA, &tmA, full_bar(stage), cb * BK, m0);
-                        else
-                            tc::tma_load_4d(dA, &tmA, full_bar(stage), cb * BK,
-                                            ow0 * a.stride - a.pad_w + s, oh0 * a.stride - a.pad_h + r, n);
-                        if (!wres) tc::tma_load_2d(dB, &tmB, full_bar(stage), kx, nb * BN);
+                        const int c1 = ow0 * a.stride - a.pad_w + s, c2 = oh0 * a.stride - a.pad_h + r;
+                        if (PAIR) tc::tma_load_4d_pair(dA, &tmA, fb, cb * BK, c1, c2, n);
+                        else tc::tma_load_4d(dA, &tmA, fb, cb * BK, c1, c2, n);
+                    }
+                    if (!wres) {
+                        const int kx = (r * a.KW + s) * a.Cin + cb * BK;
+                        if (PAIR) tc::tma_load_2d_pair(dB, &tmB, fb, kx, nb * BN + (int)rank * kBRows);
+                        else tc::tma_load_2d(dB, &tmB, fb, kx, nb * BN);
                     }
                     if (++stage == stages) { stage = 0; phase ^= 1u; }
                     if (++cb == a.cblocks) {
@@ -498,7 +562,7 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             uint32_t phase = 0;
             bool ok = true;
             int lt = 0;
-            if (wres && a.num_tiles > (int)blockIdx.x) {  // the resident weights are in shared memory
+            if (wres && unit < a.num_tiles) {  // the resident weights are in shared memory
                 ok = wait_bounded(wres_bar, 0u, abort_flag, a.status, KSTATUS_TIMEOUT_MMA);
                 tc::fence_after_sync();
             }
@@ -510,31 +574,76 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     break;
                 tc::fence_after_sync();
                 const uint32_t d = tmem_base + (uint32_t)(buf * kAcc);
-                for (int kb = 0; kb < a.kblocks; ++kb) {
-                    if (!wait_bounded(full_bar(stage), phase, abort_flag, a.status, KSTATUS_TIMEOUT_MMA)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::fence_after_sync();
-                    const uint32_t aS = sA + stage * kAStage;
-                    const uint32_t bS = sB + (wres ? kb : stage) * kBStage;
+                if constexpr (HALO) {
+                    // K blocks (s, cb): tap r reads the halo box from pixel row
+                    // r * bw; its weights are the stage's r-th block, or the
+                    // resident block (r * KW + s) * cblocks + cb.  The operand
+                    // descriptors are formed before the wait: the start address is a
+                    // descriptor's low field (address / 16, below 2^14), so the
+                    // operand at base + off has descriptor desc(base) + off / 16.
+                    int s = 0, cb = 0;
+                    const uint64_t p_tap = (uint64_t)(((uint32_t)a.bw * kRowBytes) >> 4);
+                    const uint64_t w_tap = wres ? (uint64_t)(a.KW * a.cblocks) * (kBStage >> 4) : (uint64_t)(kBStage >> 4);
+                    for (int kb = 0; kb < a.kblocks; ++kb) {
+                        const uint64_t pd0 = tc::smem_desc_kmajor(sA + stage * aStage, kRowBytes);  // pixels
+                        const uint64_t wd0 = tc::smem_desc_kmajor(                                 // weights
+                            wres ? sB + (uint32_t)(s * a.cblocks + cb) * kBStage : sB + stage * (kHaloTaps * kBStage),
+                            kRowBytes);
+                        if (!wait_bounded(full_bar(stage), phase, abort_flag, a.status, KSTATUS_TIMEOUT_MMA)) {
+                            ok = false;
+                            break;
+                        }
+                        tc::fence_after_sync();
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) {
-                        const uint64_t pd = tc::smem_desc_kmajor(aS + 32u * k, kRowBytes);  // pixels
-                        const uint64_t wd = tc::smem_desc_kmajor(bS + 32u * k, kRowBytes);  // weights
+                        for (int t = 0; t < kHaloTaps; ++t) {
+#pragma unroll
+                            for (int k = 0; k < BK / 16; ++k) {
+                                const uint64_t pd = pd0 + (uint64_t)t * p_tap + 2u * k;  // +32 bytes per K = 16 step
+                                const uint64_t wd = wd0 + (uint64_t)t * w_tap + 2u * k;
+                                const uint32_t accum = (kb | t | k) != 0 ? 1u : 0u;
+                                if (PAIR)
+                                    tc::mma_bf16_pair(d, pd, wd, kIdesc, accum);
+                                else if (SWAP)
+                                    tc::mma_bf16(d, wd, pd, kIdesc, accum);
+                                else
+                                    tc::mma_bf16(d, pd, wd, kIdesc, accum);
+                            }
+                        }
+                        if (++cb == a.cblocks) { cb = 0; ++s; }
+                        // stage free (in both CTAs of a pair) once these MMAs complete
                         if (PAIR)
-                            tc::mma_bf16_pair(d, pd, wd, kIdesc, (kb | k) != 0 ? 1u : 0u);
-                        else if (SWAP)
-                            tc::mma_bf16(d, wd, pd, kIdesc, (kb | k) != 0 ? 1u : 0u);
+                            tc::mma_commit_pair(empty_bar(stage), 0x3);
                         else
-                            tc::mma_bf16(d, pd, wd, kIdesc, (kb | k) != 0 ? 1u : 0u);
+                            tc::mma_commit(empty_bar(stage));
+                        if (++stage == stages) { stage = 0; phase ^= 1u; }
                     }
-                    // stage free (in both CTAs of a pair) once these MMAs complete
-                    if (PAIR)
-                        tc::mma_commit_pair(empty_bar(stage), 0x3);
-                    else
-                        tc::mma_commit(empty_bar(stage));
-                    if (++stage == stages) { stage = 0; phase ^= 1u; }
+                } else {
+                    for (int kb = 0; kb < a.kblocks; ++kb) {
+                        if (!wait_bounded(full_bar(stage), phase, abort_flag, a.status, KSTATUS_TIMEOUT_MMA)) {
+                            ok = false;
+                            break;
+                        }
+                        tc::fence_after_sync();
+                        const uint32_t aS = sA + stage * aStage;
+                        const uint32_t bS = sB + (wres ? kb : stage) * kBStage;
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k) {
+                            const uint64_t pd = tc::smem_desc_kmajor(aS + 32u * k, kRowBytes);  // pixels
+                            const uint64_t wd = tc::smem_desc_kmajor(bS + 32u * k, kRowBytes);  // weights
+                            if (PAIR)
+                                tc::mma_bf16_pair(d, pd, wd, kIdesc, (kb | k) != 0 ? 1u : 0u);
+                            else if (SWAP)
+                                tc::mma_bf16(d, wd, pd, kIdesc, (kb | k) != 0 ? 1u : 0u);
+                            else
+                                tc::mma_bf16(d, pd, wd, kIdesc, (kb | k) != 0 ? 1u : 0u);
+                        }
+                        // stage free (in both CTAs of a pair) once these MMAs complete
+                        if (PAIR)
+                            tc::mma_commit_pair(empty_bar(stage), 0x3);
+                        else
+                            tc::mma_commit(empty_bar(stage));
+                        if (++stage == stages) { stage = 0; phase ^= 1u; }
+                    }
                 }
                 if (ok) {  // accumulator ready
                     if (PAIR)

@@ -107,6 +107,17 @@ typedef enum {
     CONV_ALGO_IGEMM_PAIR128 = 10, /* CTA-pair MMA: M = 256 pixels, N = 128 output channels */
 } conv_algo_t;
 
+/* Staging of the tensor-core family's pixel operand, OR-ed into CONV_ALGO_IGEMM
+ * or one of its layouts (without either flag the plan's estimate chooses):
+ *   TAPS  one TMA box of input pixels per filter tap (r, s) and channel block;
+ *   HALO  one box per column shift s and channel block holding the input rows
+ *         under the tile for all three row taps, which the MMAs read at row
+ *         offsets (stride-1 layers with k_h = 3 only; CONV_ERR_UNSUPPORTED
+ *         otherwise).  Both compute the same sums ("nanoinfer", the implicit
+ *         GEMM: im2col is never materialised either way). */
+#define CONV_ALGO_STAGE_TAPS 0x100
+#define CONV_ALGO_STAGE_HALO 0x200
+
 enum {
     CONV_OK = 0,
     CONV_ERR_NULL_ARG = -1,        /* a required pointer is NULL            */

@@ -87,6 +87,10 @@ def _quant(scales, si=0.05, so=0.05):
     ((1, 8, 8, 4, 4, 3, 3), {"dtype": 7}, -9),             # bad dtype
     ((1, 8, 8, 4, 4, 3, 3), {"act": 5}, -9),               # bad activation
     ((1, 8, 8, 4, 4, 3, 3), {"algo": 9}, -9),              # bad algo
+    ((1, 8, 8, 4, 4, 3, 3), {"algo": 3 | 0x300}, -9),      # both staging flags
+    ((1, 8, 8, 4, 4, 3, 3), {"algo": 1 | 0x200}, -9),      # staging flag on the direct family
+    ((1, 8, 8, 4, 4, 3, 3), {"algo": 0x100}, -9),          # staging flag with AUTO
+    ((1, 8, 8, 4, 4, 3, 3), {"algo": 11 | 0x100}, -9),     # staging flag on a bad algo
     ((1, 8, 8, 4, 4, 3, 3), {"dtype": 2}, -1),             # int8 without quant
 ])
 def test_invalid_layers_are_named_failures(lib, shape, kw, expect):

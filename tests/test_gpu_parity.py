@@ -72,22 +72,40 @@ _LAYOUT_DESC = {"igemm_swapped": "swapped", "igemm_n256": "M=128px N=256co", "ig
                 "igemm_pair128": "cta-pair M=256px N=128co"}
 
 
+def halo_eligible(spec):
+    # halo staging: stride-1 layers with three filter rows
+    return spec.stride == 1 and spec.kh == 3
+
+
 def with_layouts(specs):
+    # Layers that can take halo staging run each layout with it and with
+    # per-tap boxes forced, as well as with the plan's own choice.
     out = []
     for spec in specs:
         for lay in ["igemm", "igemm_swapped", "igemm_n256", "igemm_n128", "igemm_n64", "igemm_pair",
                     "igemm_pair128"]:
             if lay == "igemm_swapped" and spec.cout > 128:
                 continue
-            out.append(pytest.param(spec, lay, id=f"{spec.name}-{lay}"))
+            for stage in (["", "+halo", "+taps"] if halo_eligible(spec) else [""]):
+                out.append(pytest.param(spec, lay + stage, id=f"{spec.name}-{lay}{stage}"))
     return out
 
 
 def check_layout(spec, layout):
     plan = check(spec, layout, "igemm")
-    if layout in _LAYOUT_DESC:
-        assert _LAYOUT_DESC[layout] in plan.describe(), plan.describe()
+    base, _, stage = layout.partition("+")
+    if base in _LAYOUT_DESC:
+        assert _LAYOUT_DESC[base] in plan.describe(), plan.describe()
+    if stage:
+        assert (" halo " in plan.describe()) == (stage == "halo"), plan.describe()
     return plan
+
+
+def test_halo_staging_needs_stride1_kh3():
+    for spec in (L("halo_s2", 1, 12, 12, 64, 64, 3, 3, 2, 1, 1), L("halo_5x5", 1, 12, 12, 64, 64, 5, 5, 1, 2, 2)):
+        d = make_layer(spec, torch.Generator("cpu").manual_seed(0))
+        with pytest.raises(RuntimeError, match="UNSUPPORTED"):
+            make_plan(spec, d, "igemm+halo")
 
 
 @pytest.mark.parametrize("spec,layout", with_layouts(IGEMM))
