@@ -32,14 +32,18 @@ ACTS = {"none": 0, "relu": 1, "mish": 2}
 ALGOS = {"auto": 0, "direct": 1, "depthwise": 2, "igemm": 3, "igemm_swapped": 4, "igemm_n256": 5,
          "igemm_n128": 6, "igemm_n64": 7, "igemm_pair": 8, "dwpw": 9, "igemm_pair128": 10}
 ALGO_NAMES = {v: k for k, v in ALGOS.items()}
-# Staging flags of the tensor-core family (CONV_ALGO_STAGE_*), written as a
-# suffix of the algo name: "igemm+halo", "igemm_n64+taps".
-STAGING = {"taps": 0x100, "halo": 0x200}
+# Staging and epilogue flags of the tensor-core family (CONV_ALGO_STAGE_*,
+# CONV_ALGO_EPI_*), written as suffixes of the algo name: "igemm+halo",
+# "igemm_n64+taps+ept".
+ALGO_FLAGS = {"taps": 0x100, "halo": 0x200, "sliced": 0x400, "ept": 0x800}
 
 
 def _algo_code(algo: str) -> int:
-    name, _, stage = algo.partition("+")
-    return ALGOS[name] | (STAGING[stage] if stage else 0)
+    name, *flags = algo.split("+")
+    code = ALGOS[name]
+    for f in flags:
+        code |= ALGO_FLAGS[f]
+    return code
 
 
 class ConvError(RuntimeError):

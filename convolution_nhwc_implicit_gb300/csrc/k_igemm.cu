@@ -50,8 +50,9 @@ void *kernel_ptr_bk(int bk, bool flat, bool halo) {
     }
 }
 
-void *select_kernel(int bn, int bk, bool flat, bool swap, bool pair, bool fused, bool halo) {
+void *select_kernel(int bn, int bk, bool flat, bool swap, bool pair, bool fused, bool halo, bool ept) {
     if (fused) return igemm_select_fused(bn, bk, flat, swap, pair, halo);
+    if (ept) return igemm_select_ept(bn, bk, flat, halo);
     if (pair) return bn == 128 ? kernel_ptr_bk<128, false, true>(bk, flat, halo)
                                : kernel_ptr_bk<256, false, true>(bk, flat, halo);
     if (swap) return kernel_ptr_bk<128, true, false>(bk, flat, halo);
@@ -104,7 +105,7 @@ bool igemm_supported(const conv_plan *p) {
     return true;
 }
 
-int igemm_configure(conv_plan *p, int layout, int staging) {
+int igemm_configure(conv_plan *p, int layout, int staging, int epi) {
     IgemmGeom &g = p->ig;
     const int S = p->stride;
     g.in_i8 = 0;
@@ -151,8 +152,9 @@ int igemm_configure(conv_plan *p, int layout, int staging) {
     const int smem_cap = 227 * 1024 - 1024 - 512;  // minus the alignment slack and the barriers
     const bool halo_ok = !g.flat && S == 1 && p->s.k_h == 3;  // (the halo variants' tap count)
     if (staging == 2 && !halo_ok) return CONV_ERR_UNSUPPORTED;
+    if (epi == 2 && igemm_fused(p)) return CONV_ERR_UNSUPPORTED;  // (no output options per tile)
     struct Cand {
-        int swap, pair, bn, bk, halo, bw, bh, tw, th, wres, stages, out_bufs;
+        int swap, pair, bn, bk, halo, ept, bw, bh, tw, th, wres, stages, out_bufs;
         long long tiles_m, tiles_n, units, rows;
         uint32_t a_stage;
     };
@@ -166,6 +168,8 @@ int igemm_configure(conv_plan *p, int layout, int staging) {
         if (pair && p->num_sms < 2) continue;
         if (layout != 0 && layout != cand + 1) continue;
         const int bn = swap ? 128 : (cand == 1 || cand == 4 ? 256 : (cand == 2 || cand == 5 ? 128 : 64));
+        const bool ept_ok = !swap && !pair && bn <= 128 && !igemm_fused(p);
+        if (epi == 2 && !ept_ok) continue;
         const int P = swap ? kBMSwap : kBM;
         const int bnc = swap ? 128 : (pair ? bn / 2 : bn);  // weight rows a CTA stages per K block
         // (a smaller channel block only where the largest leaves no room for
@@ -219,6 +223,10 @@ int igemm_configure(conv_plan *p, int layout, int staging) {
                     }
                     c.tiles_n = swap ? 1 : (p->s.c_out + bn - 1) / bn;
                     c.units = (pair ? (c.tiles_m + 1) / 2 : c.tiles_m) * c.tiles_n;
+                    // One epilogue per tile where each CTA gets at least two tiles
+                    // (with fewer, slicing every tile's columns over the warpgroups
+                    // finishes each tile sooner), or where forced.
+                    c.ept = ept_ok && epi != 1 && (epi == 2 || c.units >= 2LL * p->num_sms) ? 1 : 0;
                     // Shared memory: ring stages, resident weights, epilogue
                     // staging.  A halo stage holds the box's (bh + k_h - 1) x bw
                     // pixel rows and, when bh x bw < P, the P - bh x bw rows the
@@ -230,7 +238,7 @@ int igemm_configure(conv_plan *p, int layout, int staging) {
                     c.a_stage = (uint32_t)(((long long)a_rows * bk * 2 + 1023) / 1024 * 1024);
                     const long long ring_kb = halo ? (long long)g.kw * cblocks : wblocks;  // stages per tile
                     const long long wblock = (long long)bnc * bk * 2;
-                    const int one_buf = swap ? 4 * 16 * kTP : epi_groups(bn, false) * kBM * 64;
+                    const int one_buf = swap ? 4 * 16 * kTP : epi_groups(bn, false, c.ept != 0) * kBM * 64;
                     c.out_bufs = 1;
                     if (!swap && wblocks < 16 && (smem_cap - 2 * one_buf) / ((long long)c.a_stage + wblock) >= 4)
                         c.out_bufs = 2;
@@ -279,7 +287,7 @@ int igemm_configure(conv_plan *p, int layout, int staging) {
         }
     }
     if (best_cost < 0) return CONV_ERR_UNSUPPORTED;  // e.g. a forced swapped layout with c_out > 128
-    g.swap = best.swap; g.pair = best.pair; g.bn = best.bn; g.bk = best.bk; g.halo = best.halo;
+    g.swap = best.swap; g.pair = best.pair; g.bn = best.bn; g.bk = best.bk; g.halo = best.halo; g.ept = best.ept;
     g.cblocks = cin / g.bk;
     const int wblocks = p->s.k_h * g.kw * g.cblocks;
     g.tiles_n = (int)best.tiles_n; g.tiles_m = (int)best.tiles_m;
@@ -291,16 +299,16 @@ int igemm_configure(conv_plan *p, int layout, int staging) {
     {
         const int bnc = g.swap ? 128 : (g.pair ? g.bn / 2 : g.bn);
         const int wblock = bnc * g.bk * 2;
-        const int one_buf = g.swap ? 4 * 16 * kTP : epi_groups(g.bn, false) * kBM * 64;
+        const int one_buf = g.swap ? 4 * 16 * kTP : epi_groups(g.bn, false, g.ept != 0) * kBM * 64;
         const int weights = g.wres ? wblocks * wblock : g.stages * (g.halo ? 3 : 1) * wblock;
-        g.smem = 1024 + g.stages * g.a_stage + weights + one_buf * g.out_bufs + 8 * (2 * g.stages + 5) + 16;
+        g.smem = 1024 + g.stages * g.a_stage + weights + one_buf * g.out_bufs + 8 * (2 * g.stages + 9) + 16;
     }
     // Ask for more than half of an SM's shared memory so that no two CTAs of
     // this persistent kernel share an SM: each CTA then owns its TMEM
     // columns (at most 512) without waiting for another to free them.
     if (g.smem < 116 * 1024) g.smem = 116 * 1024;
     if (!tensor_map_encoder()) return CONV_ERR_CUDA;
-    void *kern = select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0, g.pair != 0, igemm_fused(p), g.halo != 0);
+    void *kern = select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0, g.pair != 0, igemm_fused(p), g.halo != 0, g.ept != 0);
     const int rc = conv_grant_smem(kern, p->device, g.smem);
     if (rc != CONV_OK) return rc;
     if (g.pair) {
@@ -308,7 +316,7 @@ int igemm_configure(conv_plan *p, int layout, int staging) {
         // SMs of one GPC), at most one per work unit
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * g.num_tiles);
-        cfg.blockDim = dim3(cta_threads(g.bn, false));
+        cfg.blockDim = dim3(cta_threads(g.bn, false, g.ept != 0));
         cfg.dynamicSmemBytes = (size_t)g.smem;
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeClusterDimension;
@@ -323,7 +331,7 @@ int igemm_configure(conv_plan *p, int layout, int staging) {
         g.grid = g.num_tiles < p->num_sms ? g.num_tiles : p->num_sms;
     }
     snprintf(p->desc, sizeof(p->desc),
-             "igemm_%s_tcgen05 %s%s %s BK=%d tile=%dx%d%s stages=%d%s out_bufs=%d tiles=%d grid=%d",
+             "igemm_%s_tcgen05 %s%s %s BK=%d tile=%dx%d%s stages=%d%s out_bufs=%d%s tiles=%d grid=%d",
              p->dtype == CONV_I8 ? (g.fold ? "i8-as-bf16-kwfold" : "i8-as-bf16")
                                  : (g.fold ? "bf16-cpad-kwfold" : (g.prep ? "bf16-cpad" : "bf16")),
              g.flat ? "flat" : "spatial",
@@ -332,7 +340,7 @@ int igemm_configure(conv_plan *p, int layout, int staging) {
                     : (g.pair ? (g.bn == 256 ? "M=256px N=256co" : "M=256px N=128co")
                               : (g.bn == 256 ? "M=128px N=256co" : (g.bn == 128 ? "M=128px N=128co" : "M=128px N=64co"))),
              g.bk, g.bh, g.bw, g.halo ? " halo" : "", g.stages, g.wres ? " resident-weights" : "", g.out_bufs,
-             g.num_tiles, g.grid);
+             g.ept ? " epi=tile" : "", g.num_tiles, g.grid);
     return CONV_OK;
 }
 
@@ -443,9 +451,9 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
     a.om.res = res;
     a.status = p->d_status;
 
-    void *k = select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0, g.pair != 0, igemm_fused(p), g.halo != 0);
+    void *k = select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0, g.pair != 0, igemm_fused(p), g.halo != 0, g.ept != 0);
     void *args[] = {&tmA, &tmB, &tmY, &a};
-    const cudaError_t e = conv_launch(k, dim3(g.grid), dim3(cta_threads(g.bn, g.swap != 0)), args, (size_t)g.smem, st,
+    const cudaError_t e = conv_launch(k, dim3(g.grid), dim3(cta_threads(g.bn, g.swap != 0, g.ept != 0)), args, (size_t)g.smem, st,
                                       g.pair ? 2 : 1);
     return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }

@@ -54,10 +54,15 @@ constexpr int kBM = 128;     // output pixels per tile (normal mode)
 constexpr int kBMSwap = 256; // output pixels per tile (swapped mode)
 constexpr int kTP = 272;     // swapped-mode transpose rows: 128 bf16 channels + 16 bytes of padding
 
-// Epilogue warpgroups per CTA: each takes a slice of every tile's columns.
-__host__ __device__ constexpr int epi_groups(int bn, bool swap) { return swap ? 4 : (bn >= 128 ? 4 : 2); }
+// Epilogue warpgroups per CTA: each takes a slice of every tile's columns,
+// or (ept: one epilogue per tile) whole tiles in turn.
+__host__ __device__ constexpr int epi_groups(int bn, bool swap, bool ept = false) {
+    return (swap || ept) ? 4 : (bn >= 128 ? 4 : 2);
+}
 // Threads per CTA: the TMA warp, the MMA warp and the epilogue warpgroups.
-__host__ __device__ constexpr int cta_threads(int bn, bool swap) { return 64 + 128 * epi_groups(bn, swap); }
+__host__ __device__ constexpr int cta_threads(int bn, bool swap, bool ept = false) {
+    return 64 + 128 * epi_groups(bn, swap, ept);
+}
 
 struct IgArgs {
     int H, W, Cin, Cout, KH, KW, stride, pad_h, pad_w, OH, OW;
@@ -359,22 +364,32 @@ __device__ __forceinline__ void epilogue_swapped_bf16(const IgArgs &a, int tile,
 // box and, unless they are resident, the three taps' weight blocks: one
 // barrier wait per twelve MMAs (measured: splitting the weights into a ring
 // of their own, for a deeper ring, was slower).
-template <int BN, int BK, bool FLAT, bool SWAP, bool PAIR, bool FUSED, bool HALO = false>
-__global__ void __launch_bounds__(cta_threads(BN, SWAP), 1)
+//
+// EPT (normal layout, BN <= 128, single CTAs): one epilogue per tile.  The
+// four epilogue warpgroups take whole tiles in turn, each from a TMEM
+// accumulator of its own (four buffers instead of two), instead of a slice
+// of every tile's columns.  For layers with many short tiles, whose time
+// goes to each tile's epilogue latency (TMEM load, activation, staging, TMA
+// store), four tiles' epilogues then run at once; and a layer with fewer
+// output channels than BN keeps every warpgroup busy.
+template <int BN, int BK, bool FLAT, bool SWAP, bool PAIR, bool FUSED, bool HALO = false, bool EPT = false>
+__global__ void __launch_bounds__(cta_threads(BN, SWAP, EPT), 1)
 igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ YMaps tmY, const IgArgs a) {
     static_assert(!(PAIR && SWAP), "the CTA-pair mode uses the normal layout");
     static_assert(!(HALO && FLAT), "halo staging is for spatial tiles");
+    static_assert(!EPT || (!SWAP && !PAIR && BN <= 128), "one epilogue per tile: normal layout, BN <= 128");
     constexpr int kPix = SWAP ? kBMSwap : kBM;  // pixel rows of a tile (per CTA)
     constexpr int kAcc = SWAP ? kBMSwap : BN;   // accumulator columns of a tile
     constexpr int kBRows = PAIR ? BN / 2 : BN;  // weight rows this CTA stages
     constexpr uint32_t kRowBytes = BK * 2;
     constexpr uint32_t kBStage = kBRows * BK * 2;  // one weight K block (this CTA's part)
-    constexpr uint32_t kTmemCols = 2 * kAcc;     // two accumulators
+    constexpr int kBufs = EPT ? 4 : 2;           // TMEM accumulators
+    constexpr uint32_t kTmemCols = kBufs * kAcc;
     constexpr uint32_t kIdesc = SWAP ? tc::idesc_bf16_f32(128, kBMSwap)
                                      : tc::idesc_bf16_f32(PAIR ? 2 * kBM : kBM, BN);
-    constexpr int kGroups = epi_groups(BN, SWAP);
-    constexpr int kCols = kAcc / kGroups;  // accumulator columns per epilogue thread
+    constexpr int kGroups = epi_groups(BN, SWAP, EPT);
+    constexpr int kCols = EPT ? kAcc : kAcc / kGroups;  // accumulator columns per epilogue thread
     static_assert(SWAP ? (BN == 128 && kCols % 16 == 0) : (kCols % 32 == 0), "epilogue column slices");
     constexpr uint32_t kOutStage = SWAP ? 16 * kTP : kBM * 64;  // per group: transpose rows / store staging
 
@@ -396,10 +411,10 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const uint32_t sBar = sOut + kGroups * a.out_bufs * kOutStage;
     auto full_bar = [&](int s) { return sBar + 8u * s; };
     auto empty_bar = [&](int s) { return sBar + 8u * (stages + s); };
-    auto tfull_bar = [&](int b) { return sBar + 8u * (2 * stages + b); };
-    auto tempty_bar = [&](int b) { return sBar + 8u * (2 * stages + 2 + b); };
-    const uint32_t wres_bar = sBar + 8u * (2 * stages + 4);  // the resident weights have landed
-    uint8_t *gmisc = gbase + (sBar - base) + 8u * (2 * stages + 5);
+    auto tfull_bar = [&](int b) { return sBar + 8u * (2 * stages + b); };       // b < 4
+    auto tempty_bar = [&](int b) { return sBar + 8u * (2 * stages + 4 + b); };
+    const uint32_t wres_bar = sBar + 8u * (2 * stages + 8);  // the resident weights have landed
+    uint8_t *gmisc = gbase + (sBar - base) + 8u * (2 * stages + 9);
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(gmisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gmisc + 4);
 
@@ -415,9 +430,10 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             tc::mbar_init(full_bar(s), 1);
             tc::mbar_init(empty_bar(s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kBufs; ++b) {
             tc::mbar_init(tfull_bar(b), 1);
-            tc::mbar_init(tempty_bar(b), PAIR ? 2 * 4 * kGroups : 128 * kGroups);  // pair: one per warp
+            // emptied by every epilogue thread (EPT: of one warpgroup); pair: by each warp
+            tc::mbar_init(tempty_bar(b), EPT ? 128 : (PAIR ? 2 * 4 * kGroups : 128 * kGroups));
         }
         tc::mbar_init(wres_bar, 1);
         *abort_flag = 0;
@@ -567,8 +583,8 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 tc::fence_after_sync();
             }
             for (int tile = unit; tile < a.num_tiles && ok; tile += units, ++lt) {
-                const int buf = lt & 1;
-                const uint32_t use = (uint32_t)(lt >> 1);
+                const int buf = lt % kBufs;
+                const uint32_t use = (uint32_t)(lt / kBufs);
                 if (!wait_bounded<PAIR>(tempty_bar(buf), (use & 1u) ^ 1u, abort_flag, a.status,
                                         KSTATUS_TIMEOUT_MMA))
                     break;
@@ -657,20 +673,22 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         // ------------------------------------------------ epilogue (warps 2 ..)
         // tcgen05.ld lets warp w reach TMEM lanes 32 * (w % 4) .. + 31, so every
         // run of four consecutive warps covers the 128 accumulator rows; warp
-        // group g (warps 2 + 4g .. 5 + 4g) drains columns [g * kCols, (g+1) * kCols).
+        // group g (warps 2 + 4g .. 5 + 4g) drains columns [g * kCols, (g+1) * kCols)
+        // (EPT: all columns of every 4th tile, from accumulator g).
         const int q = warp & 3;
         const int grp = (warp - 2) >> 2;
         const int row = q * 32 + lane;
-        const int c_base = grp * kCols;
+        const int c_base = EPT ? 0 : grp * kCols;
         const bool issuer = ((warp - 2) & 3) == 0 && lane == 0;  // issues the group's TMA stores
         const uint32_t sStage = sOut + (uint32_t)(grp * a.out_bufs) * kOutStage;  // this group's staging
         int oc = 0;  // TMA stores this group has issued (selects the staging buffer)
-        int lt = 0;
         // pair mode: accumulator-empty arrivals go to the even CTA's barrier
         const uint32_t tempty0 = PAIR ? tc::mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
-        for (int tile = unit; tile < a.num_tiles; tile += units, ++lt) {
-            const int buf = lt & 1;
-            const uint32_t use = (uint32_t)(lt >> 1);
+        // lt: the CTA's local tile index (EPT: this group's tiles, every 4th)
+        const int lt0 = EPT ? grp : 0, lstep = EPT ? kGroups : 1;
+        for (int tile = unit + lt0 * units, lt = lt0; tile < a.num_tiles; tile += lstep * units, lt += lstep) {
+            const int buf = lt % kBufs;
+            const uint32_t use = (uint32_t)(lt / kBufs);
             const bool got = wait_bounded(tfull_bar(buf), use & 1u, abort_flag, a.status,
                                           KSTATUS_TIMEOUT_EPILOGUE);
             __syncwarp();  // tcgen05.ld below is warp-collective (.sync.aligned)
@@ -691,7 +709,10 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             // TMEM and hand the buffer back to the MMA warp at once; FUSED
             // layers (registers for the residual) read it 32 columns at a time
             // and hand it back after the last chunk.
-            constexpr int kAccRegs = FUSED ? 32 : kCols;
+            // (EPT: a whole tile's columns would not fit in registers; the
+            // buffer is this group's alone, so it can wait for the last chunk)
+            constexpr bool kChunked = FUSED || EPT;
+            constexpr int kAccRegs = kChunked ? 32 : kCols;
             uint32_t acc[kAccRegs];
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c_base);
             auto release = [&]() {
@@ -703,7 +724,7 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     tc::mbar_arrive(tempty_bar(buf));
                 }
             };
-            if constexpr (!FUSED) {
+            if constexpr (!kChunked) {
 #pragma unroll
                 for (int c = 0; c < kCols; c += 32)
                     tc::tmem_ld_32x32(tbase + (uint32_t)c, *reinterpret_cast<uint32_t(*)[32]>(acc + c));
@@ -719,7 +740,7 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const int nb = tile % a.tiles_n;
             const int mt = PAIR ? (tile / a.tiles_n) * 2 + (int)rank : tile / a.tiles_n;
             if (PAIR && mt >= a.tiles_m) {  // the empty half of the last pair tile
-                if constexpr (FUSED) release();
+                if constexpr (kChunked) release();
                 continue;
             }
             int n = 0, oh0 = 0, ow0 = 0, m0 = 0;
@@ -749,7 +770,7 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             for (int c = 0; c < kCols; c += 32) {
                 const int co = nb * BN + c_base + c;
                 const bool live = co < a.Cout;  // the same for the whole group
-                if constexpr (FUSED) {
+                if constexpr (kChunked) {
                     if (live) {
                         tc::tmem_ld_32x32(tbase + (uint32_t)c, *reinterpret_cast<uint32_t(*)[32]>(acc));
                         tc::tmem_ld_wait();
@@ -757,7 +778,7 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     if (c + 32 == kCols) release();
                 }
                 if (!live) continue;
-                const uint32_t *av = acc + (FUSED ? 0 : c);  // this chunk's 32 accumulator columns
+                const uint32_t *av = acc + (kChunked ? 0 : c);  // this chunk's 32 accumulator columns
                 const uint32_t sbuf = sStage + (uint32_t)(oc & (a.out_bufs - 1)) * kOutStage;
                 const uint32_t srow = sbuf + (uint32_t)row * 64u;
                 // the store that last used this staging buffer has read it

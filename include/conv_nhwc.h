@@ -117,6 +117,14 @@ typedef enum {
  *         GEMM: im2col is never materialised either way). */
 #define CONV_ALGO_STAGE_TAPS 0x100
 #define CONV_ALGO_STAGE_HALO 0x200
+/* Epilogue split of the tensor-core family, OR-ed in the same way (default:
+ * one epilogue per tile where each CTA gets at least two tiles):
+ *   SLICED    every epilogue warpgroup drains a slice of each tile's columns;
+ *   PER_TILE  each warpgroup drains whole tiles in turn from a TMEM
+ *             accumulator of its own (normal layouts with N <= 128 and no
+ *             conv_output_t options; CONV_ERR_UNSUPPORTED otherwise). */
+#define CONV_ALGO_EPI_SLICED 0x400
+#define CONV_ALGO_EPI_PER_TILE 0x800
 
 enum {
     CONV_OK = 0,

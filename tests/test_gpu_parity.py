@@ -86,19 +86,33 @@ def with_layouts(specs):
                     "igemm_pair128"]:
             if lay == "igemm_swapped" and spec.cout > 128:
                 continue
-            for stage in (["", "+halo", "+taps"] if halo_eligible(spec) else [""]):
-                out.append(pytest.param(spec, lay + stage, id=f"{spec.name}-{lay}{stage}"))
+            variants = ["", "+halo", "+taps"] if halo_eligible(spec) else [""]
+            # the epilogue split, on the layouts that offer both
+            if lay in ("igemm", "igemm_n128", "igemm_n64"):
+                variants += ["+ept", "+sliced"] + (["+halo+ept"] if halo_eligible(spec) else [])
+            for v in variants:
+                out.append(pytest.param(spec, lay + v, id=f"{spec.name}-{lay}{v}"))
     return out
 
 
 def check_layout(spec, layout):
     plan = check(spec, layout, "igemm")
-    base, _, stage = layout.partition("+")
+    base, *flags = layout.split("+")
     if base in _LAYOUT_DESC:
         assert _LAYOUT_DESC[base] in plan.describe(), plan.describe()
-    if stage:
-        assert (" halo " in plan.describe()) == (stage == "halo"), plan.describe()
+    if "halo" in flags or "taps" in flags:
+        assert (" halo " in plan.describe()) == ("halo" in flags), plan.describe()
+    if "ept" in flags or "sliced" in flags:
+        assert ("epi=tile" in plan.describe()) == ("ept" in flags), plan.describe()
     return plan
+
+
+def test_epilogue_per_tile_needs_normal_layout():
+    spec = L("ept_cout256", 1, 8, 8, 64, 256, 3, 3, 1, 1, 1)
+    d = make_layer(spec, torch.Generator("cpu").manual_seed(0))
+    for algo in ("igemm_swapped+ept", "igemm_n256+ept", "igemm_pair+ept", "igemm_pair128+ept"):
+        with pytest.raises(RuntimeError, match="UNSUPPORTED"):
+            make_plan(spec, d, algo)
 
 
 def test_halo_staging_needs_stride1_kh3():
