@@ -247,25 +247,65 @@ def run_ours(args, rank, world, device):
     clk = clocks.stop()
     step_ms = np.array([e0[k].elapsed_time(e1[k]) for k in range(args.steps)])
 
-    # Per-layer figures (outside the timed region): each layer alone as a
-    # graph between two events, cold (L2 flushed before each replay) and warm.
-    reps = min(args.steps, 50)
-    per_layer = np.zeros((reps, nl))
-    warm = np.zeros(nl)
-    for i in range(nl):
-        gi, (ea, eb) = capture(lambda i=i: plans[i].run(X[i], Wt[i], B[i], Y[i], torch.cuda.current_stream(dev)),
-                               with_events=True)
-        for r in range(reps):
+    # Per-layer figures.  (1) In the step: the same step captured with an
+    # event between consecutive layers, replayed `steps` times with the same
+    # L2 flush before each replay; a layer's duration is the mean over the
+    # replays of the time between its two events (the events serialise the
+    # layers, so this graph is not the one `value` times).  (2) Alone: each
+    # layer R times in one graph, cold ([flush, layer] x R minus [flush] x R)
+    # and warm ([layer] x R back to back), divided by R: the timer's ~2 us
+    # tick then costs at most ~0.1 us per launch.
+    def evented_step():
+        st = torch.cuda.current_stream(dev)
+        for i in range(nl):
+            lev[i].record(st)
+            plans[i].run(X[i], Wt[i], B[i], Y[i], st)
+        lev[nl].record(st)
+
+    lev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(nl + 1)]
+    gl, _ = capture(evented_step)
+    per_layer = np.zeros((args.steps, nl))
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        gl.replay()
+        torch.cuda.synchronize()
+        for i in range(nl):
+            per_layer[k, i] = lev[i].elapsed_time(lev[i + 1])
+    del gl
+
+    R = 20
+
+    def graph_time(fn, reps=5):
+        g, (ea, eb) = capture(fn, with_events=True)
+        best = None
+        for _ in range(reps):
+            g.replay()
+            torch.cuda.synchronize()
+            t = ea.elapsed_time(eb) * 1e3
+            best = t if best is None else min(best, t)
+        del g
+        return best
+
+    def flushes():
+        for r in range(R):
             flush.fill_(r & 0xFF)
-            gi.replay()
-            torch.cuda.synchronize()
-            per_layer[r, i] = ea.elapsed_time(eb)
-        ws = []
-        for r in range(20):
-            gi.replay()
-            torch.cuda.synchronize()
-            ws.append(ea.elapsed_time(eb) * 1e3)
-        warm[i] = float(np.median(ws))
+
+    t_flush = graph_time(flushes)
+    alone_cold = np.zeros(nl)
+    alone_warm = np.zeros(nl)
+    for i in range(nl):
+        def cold(i=i):
+            st = torch.cuda.current_stream(dev)
+            for r in range(R):
+                flush.fill_(r & 0xFF)
+                plans[i].run(X[i], Wt[i], B[i], Y[i], st)
+
+        def warm(i=i):
+            st = torch.cuda.current_stream(dev)
+            for r in range(R):
+                plans[i].run(X[i], Wt[i], B[i], Y[i], st)
+        alone_cold[i] = (graph_time(cold) - t_flush) / R
+        alone_warm[i] = graph_time(warm) / R
     for p in plans:
         p.check_device_status()
     my_ms = float(step_ms.sum())
@@ -281,7 +321,7 @@ def run_ours(args, rank, world, device):
     layer_rows = []
     for i, d in enumerate(layers):
         s = d.spec
-        us = float(np.median(per_layer[:, i]) * 1e3)
+        us = float(per_layer[:, i].mean() * 1e3)
         bound, ai = layer_bound(s, peaks)
         fl = flops_of(s)
         by = alg_bytes(s)
@@ -291,7 +331,7 @@ def run_ours(args, rank, world, device):
             ach, pk, unit = by / (us * 1e-6) / 1e9, peaks["hbm_gbs"], "GB/s"
         layer_rows.append({
             "layer": s.name, "kernel": plans[i].describe(), "us": round(us, 2),
-            "us_mean": round(float(per_layer[:, i].mean() * 1e3), 2), "us_warm_l2": round(float(warm[i]), 2),
+            "us_alone_cold": round(float(alone_cold[i]), 2), "us_alone_warm": round(float(alone_warm[i]), 2),
             "tflops": round(fl / (us * 1e-6) / 1e12, 1), "gbs": round(by / (us * 1e-6) / 1e9, 1),
             "ai_flop_per_byte": round(ai, 1), "bound": bound,
             "achieved": round(ach, 1), "peak": pk, "unit": unit, "frac": round(ach / pk, 4),
@@ -336,8 +376,9 @@ def run_ours(args, rank, world, device):
         "data": "synthetic",
         "config": {"workload": args.workload, "layers": len(layers),
                    "batch_per_gpu": layers[0].spec.n, "l2": "flushed before every step (outside the events)",
-                   "launch": "CUDA graph replay of the step, events around each replay; per-layer figures "
-                             "from each layer's own graph",
+                   "launch": "CUDA graph replay of the step, events around each replay; per-layer 'us': "
+                             "the step replayed again with events between its layers (mean over the steps); "
+                             "'us_alone_*': each layer 20x in its own graph",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roofline, "layers": layer_rows, "e2e": e2e,
         "peaks": {"bf16_tflops": peaks["bf16_tflops"], "hbm_gbs": peaks["hbm_gbs"],
@@ -350,12 +391,13 @@ def run_ours(args, rank, world, device):
     return out
 
 
-def measure_next_rows(dev, peaks, reps=30):
+def measure_next_rows(dev, peaks, reps=20):
     """The adjacent rows built beyond the five layer sets (the residual-add
-    epilogue, concat + 2x upsample output placement, the SPP block), each
-    timed like a layer of the main step: one call captured as a CUDA graph
-    between two events, replayed `reps` times with the L2 flushed before
-    every replay; the mean event time is reported with its roofline."""
+    epilogue, concat + 2x upsample output placement, the SPP block, the fused
+    depthwise -> pointwise pair), each timed like a layer alone in the main
+    step: `reps` calls, each after an L2 flush, captured in one CUDA graph
+    between two events, minus the same graph of flushes alone, divided by
+    `reps`; reported with its roofline."""
     import torch
     import convolution_nhwc_implicit_gb300 as cl
     from conv_workloads import LayerSpec, alg_bytes, make_layer
@@ -363,24 +405,39 @@ def measure_next_rows(dev, peaks, reps=30):
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20)
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
 
-    def timed(fn):
-        fn()
-        torch.cuda.synchronize()
+    def graph_us(body):
         e0 = torch.cuda.Event(enable_timing=True, external=True)
         e1 = torch.cuda.Event(enable_timing=True, external=True)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             st = torch.cuda.current_stream(dev)
             e0.record(st)
-            fn()
+            body()
             e1.record(st)
-        ts = []
-        for _ in range(reps):
-            flush.fill_(1)
+        best = None
+        for _ in range(5):
             g.replay()
             torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1) * 1e3)
-        return float(np.mean(ts))
+            t = e0.elapsed_time(e1) * 1e3
+            best = t if best is None else min(best, t)
+        del g
+        return best
+
+    def flushes():
+        for r in range(reps):
+            flush.fill_(r & 0xFF)
+
+    t_flush = graph_us(flushes)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+
+        def body():
+            for r in range(reps):
+                flush.fill_(r & 0xFF)
+                fn()
+        return (graph_us(body) - t_flush) / reps
 
     def roof(flops, nbytes, us):
         ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
@@ -504,7 +561,8 @@ def run_e2e(args, layers, plans, dev, stream, total_flops, world):
 # Source files that define each kernel family (a change to any of them voids
 # the DRAM traffic captured for that family).
 _FAMILY_SOURCES = {
-    "igemm": ["k_igemm.cu", "k_igemm_kernel.cuh", "k_prep.cu", "tc_ptx.cuh", "epilogue.cuh", "conv_internal.h"],
+    "igemm": ["k_igemm.cu", "k_igemm_ept.cu", "k_igemm_kernel.cuh", "k_prep.cu", "tc_ptx.cuh", "epilogue.cuh",
+              "conv_internal.h"],
     "dw3x3+pw1x1": ["k_dwpw.cu", "epilogue.cuh", "conv_internal.h"],
     "dw3x3": ["k_dw3x3.cu", "tc_ptx.cuh", "epilogue.cuh", "conv_internal.h"],
     "direct": ["k_direct.cu", "epilogue.cuh", "conv_internal.h"],
@@ -580,10 +638,16 @@ def oracle_sample(layers, budget_s, seed=0):
             npts += count
         return fl, secs, npts
 
+    # calibrate: grow the sample until it takes at least half the budget
+    # (a tiny first sample is dominated by fixed costs and overestimates the
+    # time per point)
     frac = 2e-5
     fl, secs, npts = run(frac)
-    scale = max(1.0, budget_s / max(secs, 1e-3))
-    fl, secs, npts = run(min(1.0, frac * scale))
+    for _ in range(4):
+        if secs >= 0.5 * budget_s or frac >= 1.0:
+            break
+        frac = min(1.0, frac * min(100.0, budget_s / max(secs, 1e-3)))
+        fl, secs, npts = run(frac)
     return fl, secs, npts, oracle.max_threads(0)
 
 
