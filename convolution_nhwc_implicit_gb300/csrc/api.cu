@@ -162,9 +162,11 @@ int conv_plan_create_fused(const conv_shape_t *shape, int stride, int pad_h, int
     // staging and epilogue flags (tensor-core family only), then the family / layout
     const int stage_flags = (int)algo & (CONV_ALGO_STAGE_TAPS | CONV_ALGO_STAGE_HALO);
     const int epi_flags = (int)algo & (CONV_ALGO_EPI_SLICED | CONV_ALGO_EPI_PER_TILE);
-    algo = (conv_algo_t)((int)algo & ~(CONV_ALGO_STAGE_TAPS | CONV_ALGO_STAGE_HALO | CONV_ALGO_EPI_SLICED |
-                                       CONV_ALGO_EPI_PER_TILE));
-    if ((int)algo < CONV_ALGO_AUTO || ((int)algo > CONV_ALGO_IGEMM_PAIR && algo != CONV_ALGO_IGEMM_PAIR128))
+    const int unknown_bits = (int)algo & ~(0xFF | CONV_ALGO_STAGE_TAPS | CONV_ALGO_STAGE_HALO | CONV_ALGO_EPI_SLICED |
+                                           CONV_ALGO_EPI_PER_TILE);
+    algo = (conv_algo_t)((int)algo & 0xFF);
+    if (unknown_bits || (int)algo < CONV_ALGO_AUTO ||
+        ((int)algo > CONV_ALGO_IGEMM_PAIR && algo != CONV_ALGO_IGEMM_PAIR128))
         return CONV_ERR_INVALID_ARG;
     if (stage_flags == (CONV_ALGO_STAGE_TAPS | CONV_ALGO_STAGE_HALO) ||
         epi_flags == (CONV_ALGO_EPI_SLICED | CONV_ALGO_EPI_PER_TILE) ||
