@@ -25,7 +25,7 @@ from dataclasses import dataclass, field, replace
 
 import torch
 
-__all__ = ["LayerSpec", "LayerData", "CONFIGS", "SEEDS", "generate", "make_layer",
+__all__ = ["LayerSpec", "LayerData", "CONFIGS", "SEEDS", "generate", "make_layer", "make_layer_device_x",
            "spec_by_name", "macs", "alg_bytes", "output_hw"]
 
 
@@ -207,6 +207,27 @@ def make_layer(s: LayerSpec, g: torch.Generator) -> LayerData:
         lo, hi = s.ws_dist[1], s.ws_dist[2]
         ws = torch.rand((s.cout,), generator=g, dtype=torch.float32) * (hi - lo) + lo
     return LayerData(s, _cast(x, s.dtype), _cast(w, s.dtype), b, ws)
+
+
+def make_layer_device_x(s: LayerSpec, seed: int, device) -> LayerData:
+    """As make_layer, but x is drawn on ``device`` by a generator of that
+    device seeded with ``seed`` (for inputs too large to draw on the host):
+    uniform x_dist only, or int U[lo, hi] for int8.  w, b (and int8 scales)
+    are drawn on the host from a CPU generator seeded with ``seed``."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    gd = torch.Generator(device=device).manual_seed(seed)
+    xshape = (s.n, s.h, s.w, s.cin)
+    kind = s.x_dist[0]
+    if kind == "uniform":
+        lo, hi = s.x_dist[1], s.x_dist[2]
+        x = torch.rand(xshape, generator=gd, device=device, dtype=torch.float32).mul_(hi - lo).add_(lo)
+    elif kind == "int":
+        x = torch.randint(s.x_dist[1], s.x_dist[2] + 1, xshape, generator=gd, device=device, dtype=torch.int16)
+    else:
+        raise ValueError(f"device draw of {kind!r} inputs is not offered")
+    x = _cast(x, s.dtype)
+    d = make_layer(replace(s, n=0), g)  # w, b, scales only (x of an empty batch)
+    return LayerData(s, x, d.w, d.b, d.w_scales)
 
 
 def generate(config: str, layers: list[str] | None = None) -> list[LayerData]:
