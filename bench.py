@@ -164,6 +164,10 @@ def run_ours(args, rank, world, device):
     sm_mhz = float(peaks.get("sm_max_mhz") or 2070.0)
     peaks["fp32_ffma_tflops"] = round(props.multi_processor_count * 128 * 2 * sm_mhz * 1e6 / 1e12, 1)
     layers = generate(args.workload)
+    if args.only:  # (profile pass) just these layers of the set
+        layers = [d for d in layers if d.spec.name in args.only.split(",")]
+        if not layers:
+            raise SystemExit(f"--only: no layer of {args.workload} is named {args.only}")
     plans, X, Wt, B, Y = [], [], [], [], []
     for d in layers:
         s = d.spec
@@ -696,6 +700,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next-rows", action="store_true", help="skip timing the residual / concat / SPP rows")
+    ap.add_argument("--only", default="",
+                    help="run only these layers of the set (comma-separated names; for profiler captures)")
     ap.add_argument("--profile-pass", action="store_true",
                     help="run the layers eagerly (warmup + 1 passes, in order) for a profiler and print their "
                          "plans; no timing")
