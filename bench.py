@@ -310,6 +310,21 @@ def run_ours(args, rank, world, device):
                 plans[i].run(X[i], Wt[i], B[i], Y[i], st)
         alone_cold[i] = (graph_time(cold) - t_flush) / R
         alone_warm[i] = graph_time(warm) / R
+
+    # The per-launch floor: a layer of almost no work (depthwise 3x3 on one
+    # 8x8x8 bf16 image) 20 times back to back in one graph, per launch.
+    tiny = cl.Plan(1, 8, 8, 8, 8, 3, 3, 1, 1, 1, 8, "bf16", "none")
+    tx = torch.zeros(1, 8, 8, 8, dtype=torch.bfloat16, device=dev)
+    tw = torch.zeros(8, 3, 3, 1, dtype=torch.bfloat16, device=dev)
+    ty = torch.empty(1, 8, 8, 8, dtype=torch.bfloat16, device=dev)
+
+    def tiny_run():
+        st = torch.cuda.current_stream(dev)
+        for r in range(R):
+            tiny.run(tx, tw, None, ty, st)
+    tiny_run()
+    torch.cuda.synchronize()
+    launch_floor = graph_time(tiny_run) / R
     for p in plans:
         p.check_device_status()
     my_ms = float(step_ms.sum())
@@ -389,6 +404,7 @@ def run_ours(args, rank, world, device):
                   "fp32_ffma_tflops": peaks["fp32_ffma_tflops"], "source": peaks_src,
                   "int8_probe": int8_probe},
         "next_rows": measure_next_rows(dev, peaks) if rank == 0 and not args.no_next_rows else None,
+        "launch_floor_us": round(float(launch_floor), 2),
         "gpu_launches": sum(p.launches for p in plans) * args.steps, "clocks": clk,
         "wall_s_timed_region": round(wall, 4),
     }

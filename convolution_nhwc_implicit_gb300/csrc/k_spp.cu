@@ -149,6 +149,65 @@ __global__ void __launch_bounds__(kThreads) spp_kernel(const uint4 *__restrict__
     store_tile(A, 0, y, a, n, h0, w0, cv0, 2);
 }
 
+// Whole-image variant, for images whose H x W x cbv vectors fit in shared
+// memory twice: a CTA owns one image and cbv channel vectors, so nothing is
+// loaded or pooled twice (the tiled kernel above re-reads a 6-pixel halo
+// around every 8x8 tile).  Windows are clipped to the image instead of
+// padded with -inf: a 5-wide max over the clipped window of 5-wide maxima
+// over clipped windows is the 9-wide max over the clipped window, exactly as
+// with padding, so the cascade is unchanged.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) spp_image_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ y,
+                                                             const SppArgs a) {
+    pdl_trigger();  // see conv_launch
+    pdl_wait();
+    extern __shared__ __align__(16) uint4 sm[];
+    const int n = blockIdx.x;
+    const int cv0 = blockIdx.y * a.cbv;
+    const int np = a.H * a.W;
+    const int nel = np * a.cbv;
+    uint4 *A = sm;
+    uint4 *B = sm + nel;
+    const uint4 neg = make_uint4(VMax<T>::kNeg, VMax<T>::kNeg, VMax<T>::kNeg, VMax<T>::kNeg);
+    const long long xbase = (long long)n * np;
+    // x -> A (and to its own slice of y, if asked)
+    for (int e = threadIdx.x; e < nel; e += kThreads) {
+        const int cv = e % a.cbv, p = e / a.cbv;
+        uint4 v = neg;
+        if (cv0 + cv < a.CV) {
+            v = __ldg(x + (xbase + p) * a.CV + cv0 + cv);
+            if (a.off[3] >= 0) y[(xbase + p) * a.Cy + a.off[3] + cv0 + cv] = v;
+        }
+        A[e] = v;
+    }
+    __syncthreads();
+    for (int level = 0; level < 3; ++level) {  // 5x5, 9x9, 13x13
+        // along rows (A -> B), then along columns (B -> A): clipped 5-wide maxima
+        for (int dir = 0; dir < 2; ++dir) {
+            const uint4 *src = dir ? B : A;
+            uint4 *dst = dir ? A : B;
+            for (int e = threadIdx.x; e < nel; e += kThreads) {
+                const int cv = e % a.cbv, p = e / a.cbv;
+                const int h = p / a.W, w = p - h * a.W;
+                const int pos = dir ? h : w, len = dir ? a.H : a.W;
+                const int step = (dir ? a.W : 1) * a.cbv;
+                const int lo = pos < 2 ? -pos : -2, hi = pos + 2 >= len ? len - 1 - pos : 2;
+                uint4 m = src[e + lo * step];
+                for (int d = lo + 1; d <= hi; ++d) m = VMax<T>::max(m, src[e + d * step]);
+                dst[e] = m;
+            }
+            __syncthreads();
+        }
+        if (a.off[level] >= 0) {
+            for (int e = threadIdx.x; e < nel; e += kThreads) {
+                const int cv = e % a.cbv, p = e / a.cbv;
+                if (cv0 + cv < a.CV) y[(xbase + p) * a.Cy + a.off[level] + cv0 + cv] = A[e];
+            }
+        }
+        // (the next level's row pass overwrites B only: A stays readable here)
+    }
+}
+
 bool overlaps(const void *p, size_t np, const void *q, size_t nq) {
     const uintptr_t a0 = (uintptr_t)p, b0 = (uintptr_t)q;
     return np && nq && a0 < b0 + nq && b0 < a0 + np;
@@ -181,6 +240,39 @@ extern "C" int conv_spp_run(int32_t n, int32_t h, int32_t w, int32_t c, conv_dty
 
     SppArgs a;
     a.N = n; a.H = h; a.W = w; a.CV = c * es / 16;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CONV_ERR_CUDA;
+    int num_sms = 0;
+    if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return CONV_ERR_CUDA;
+    // Whole images when two copies of an image's channel block fit in 96 KB:
+    // the fewest channel vectors per CTA that still give every SM two CTAs.
+    {
+        const long long px = (long long)h * w;
+        int cbv = 0;
+        for (int v = 1; v <= a.CV && v <= 16; v *= 2) {
+            if (a.CV % v != 0 || 2 * px * v * 16 > 96 * 1024) break;
+            cbv = v;
+            if ((long long)n * (a.CV / v) <= 2LL * num_sms) break;
+        }
+        if (cbv > 0 && (long long)n * (a.CV / cbv) <= 0x7fffffffll && a.CV / cbv <= 65535) {
+            a.cbv = cbv;
+            a.tiles_w = a.tiles_h = 1;
+            a.Cy = y_channels * es / 16;
+            for (int i = 0; i < 4; ++i) a.off[i] = offs[i] < 0 ? -1 : offs[i] * es / 16;
+            const size_t smem = (size_t)2 * px * cbv * sizeof(uint4);
+            const void *k = dtype == CONV_F32 ? (const void *)&spp_image_kernel<float>
+                                              : (dtype == CONV_BF16 ? (const void *)&spp_image_kernel<__nv_bfloat16>
+                                                                    : (const void *)&spp_image_kernel<int8_t>);
+            const int rc = conv_grant_smem(k, dev, (int)smem);
+            if (rc != CONV_OK) return rc;
+            const uint4 *xv = static_cast<const uint4 *>(x);
+            uint4 *yv = static_cast<uint4 *>(y);
+            void *args[] = {(void *)&xv, (void *)&yv, (void *)&a};
+            const cudaError_t e = conv_launch(k, dim3((unsigned)n, (unsigned)(a.CV / cbv)), dim3(kThreads), args,
+                                              smem, (cudaStream_t)stream);
+            return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+        }
+    }
     a.cbv = a.CV < 8 ? a.CV : 8;
     a.tiles_w = (w + kTW - 1) / kTW;
     a.tiles_h = (h + kTH - 1) / kTH;
@@ -193,8 +285,6 @@ extern "C" int conv_spp_run(int32_t n, int32_t h, int32_t w, int32_t c, conv_dty
     const void *k = dtype == CONV_F32 ? (const void *)&spp_kernel<float>
                                       : (dtype == CONV_BF16 ? (const void *)&spp_kernel<__nv_bfloat16>
                                                             : (const void *)&spp_kernel<int8_t>);
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return CONV_ERR_CUDA;
     const int rc = conv_grant_smem(k, dev, (int)smem);
     if (rc != CONV_OK) return rc;
     const uint4 *xv = static_cast<const uint4 *>(x);

@@ -18,6 +18,9 @@ CASES = [
     ("i8_13x9x48_no_copy", 1, 13, 9, 48, "i8", 192, 16, 80, 144, -1),
     ("single_pixel", 1, 1, 1, 8, "bf16", 32, 0, 8, 16, 24),
     ("wide_image_c8", 2, 3, 40, 8, "bf16", 48, 8, 16, 32, 0),
+    # images too large for the whole-image kernel: 8x8 tiles with a 6-pixel halo
+    ("tiled_80x80x64", 1, 80, 80, 64, "bf16", 256, 0, 64, 128, 192),
+    ("tiled_i8_b2_57x61x32", 2, 57, 61, 32, "i8", 128, 96, 64, 32, 0),
 ]
 DT = {"f32": torch.float32, "bf16": torch.bfloat16, "i8": torch.int8}
 
