@@ -148,6 +148,27 @@ class ClockSampler:
                 "samples": len(sm), "window": where}
 
 
+# ---------------------------------------------------------------- replicas
+
+def max_over_ranks(ms, world, device):
+    """The slowest rank's time: every rank runs the same fixed work (weak
+    scaling, no data-path collective), so the job takes as long as its
+    slowest replica.  `device` is where the reduction runs (the rank's GPU
+    under NCCL, the CPU under gloo)."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_step, world, steps, ms):
+    """Whole-job throughput: the work of every rank's `steps` steps over the
+    slowest rank's time (ms)."""
+    return flops_per_step * world * steps / (ms * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, device):
@@ -327,14 +348,10 @@ def run_ours(args, rank, world, device):
     launch_floor = graph_time(tiny_run) / R
     for p in plans:
         p.check_device_status()
-    my_ms = float(step_ms.sum())
-    if world > 1:
-        t = torch.tensor([my_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        my_ms = float(t.item())
+    my_ms = max_over_ranks(float(step_ms.sum()), world, dev)
     total_flops = sum(flops_of(d.spec) for d in layers)
     ms_per_step = my_ms / args.steps
-    value = total_flops * world * args.steps / (my_ms * 1e-3) / 1e12
+    value = job_tflops(total_flops, world, args.steps, my_ms)
 
     # ---- per-layer figures and the dominant kernel's roofline
     layer_rows = []
@@ -598,12 +615,8 @@ def run_e2e(args, layers, plans, dev, stream, total_flops, world):
         step(i)
     e1.record(s_down)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": round(total_flops * world * k / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    return {"value": round(job_tflops(total_flops, world, k, ms), 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": round(ms / k, 4),
             "how": "uploads, layers and downloads on three streams, two device buffer sets"}
