@@ -32,10 +32,11 @@ ACTS = {"none": 0, "relu": 1, "mish": 2}
 ALGOS = {"auto": 0, "direct": 1, "depthwise": 2, "igemm": 3, "igemm_swapped": 4, "igemm_n256": 5,
          "igemm_n128": 6, "igemm_n64": 7, "igemm_pair": 8, "dwpw": 9, "igemm_pair128": 10}
 ALGO_NAMES = {v: k for k, v in ALGOS.items()}
-# Staging and epilogue flags of the tensor-core family (CONV_ALGO_STAGE_*,
-# CONV_ALGO_EPI_*), written as suffixes of the algo name: "igemm+halo",
-# "igemm_n64+taps+ept".
-ALGO_FLAGS = {"taps": 0x100, "halo": 0x200, "sliced": 0x400, "ept": 0x800}
+# Staging, epilogue and int8-widening flags of the tensor-core family
+# (CONV_ALGO_STAGE_*, CONV_ALGO_EPI_*, CONV_ALGO_WIDEN_*), written as suffixes
+# of the algo name: "igemm+halo", "igemm_n64+taps+ept", "igemm+inkernel".
+ALGO_FLAGS = {"taps": 0x100, "halo": 0x200, "sliced": 0x400, "ept": 0x800, "prepass": 0x1000,
+              "inkernel": 0x2000}
 
 
 def _algo_code(algo: str) -> int:

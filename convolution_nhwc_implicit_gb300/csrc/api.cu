@@ -162,15 +162,17 @@ int conv_plan_create_fused(const conv_shape_t *shape, int stride, int pad_h, int
     // staging and epilogue flags (tensor-core family only), then the family / layout
     const int stage_flags = (int)algo & (CONV_ALGO_STAGE_TAPS | CONV_ALGO_STAGE_HALO);
     const int epi_flags = (int)algo & (CONV_ALGO_EPI_SLICED | CONV_ALGO_EPI_PER_TILE);
+    const int widen_flags = (int)algo & (CONV_ALGO_WIDEN_PREPASS | CONV_ALGO_WIDEN_INKERNEL);
     const int unknown_bits = (int)algo & ~(0xFF | CONV_ALGO_STAGE_TAPS | CONV_ALGO_STAGE_HALO | CONV_ALGO_EPI_SLICED |
-                                           CONV_ALGO_EPI_PER_TILE);
+                                           CONV_ALGO_EPI_PER_TILE | CONV_ALGO_WIDEN_PREPASS | CONV_ALGO_WIDEN_INKERNEL);
     algo = (conv_algo_t)((int)algo & 0xFF);
     if (unknown_bits || (int)algo < CONV_ALGO_AUTO ||
         ((int)algo > CONV_ALGO_IGEMM_PAIR && algo != CONV_ALGO_IGEMM_PAIR128))
         return CONV_ERR_INVALID_ARG;
     if (stage_flags == (CONV_ALGO_STAGE_TAPS | CONV_ALGO_STAGE_HALO) ||
         epi_flags == (CONV_ALGO_EPI_SLICED | CONV_ALGO_EPI_PER_TILE) ||
-        ((stage_flags || epi_flags) && (algo < CONV_ALGO_IGEMM || algo == CONV_ALGO_DWPW)))
+        widen_flags == (CONV_ALGO_WIDEN_PREPASS | CONV_ALGO_WIDEN_INKERNEL) ||
+        ((stage_flags || epi_flags || widen_flags) && (algo < CONV_ALGO_IGEMM || algo == CONV_ALGO_DWPW)))
         return CONV_ERR_INVALID_ARG;
     int oh = 0, ow = 0;
     int rc = validate(shape, stride, pad_h, pad_w, groups, dtype, act, quant, &oh, &ow);
@@ -260,7 +262,8 @@ int conv_plan_create_fused(const conv_shape_t *shape, int stride, int pad_h, int
                                  ? 6
                                  : (algo >= CONV_ALGO_IGEMM_SWAPPED ? (int)algo - CONV_ALGO_IGEMM_SWAPPED + 1 : 0),
                              stage_flags == CONV_ALGO_STAGE_TAPS ? 1 : (stage_flags == CONV_ALGO_STAGE_HALO ? 2 : 0),
-                             epi_flags == CONV_ALGO_EPI_SLICED ? 1 : (epi_flags == CONV_ALGO_EPI_PER_TILE ? 2 : 0));
+                             epi_flags == CONV_ALGO_EPI_SLICED ? 1 : (epi_flags == CONV_ALGO_EPI_PER_TILE ? 2 : 0),
+                             widen_flags == CONV_ALGO_WIDEN_PREPASS ? 1 : (widen_flags == CONV_ALGO_WIDEN_INKERNEL ? 2 : 0));
         if (rc != CONV_OK) { conv_plan_destroy(p); return rc; }
     } else if (chosen == CONV_ALGO_DEPTHWISE) {
         rc = dw3x3_configure(p);

@@ -32,6 +32,9 @@ struct IgemmGeom {
     int halo;      // 1: halo staging (a stage holds the tile's input rows for all k_h taps of one column shift)
     int a_stage;   // bytes of the activation part of a ring stage
     int ept;       // 1: one epilogue per tile (each warpgroup drains whole tiles, four TMEM accumulators)
+    int cvt;       // 1: int8 operands widened to bf16 in the kernel (converter warpgroup), no pre-pass
+    int raw_stage; // cvt: bytes of a raw int8 activation stage
+    int raw_region;  // cvt: bytes of the raw region (raw weights, then the raw ring)
     int stages;    // shared-memory pipeline depth
     int out_bufs;  // epilogue output staging buffers per group (1 or 2)
     int wres;      // 1: all weights resident in shared memory (one N block, loaded once per CTA)
@@ -134,13 +137,17 @@ void *igemm_select_fused(int bn, int bk, bool flat, bool swap, bool pair, bool h
 // The variant with one epilogue per tile (normal layout, BN 64 or 128, no
 // output options), compiled in its own translation unit.
 void *igemm_select_ept(int bn, int bk, bool flat, bool halo);
+// The variant that widens int8 operands in the kernel (normal layout,
+// resident weights, no output options), compiled in its own translation unit.
+void *igemm_select_cvt(int bn, int bk, bool flat, bool halo);
 // Fills p->ig and sets kernel attributes; CONV_* status.  layout 0 picks
 // the tile layout by estimated time; 1..6 force swapped, N256, N128, N64,
 // CTA pair (N = 256), CTA pair (N = 128).  staging 0 picks per-tap or halo
 // staging by estimated time; 1 forces per-tap boxes, 2 halo staging.  epi 0
 // picks the epilogue split by the tile count; 1 forces column slices, 2 one
-// epilogue per tile.
-int igemm_configure(conv_plan *p, int layout, int staging, int epi);
+// epilogue per tile.  widen (int8 layers) 0 picks, 1 forces the widening
+// pre-pass, 2 the in-kernel converter.
+int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen);
 
 // Host-side argument checks shared by the entry points (api.cu).
 int conv_validate_layer(const conv_shape_t *s, int stride, int pad_h, int pad_w, int groups,

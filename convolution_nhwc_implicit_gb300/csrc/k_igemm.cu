@@ -50,9 +50,10 @@ void *kernel_ptr_bk(int bk, bool flat, bool halo) {
     }
 }
 
-void *select_kernel(int bn, int bk, bool flat, bool swap, bool pair, bool fused, bool halo, bool ept) {
+void *select_kernel(int bn, int bk, bool flat, bool swap, bool pair, bool fused, bool halo, bool ept, bool cvt) {
     if (fused) return igemm_select_fused(bn, bk, flat, swap, pair, halo);
     if (ept) return igemm_select_ept(bn, bk, flat, halo);
+    if (cvt) return igemm_select_cvt(bn, bk, flat, halo);
     if (pair) return bn == 128 ? kernel_ptr_bk<128, false, true>(bk, flat, halo)
                                : kernel_ptr_bk<256, false, true>(bk, flat, halo);
     if (swap) return kernel_ptr_bk<128, true, false>(bk, flat, halo);
@@ -105,12 +106,11 @@ bool igemm_supported(const conv_plan *p) {
     return true;
 }
 
-int igemm_configure(conv_plan *p, int layout, int staging, int epi) {
+int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
     IgemmGeom &g = p->ig;
     const int S = p->stride;
     g.in_i8 = 0;
     const int cin = igemm_cin(p);
-    g.prep = (cin != p->s.c_in || p->dtype == CONV_I8) ? 1 : 0;
     g.cin = cin;
     g.fold = igemm_fold(p) ? 1 : 0;
     g.kw = g.fold ? 1 : p->s.k_w;
@@ -118,14 +118,10 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi) {
     g.wx = g.fold ? p->s.w + 2 * p->pad_w - p->s.k_w + 1 : p->s.w;
     // (a flat tile's pixels have no (oh, ow) structure for the upsample replicas)
     g.flat = (p->s.k_h == 1 && g.kw == 1 && S == 1 && p->pad_h == 0 && g.padw == 0 && p->up == 1) ? 1 : 0;
-    if (g.prep) {
-        // plan-owned bf16 copies of x and w (channels padded to `cin`)
-        const size_t xb = (size_t)p->s.n * p->s.h * g.wx * cin * 2;
-        const size_t wb = (size_t)p->s.c_out * p->s.k_h * g.kw * cin * 2;
-        p->cin_p = cin;
-        if (xb && cudaMalloc(&p->d_xprep, xb) != cudaSuccess) return CONV_ERR_OOM;
-        if (cudaMalloc(&p->d_wprep, wb) != cudaSuccess) return CONV_ERR_OOM;
-    }
+    // int8 operands can be widened in the kernel (CVT variants) where their
+    // channel rows are whole 16-byte TMA units and nothing is folded or padded
+    const bool cvt_ok = p->dtype == CONV_I8 && cin == p->s.c_in && !igemm_fold(p) && !igemm_fused(p);
+    if (widen == 2 && !cvt_ok) return CONV_ERR_UNSUPPORTED;
 
     // Candidates: the tile layout (swapped, Cout <= 128, with 256-pixel
     // tiles; normal with 128-pixel tiles and BN in {256, 128, 64}; the CTA
@@ -154,12 +150,14 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi) {
     if (staging == 2 && !halo_ok) return CONV_ERR_UNSUPPORTED;
     if (epi == 2 && igemm_fused(p)) return CONV_ERR_UNSUPPORTED;  // (no output options per tile)
     struct Cand {
-        int swap, pair, bn, bk, halo, ept, bw, bh, tw, th, wres, stages, out_bufs;
+        int swap, pair, bn, bk, halo, ept, cvt, bw, bh, tw, th, wres, stages, out_bufs;
         long long tiles_m, tiles_n, units, rows;
-        uint32_t a_stage;
+        uint32_t a_stage, raw_stage, raw_region;
     };
-    Cand best{};
-    long long best_cost = -1;
+    // two tracks: int8 widened by the pre-pass (or no widening), and widened
+    // in the kernel; the second wins wherever it has a candidate (see below)
+    Cand bests[2]{};
+    long long best_costs[2] = {-1, -1};
     const int bk_max = cin % 64 == 0 ? 64 : (cin % 32 == 0 ? 32 : 16);
     for (int cand = 0; cand < 6; ++cand) {
         const bool swap = cand == 0;
@@ -208,9 +206,12 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi) {
                         if (cw >= p->ow) break;  // wider tiles only waste more columns
                     }
                 }
-                for (int si = 0; si < nshapes; ++si) {
+                for (int ci = 0; ci < 2 * nshapes; ++ci) {
+                    const int si = ci / 2, cvt = ci % 2;  // cvt: int8 widened in the kernel
+                    if (cvt && (!cvt_ok || swap || pair || bn > 128 || widen == 1)) continue;
+                    if (!cvt && widen == 2) continue;
                     Cand c{};
-                    c.swap = swap; c.pair = pair; c.bn = bn; c.bk = bk; c.halo = halo;
+                    c.swap = swap; c.pair = pair; c.bn = bn; c.bk = bk; c.halo = halo; c.cvt = cvt;
                     c.bw = shapes[si][0]; c.bh = shapes[si][1];
                     if (g.flat) {
                         const long long M = (long long)p->s.n * p->s.h * g.wx;
@@ -226,7 +227,15 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi) {
                     // One epilogue per tile where each CTA gets at least two tiles
                     // (with fewer, slicing every tile's columns over the warpgroups
                     // finishes each tile sooner), or where forced.
-                    c.ept = ept_ok && epi != 1 && (epi == 2 || c.units >= 2LL * p->num_sms) ? 1 : 0;
+                    c.ept = !cvt && ept_ok && epi != 1 && (epi == 2 || c.units >= 2LL * p->num_sms) ? 1 : 0;
+                    if (cvt && epi == 2) continue;
+                    // In-kernel widening where each CTA gets at least four tiles
+                    // (or where forced): every CTA widens the whole weight tensor
+                    // before its first MMA, which a layer of about one tile per
+                    // CTA pays in full (measured: int8 3x3 64->64 @96, 96 tiles,
+                    // 16.1 us against 9.7 with the pre-pass; @160 batch 8, 1600
+                    // tiles, 54.2 against 70.5).
+                    if (cvt && widen != 2 && c.units < 4LL * p->num_sms) continue;
                     // Shared memory: ring stages, resident weights, epilogue
                     // staging.  A halo stage holds the box's (bh + k_h - 1) x bw
                     // pixel rows and, when bh x bw < P, the P - bh x bw rows the
@@ -251,6 +260,21 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi) {
                     const long long stage_bytes = c.a_stage + (c.wres ? 0 : taps * wblock);
                     long long st = (smem_cap - out_bytes - (c.wres ? wall : 0)) / stage_bytes;
                     if (st > 8) st = 8;
+                    if (cvt) {
+                        // resident (widened) weights, and a raw region holding first the
+                        // raw int8 weights, then the raw ring of int8 activation boxes
+                        if (!c.wres) continue;
+                        c.raw_stage = (uint32_t)(((long long)box_rows * bk + 127) / 128 * 128);
+                        const long long wraw = wblocks * bnc * bk;
+                        for (; st >= 2; --st) {
+                            const long long ring = st * (long long)c.raw_stage;
+                            const long long region = ((ring > wraw ? ring : wraw) + 1023) / 1024 * 1024;
+                            if (st * c.a_stage + wall + out_bytes + region + 16 * st <= smem_cap) {
+                                c.raw_region = (uint32_t)region;
+                                break;
+                            }
+                        }
+                    }
                     if (st < 2) continue;
                     c.stages = (int)st;
                     fits = 1;
@@ -273,6 +297,8 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi) {
                     const long long cost = waves * (t_tile + 500);
                     // ties: more work units (more SMs busy), then fewer staged
                     // rows, then the narrower N tile
+                    Cand &best = bests[cvt];
+                    long long &best_cost = best_costs[cvt];
                     const bool better =
                         best_cost < 0 || cost < best_cost ||
                         (cost == best_cost &&
@@ -286,8 +312,24 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi) {
             }
         }
     }
-    if (best_cost < 0) return CONV_ERR_UNSUPPORTED;  // e.g. a forced swapped layout with c_out > 128
+    const int track = best_costs[1] >= 0 ? 1 : 0;
+    if (best_costs[track] < 0) return CONV_ERR_UNSUPPORTED;  // e.g. a forced swapped layout with c_out > 128
+    const Cand &best = bests[track];
     g.swap = best.swap; g.pair = best.pair; g.bn = best.bn; g.bk = best.bk; g.halo = best.halo; g.ept = best.ept;
+    g.cvt = best.cvt;
+    g.raw_stage = (int)best.raw_stage;
+    g.raw_region = (int)best.raw_region;
+    // plan-owned bf16 copies of x and w (channels padded to `cin`), unless the
+    // kernel reads the operands as they are (bf16 with whole rows) or widens
+    // them itself (CVT)
+    g.prep = (cin != p->s.c_in || (p->dtype == CONV_I8 && !g.cvt)) ? 1 : 0;
+    if (g.prep) {
+        const size_t xb = (size_t)p->s.n * p->s.h * g.wx * cin * 2;
+        const size_t wb = (size_t)p->s.c_out * p->s.k_h * g.kw * cin * 2;
+        p->cin_p = cin;
+        if (xb && cudaMalloc(&p->d_xprep, xb) != cudaSuccess) return CONV_ERR_OOM;
+        if (cudaMalloc(&p->d_wprep, wb) != cudaSuccess) return CONV_ERR_OOM;
+    }
     g.cblocks = cin / g.bk;
     const int wblocks = p->s.k_h * g.kw * g.cblocks;
     g.tiles_n = (int)best.tiles_n; g.tiles_m = (int)best.tiles_m;
@@ -301,14 +343,16 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi) {
         const int wblock = bnc * g.bk * 2;
         const int one_buf = g.swap ? 4 * 16 * kTP : epi_groups(g.bn, false, g.ept != 0) * kBM * 64;
         const int weights = g.wres ? wblocks * wblock : g.stages * (g.halo ? 3 : 1) * wblock;
-        g.smem = 1024 + g.stages * g.a_stage + weights + one_buf * g.out_bufs + 8 * (2 * g.stages + 9) + 16;
+        g.smem = 1024 + g.stages * g.a_stage + weights + one_buf * g.out_bufs + (g.cvt ? g.raw_region : 0) +
+                 8 * (g.cvt ? 4 * g.stages + 10 : 2 * g.stages + 9) + 16;
     }
     // Ask for more than half of an SM's shared memory so that no two CTAs of
     // this persistent kernel share an SM: each CTA then owns its TMEM
     // columns (at most 512) without waiting for another to free them.
     if (g.smem < 116 * 1024) g.smem = 116 * 1024;
     if (!tensor_map_encoder()) return CONV_ERR_CUDA;
-    void *kern = select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0, g.pair != 0, igemm_fused(p), g.halo != 0, g.ept != 0);
+    void *kern = select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0, g.pair != 0, igemm_fused(p), g.halo != 0, g.ept != 0,
+                              g.cvt != 0);
     const int rc = conv_grant_smem(kern, p->device, g.smem);
     if (rc != CONV_OK) return rc;
     if (g.pair) {
@@ -316,7 +360,7 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi) {
         // SMs of one GPC), at most one per work unit
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * g.num_tiles);
-        cfg.blockDim = dim3(cta_threads(g.bn, false, g.ept != 0));
+        cfg.blockDim = dim3(cta_threads(g.bn, false, g.ept != 0, g.cvt != 0));
         cfg.dynamicSmemBytes = (size_t)g.smem;
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeClusterDimension;
@@ -332,7 +376,7 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi) {
     }
     snprintf(p->desc, sizeof(p->desc),
              "igemm_%s_tcgen05 %s%s %s BK=%d tile=%dx%d%s stages=%d%s out_bufs=%d%s tiles=%d grid=%d",
-             p->dtype == CONV_I8 ? (g.fold ? "i8-as-bf16-kwfold" : "i8-as-bf16")
+             p->dtype == CONV_I8 ? (g.fold ? "i8-as-bf16-kwfold" : (g.cvt ? "i8-widened-in-kernel" : "i8-as-bf16"))
                                  : (g.fold ? "bf16-cpad-kwfold" : (g.prep ? "bf16-cpad" : "bf16")),
              g.flat ? "flat" : "spatial",
              g.swap ? " swapped" : (g.pair ? " cta-pair" : ""),
@@ -359,35 +403,37 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
     alignas(64) CUtensorMap tmA, tmB;
     const cuuint32_t ones[4] = {1, 1, 1, 1};
     CUresult rc;
+    // CVT: the operands as they are, int8, unswizzled (the converter
+    // warpgroup widens them into the swizzled bf16 layout)
+    const cuuint64_t es = g.cvt ? 1 : 2;
+    const CUtensorMapDataType op_type = g.cvt ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapSwizzle op_swz = g.cvt ? CU_TENSOR_MAP_SWIZZLE_NONE : swizzle_for(g.bk);
     if (g.flat) {
         const cuuint64_t dims[2] = {(cuuint64_t)cin, (cuuint64_t)p->s.n * p->s.h * g.wx};
-        const cuuint64_t strides[1] = {(cuuint64_t)cin * 2};
+        const cuuint64_t strides[1] = {(cuuint64_t)cin * es};
         const cuuint32_t box[2] = {(cuuint32_t)g.bk, (cuuint32_t)(g.swap ? kBMSwap : kBM)};
-        rc = encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims, strides, box, ones,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(g.bk), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        rc = encode(&tmA, op_type, 2, const_cast<void *>(x), dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    op_swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     } else {
         const cuuint64_t dims[4] = {(cuuint64_t)cin, (cuuint64_t)g.wx, (cuuint64_t)p->s.h,
                                     (cuuint64_t)p->s.n};
-        const cuuint64_t strides[3] = {(cuuint64_t)cin * 2, (cuuint64_t)g.wx * cin * 2,
-                                       (cuuint64_t)p->s.h * g.wx * cin * 2};
+        const cuuint64_t strides[3] = {(cuuint64_t)cin * es, (cuuint64_t)g.wx * cin * es,
+                                       (cuuint64_t)p->s.h * g.wx * cin * es};
         // halo staging: the bh + k_h - 1 input rows under the tile (stride 1)
         const cuuint32_t box_h = g.halo ? (cuuint32_t)(g.bh + p->s.k_h - 1) : (cuuint32_t)(g.bh * S);
         const cuuint32_t box[4] = {(cuuint32_t)g.bk, (cuuint32_t)(g.bw * S), box_h, 1};
         const cuuint32_t estr[4] = {1, (cuuint32_t)S, (cuuint32_t)S, 1};
-        rc = encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(x), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(g.bk), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        rc = encode(&tmA, op_type, 4, const_cast<void *>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    op_swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     if (rc != CUDA_SUCCESS) return CONV_ERR_CUDA;
     {
         const cuuint64_t K = (cuuint64_t)p->s.k_h * g.kw * cin;
         const cuuint64_t dims[2] = {K, (cuuint64_t)p->s.c_out};
-        const cuuint64_t strides[1] = {K * 2};
+        const cuuint64_t strides[1] = {K * es};
         const cuuint32_t box[2] = {(cuuint32_t)g.bk, (cuuint32_t)(g.pair ? g.bn / 2 : g.bn)};
-        rc = encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(w), dims, strides, box, ones,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(g.bk), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        rc = encode(&tmB, op_type, 2, const_cast<void *>(w), dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    op_swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (rc != CUDA_SUCCESS) return CONV_ERR_CUDA;
     }
 
@@ -433,8 +479,11 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
     a.num_tiles = g.num_tiles; a.cblocks = g.cblocks; a.kblocks = g.kblocks; a.stages = g.stages;
     a.tiles_m = g.tiles_m;
     a.M = (long long)p->s.n * p->s.h * g.wx;
-    a.a_bytes = (uint32_t)((g.flat ? (g.swap ? kBMSwap : kBM) : g.bw * (g.halo ? g.bh + p->s.k_h - 1 : g.bh)) *
-                           g.bk * 2);
+    const int box_rows = g.flat ? (g.swap ? kBMSwap : kBM) : g.bw * (g.halo ? g.bh + p->s.k_h - 1 : g.bh);
+    a.a_bytes = (uint32_t)(box_rows * g.bk * (int)es);
+    a.box_rows = box_rows;
+    a.raw_stage = (uint32_t)g.raw_stage;
+    a.raw_region = (uint32_t)g.raw_region;
     a.a_stage = (uint32_t)g.a_stage;
     a.halo = g.halo;
     a.wblocks = p->s.k_h * g.kw * g.cblocks;
@@ -451,9 +500,10 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
     a.om.res = res;
     a.status = p->d_status;
 
-    void *k = select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0, g.pair != 0, igemm_fused(p), g.halo != 0, g.ept != 0);
+    void *k = select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0, g.pair != 0, igemm_fused(p), g.halo != 0, g.ept != 0,
+                              g.cvt != 0);
     void *args[] = {&tmA, &tmB, &tmY, &a};
-    const cudaError_t e = conv_launch(k, dim3(g.grid), dim3(cta_threads(g.bn, g.swap != 0, g.ept != 0)), args, (size_t)g.smem, st,
+    const cudaError_t e = conv_launch(k, dim3(g.grid), dim3(cta_threads(g.bn, g.swap != 0, g.ept != 0, g.cvt != 0)), args, (size_t)g.smem, st,
                                       g.pair ? 2 : 1);
     return e == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }

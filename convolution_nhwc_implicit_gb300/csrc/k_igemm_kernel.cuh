@@ -59,9 +59,10 @@ constexpr int kTP = 272;     // swapped-mode transpose rows: 128 bf16 channels +
 __host__ __device__ constexpr int epi_groups(int bn, bool swap, bool ept = false) {
     return (swap || ept) ? 4 : (bn >= 128 ? 4 : 2);
 }
-// Threads per CTA: the TMA warp, the MMA warp and the epilogue warpgroups.
-__host__ __device__ constexpr int cta_threads(int bn, bool swap, bool ept = false) {
-    return 64 + 128 * epi_groups(bn, swap, ept);
+// Threads per CTA: the TMA warp, the MMA warp and the epilogue warpgroups
+// (and, cvt: the converter warpgroup).
+__host__ __device__ constexpr int cta_threads(int bn, bool swap, bool ept = false, bool cvt = false) {
+    return 64 + 128 * epi_groups(bn, swap, ept) + (cvt ? 128 : 0);
 }
 
 struct IgArgs {
@@ -86,6 +87,12 @@ struct IgArgs {
                          //    memory; the ring then holds activations only
     OutMap om;           // output placement (concat slice, 2x upsample) and residual
     int *status;
+    // CVT (int8 operands widened in the kernel): the raw int8 activation part
+    // of a stage (a_bytes of them written by TMA, box_rows pixel rows of BK
+    // bytes), and the raw weights' bytes (loaded once, then widened)
+    uint32_t raw_stage;
+    int box_rows;
+    uint32_t raw_region;  // bytes of the raw region (the raw weights, then the raw ring, share it)
 };
 
 // The output tensor maps of the TMA-store epilogue: one per upsample
@@ -372,13 +379,25 @@ __device__ __forceinline__ void epilogue_swapped_bf16(const IgArgs &a, int tile,
 // goes to each tile's epilogue latency (TMEM load, activation, staging, TMA
 // store), four tiles' epilogues then run at once; and a layer with fewer
 // output channels than BN keeps every warpgroup busy.
-template <int BN, int BK, bool FLAT, bool SWAP, bool PAIR, bool FUSED, bool HALO = false, bool EPT = false>
-__global__ void __launch_bounds__(cta_threads(BN, SWAP, EPT), 1)
+//
+// CVT (int8 layers, normal layout, single CTAs, resident weights): the int8
+// operands are widened to bf16 in the kernel instead of by a pre-pass (no
+// second launch, no bf16 copy in HBM).  TMA brings the raw int8 activation
+// boxes into a raw ring and, once, the raw int8 weights; a converter
+// warpgroup widens each raw stage into the stage's bf16 operand (an int8 is
+// exact in bf16), writing it in the swizzled K-major layout the MMA reads
+// (the 16-byte chunk index XOR the address bits above the row), then fences
+// the writes for the tensor cores and marks the stage full.  The widened
+// weights stay resident.
+template <int BN, int BK, bool FLAT, bool SWAP, bool PAIR, bool FUSED, bool HALO = false, bool EPT = false,
+          bool CVT = false>
+__global__ void __launch_bounds__(cta_threads(BN, SWAP, EPT, CVT), 1)
 igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ YMaps tmY, const IgArgs a) {
     static_assert(!(PAIR && SWAP), "the CTA-pair mode uses the normal layout");
     static_assert(!(HALO && FLAT), "halo staging is for spatial tiles");
     static_assert(!EPT || (!SWAP && !PAIR && BN <= 128), "one epilogue per tile: normal layout, BN <= 128");
+    static_assert(!CVT || (!SWAP && !PAIR && !EPT && !FUSED), "in-kernel widening: plain normal layout");
     constexpr int kPix = SWAP ? kBMSwap : kBM;  // pixel rows of a tile (per CTA)
     constexpr int kAcc = SWAP ? kBMSwap : BN;   // accumulator columns of a tile
     constexpr int kBRows = PAIR ? BN / 2 : BN;  // weight rows this CTA stages
@@ -408,13 +427,19 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const uint32_t sA = base;
     const uint32_t sB = base + stages * aStage;
     const uint32_t sOut = sB + (wres ? (uint32_t)a.wblocks * kBStage : stages * (HALO ? kHaloTaps : 1) * kBStage);
-    const uint32_t sBar = sOut + kGroups * a.out_bufs * kOutStage;
+    const uint32_t sBar = sOut + kGroups * a.out_bufs * kOutStage + (CVT ? a.raw_region : 0u);
     auto full_bar = [&](int s) { return sBar + 8u * s; };
     auto empty_bar = [&](int s) { return sBar + 8u * (stages + s); };
     auto tfull_bar = [&](int b) { return sBar + 8u * (2 * stages + b); };       // b < 4
     auto tempty_bar = [&](int b) { return sBar + 8u * (2 * stages + 4 + b); };
     const uint32_t wres_bar = sBar + 8u * (2 * stages + 8);  // the resident weights have landed
-    uint8_t *gmisc = gbase + (sBar - base) + 8u * (2 * stages + 9);
+    // CVT: the raw region (between the epilogue staging and the barriers),
+    // its ring's barriers, and the raw weights' barrier
+    const uint32_t sRaw = sOut + kGroups * a.out_bufs * kOutStage;
+    auto raw_full_bar = [&](int s) { return sBar + 8u * (2 * stages + 9 + s); };
+    auto raw_empty_bar = [&](int s) { return sBar + 8u * (3 * stages + 9 + s); };
+    const uint32_t wraw_bar = sBar + 8u * (4 * stages + 9);
+    uint8_t *gmisc = gbase + (sBar - base) + 8u * (CVT ? 4 * stages + 10 : 2 * stages + 9);
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(gmisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gmisc + 4);
 
@@ -436,6 +461,13 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             tc::mbar_init(tempty_bar(b), EPT ? 128 : (PAIR ? 2 * 4 * kGroups : 128 * kGroups));
         }
         tc::mbar_init(wres_bar, 1);
+        if constexpr (CVT) {
+            for (int s = 0; s < stages; ++s) {
+                tc::mbar_init(raw_full_bar(s), 1);
+                tc::mbar_init(raw_empty_bar(s), 1);
+            }
+            tc::mbar_init(wraw_bar, 1);
+        }
         *abort_flag = 0;
         tc::fence_mbar_init();
         tc::tma_prefetch_desc(&tmA);
@@ -471,7 +503,21 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             bool ok = true;
             // pair mode: both CTAs' loads complete on the even CTA's barriers
             const uint32_t full0 = PAIR ? tc::mapa_shared(full_bar(0), 0) : full_bar(0);
-            if (wres && unit < a.num_tiles) {
+            if (CVT && unit < a.num_tiles) {
+                // the raw int8 weights into the raw region, once; the converter
+                // widens them into the resident blocks, and only then may the
+                // raw ring (the same memory) be filled
+                tc::mbar_arrive_expect_tx(wraw_bar, (uint32_t)a.wblocks * kBRows * BK);
+                int r = 0, s = 0, cb = 0;
+                for (int kb = 0; kb < a.wblocks; ++kb) {
+                    tc::tma_load_2d(sRaw + (uint32_t)kb * kBRows * BK, &tmB, wraw_bar, (r * a.KW + s) * a.Cin + cb * BK, 0);
+                    if (++cb == a.cblocks) {
+                        cb = 0;
+                        if (++s == a.KW) { s = 0; ++r; }
+                    }
+                }
+                ok = wait_bounded(wres_bar, 0u, abort_flag, a.status, KSTATUS_TIMEOUT_PRODUCER);
+            } else if (wres && unit < a.num_tiles) {
                 // every K block of the (single) N block of weights, once; pair
                 // mode: each CTA its half, both completing on the even CTA's barrier
                 const uint32_t wbar = PAIR ? tc::mapa_shared(wres_bar, 0) : wres_bar;
@@ -504,6 +550,32 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     oh0 = (t2 % a.tiles_h) * a.bh;
                     n = t2 / a.tiles_h;
                     ow0 = tw * a.bw;
+                }
+                if constexpr (CVT) {
+                    // raw int8 activation boxes into the raw ring (per-tap or halo
+                    // boxes, in the K block order of the plain variants)
+                    int r = 0, s = 0, cb = 0;
+                    for (int kb = 0; kb < a.kblocks; ++kb) {
+                        if (!wait_bounded(raw_empty_bar(stage), phase ^ 1u, abort_flag, a.status,
+                                          KSTATUS_TIMEOUT_PRODUCER)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t dR = sRaw + stage * a.raw_stage;
+                        tc::mbar_arrive_expect_tx(raw_full_bar(stage), a.a_bytes);
+                        if (FLAT) {
+                            tc::tma_load_2d(dR, &tmA, raw_full_bar(stage), cb * BK, m0);
+                        } else {
+                            const int c1 = ow0 * a.stride - a.pad_w + s, c2 = oh0 * a.stride - a.pad_h + r;
+                            tc::tma_load_4d(dR, &tmA, raw_full_bar(stage), cb * BK, c1, c2, n);
+                        }
+                        if (++stage == stages) { stage = 0; phase ^= 1u; }
+                        if (++cb == a.cblocks) {
+                            cb = 0;
+                            if (++s == a.KW) { s = 0; if (!HALO) ++r; }
+                        }
+                    }
+                    continue;
                 }
                 if constexpr (HALO) {
                     // K blocks (s, cb), cb fastest: a stage holds the halo box and
@@ -667,6 +739,82 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     else
                         tc::mma_commit(tfull_bar(buf));
                 }
+            }
+        }
+    } else if (CVT && warp >= 2 + 4 * kGroups) {
+        // ------------------------------------------------ converter (the last warpgroup)
+        // int8 -> bf16 (exact) into the swizzled K-major operand: a 16-byte
+        // chunk of 8 bf16 channels, chunk j of row r, goes to chunk
+        // j ^ ((r * row bytes) >> 7 & (chunks - 1)) of the row (the 128-, 64- or
+        // 32-byte swizzle of a 1024-aligned slot).
+        constexpr int kChunks = BK / 8;  // 16-byte bf16 chunks per row
+        const int ct = threadIdx.x - (64 + 128 * kGroups);
+        auto widen = [&](uint32_t src, uint32_t dst, int rows) {
+            for (int idx = ct; idx < rows * kChunks; idx += 128) {
+                const int r = idx / kChunks, j = idx % kChunks;
+                uint32_t lo, hi;  // 8 int8 values
+                asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(lo), "=r"(hi) : "r"(src + (uint32_t)(r * BK + j * 8)));
+                uint32_t o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t wd = e < 2 ? lo : hi;
+                    const int sh = (e & 1) * 16;
+                    const float f0 = (float)(int8_t)(wd >> sh), f1 = (float)(int8_t)(wd >> (sh + 8));
+                    // bf16 of a small integer is its float's upper half, exactly
+                    o[e] = (__float_as_uint(f0) >> 16) | (__float_as_uint(f1) & 0xffff0000u);
+                }
+                const uint32_t sw = (uint32_t)((r * kRowBytes) >> 7) & (uint32_t)(kChunks - 1);
+                const uint32_t d = dst + (uint32_t)(r * kRowBytes) + (((uint32_t)j ^ sw) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d), "r"(o[0]), "r"(o[1]), "r"(o[2]),
+                             "r"(o[3])
+                             : "memory");
+            }
+        };
+        // One thread does the (bounded) waits and tells the others through
+        // shared memory, so that the warpgroup gives up, if it must, as one
+        // (a hardware named barrier has no time limit).
+        volatile int *go = reinterpret_cast<volatile int *>(gmisc + 8);
+        auto all_ok = [&](bool mine) {
+            if (ct == 0) *go = mine ? 1 : 0;
+            tc::named_bar_sync(6, 128);
+            const bool r = *go != 0;
+            tc::named_bar_sync(6, 128);  // everyone has read it before it changes
+            return r;
+        };
+        bool ok = true;
+        if (CVT && unit < a.num_tiles) {
+            // the resident weights: every K block [kBRows x BK], widened once
+            ok = all_ok(ct != 0 || wait_bounded(wraw_bar, 0u, abort_flag, a.status, KSTATUS_TIMEOUT_EPILOGUE));
+            if (ok) {
+                (void)tc::mbar_try_wait(wraw_bar, 0u);  // (complete: each thread's own acquire of the TMA bytes)
+                for (int kb = 0; kb < a.wblocks; ++kb)
+                    widen(sRaw + (uint32_t)kb * kBRows * BK, sB + (uint32_t)kb * kBStage, kBRows);
+                tc::fence_proxy_async_smem();  // the widened weights visible to the tensor cores
+                tc::named_bar_sync(6, 128);
+                if (ct == 0) tc::mbar_arrive(wres_bar);
+            }
+        }
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int tile = unit; tile < a.num_tiles && ok; tile += units) {
+            for (int kb = 0; kb < a.kblocks; ++kb) {
+                // raw stage landed, and its operand slot consumed by the MMAs
+                ok = all_ok(ct != 0 ||
+                            (wait_bounded(raw_full_bar(stage), phase, abort_flag, a.status, KSTATUS_TIMEOUT_EPILOGUE) &&
+                             wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, a.status, KSTATUS_TIMEOUT_EPILOGUE)));
+                if (!ok) break;
+                // (both complete: each thread's own acquire of the TMA bytes and of
+                // the MMAs' release of the slot)
+                (void)tc::mbar_try_wait(raw_full_bar(stage), phase);
+                (void)tc::mbar_try_wait(empty_bar(stage), phase ^ 1u);
+                widen(sRaw + stage * a.raw_stage, sA + stage * aStage, a.box_rows);
+                tc::fence_proxy_async_smem();
+                tc::named_bar_sync(6, 128);  // every converter thread's rows are written
+                if (ct == 0) {
+                    tc::mbar_arrive(raw_empty_bar(stage));
+                    tc::mbar_arrive(full_bar(stage));
+                }
+                if (++stage == stages) { stage = 0; phase ^= 1u; }
             }
         }
     } else {

@@ -125,6 +125,17 @@ typedef enum {
  *             conv_output_t options; CONV_ERR_UNSUPPORTED otherwise). */
 #define CONV_ALGO_EPI_SLICED 0x400
 #define CONV_ALGO_EPI_PER_TILE 0x800
+/* How int8 layers reach the tensor cores (which have no integer MMA on
+ * sm_103a; an int8 value is exact in bf16), OR-ed in the same way (default:
+ * in the kernel where it can, else the pre-pass):
+ *   PREPASS   a pre-pass kernel writes bf16 copies of x and w into plan-owned
+ *             buffers, which the tensor-core kernel reads;
+ *   INKERNEL  the kernel loads the int8 tensors as they are and a converter
+ *             warpgroup widens them in shared memory (normal layouts with
+ *             N <= 128 whose weights stay resident, c_in % 16 == 0, no
+ *             conv_output_t options; CONV_ERR_UNSUPPORTED otherwise). */
+#define CONV_ALGO_WIDEN_PREPASS 0x1000
+#define CONV_ALGO_WIDEN_INKERNEL 0x2000
 
 enum {
     CONV_OK = 0,

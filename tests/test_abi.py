@@ -93,7 +93,9 @@ def _quant(scales, si=0.05, so=0.05):
     ((1, 8, 8, 4, 4, 3, 3), {"algo": 11 | 0x100}, -9),     # staging flag on a bad algo
     ((1, 8, 8, 4, 4, 3, 3), {"algo": 3 | 0xC00}, -9),      # both epilogue flags
     ((1, 8, 8, 4, 4, 3, 3), {"algo": 2 | 0x800}, -9),      # epilogue flag on the depthwise family
-    ((1, 8, 8, 4, 4, 3, 3), {"algo": 3 | 0x1000}, -9),     # an unknown flag bit
+    ((1, 8, 8, 4, 4, 3, 3), {"algo": 3 | 0x4000}, -9),     # an unknown flag bit
+    ((1, 8, 8, 4, 4, 3, 3), {"algo": 3 | 0x3000}, -9),     # both widening flags
+    ((1, 8, 8, 4, 4, 3, 3), {"algo": 1 | 0x2000}, -9),     # widening flag on the direct family
     ((1, 8, 8, 4, 4, 3, 3), {"dtype": 2}, -1),             # int8 without quant
 ])
 def test_invalid_layers_are_named_failures(lib, shape, kw, expect):

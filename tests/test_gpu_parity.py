@@ -152,7 +152,36 @@ IGEMM_I8 = [
 @pytest.mark.parametrize("spec,layout", with_layouts(IGEMM_I8))
 def test_igemm_int8_exact(spec, layout):
     plan = check_layout(spec, layout)
-    assert "i8-as-bf16" in plan.describe()
+    assert "i8-as-bf16" in plan.describe() or "i8-widened-in-kernel" in plan.describe()
+
+
+# int8 operands widened in the kernel (converter warpgroup) or by the
+# pre-pass, forced, on the layers whose rows are whole 16-byte units and
+# whose weights stay resident: bit-identical results either way.
+I8_WIDEN = [s for s in IGEMM_I8 if s.name in ("i8_3x3_64to64_ragged", "i8_3x3_relu_sat", "i8_1x1_32to64",
+                                                "i8_3x3_s2_cin48_pad")]
+
+
+# (N = 128 keeps nine resident 128-row weight blocks, too many for shared
+# memory beside the rings: in the kernel only for the 1x1 layer there)
+@pytest.mark.parametrize("spec,layout", [
+    pytest.param(spec, f"{lay}+{w}", id=f"{spec.name}-{lay}+{w}")
+    for spec in I8_WIDEN for lay in ("igemm", "igemm_n64", "igemm_n128") for w in ("inkernel", "prepass")
+    if not (w == "inkernel" and lay == "igemm_n128" and spec.kh > 1)
+] + [pytest.param(spec, "igemm_n64+halo+inkernel", id=f"{spec.name}-igemm_n64+halo+inkernel")
+     for spec in I8_WIDEN if spec.stride == 1 and spec.kh == 3])
+def test_igemm_int8_widening(spec, layout):
+    plan = check(spec, layout, "igemm")
+    want = "i8-widened-in-kernel" if "inkernel" in layout else "i8-as-bf16"
+    assert want in plan.describe(), plan.describe()
+    assert plan.launches == (1 if "inkernel" in layout else 2)
+
+
+def test_int8_widening_in_kernel_needs_whole_rows():
+    spec = L("i8_cin3_no_cvt", 1, 18, 16, 3, 16, 3, 3, 1, 1, 1, dtype="i8")
+    d = make_layer(spec, torch.Generator("cpu").manual_seed(0))
+    with pytest.raises(RuntimeError, match="UNSUPPORTED"):
+        make_plan(spec, d, "igemm+inkernel")
 
 
 # bf16 layers whose channel rows are too short for TMA: channels padded to 16.
