@@ -625,7 +625,7 @@ def run_e2e(args, layers, plans, dev, stream, total_flops, world):
 # Source files that define each kernel family (a change to any of them voids
 # the DRAM traffic captured for that family).
 _FAMILY_SOURCES = {
-    "igemm": ["k_igemm.cu", "k_igemm_ept.cu", "k_igemm_kernel.cuh", "k_prep.cu", "tc_ptx.cuh", "epilogue.cuh",
+    "igemm": ["k_igemm.cu", "k_igemm_ept.cu", "k_igemm_cvt.cu", "k_igemm_kernel.cuh", "k_prep.cu", "tc_ptx.cuh", "epilogue.cuh",
               "conv_internal.h"],
     "dw3x3+pw1x1": ["k_dwpw.cu", "epilogue.cuh", "conv_internal.h"],
     "dw3x3": ["k_dw3x3.cu", "tc_ptx.cuh", "epilogue.cuh", "conv_internal.h"],

@@ -139,7 +139,7 @@ void *igemm_select_fused(int bn, int bk, bool flat, bool swap, bool pair, bool h
 void *igemm_select_ept(int bn, int bk, bool flat, bool halo);
 // The variant that widens int8 operands in the kernel (normal layout,
 // resident weights, no output options), compiled in its own translation unit.
-void *igemm_select_cvt(int bn, int bk, bool flat, bool halo);
+void *igemm_select_cvt(int mode, int bn, int bk, bool flat, bool halo, bool ept);
 // Fills p->ig and sets kernel attributes; CONV_* status.  layout 0 picks
 // the tile layout by estimated time; 1..6 force swapped, N256, N128, N64,
 // CTA pair (N = 256), CTA pair (N = 128).  staging 0 picks per-tap or halo

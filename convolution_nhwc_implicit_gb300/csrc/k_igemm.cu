@@ -50,10 +50,10 @@ void *kernel_ptr_bk(int bk, bool flat, bool halo) {
     }
 }
 
-void *select_kernel(int bn, int bk, bool flat, bool swap, bool pair, bool fused, bool halo, bool ept, bool cvt) {
+void *select_kernel(int bn, int bk, bool flat, bool swap, bool pair, bool fused, bool halo, bool ept, int cvt) {
     if (fused) return igemm_select_fused(bn, bk, flat, swap, pair, halo);
+    if (cvt) return igemm_select_cvt(cvt, bn, bk, flat, halo, ept);
     if (ept) return igemm_select_ept(bn, bk, flat, halo);
-    if (cvt) return igemm_select_cvt(bn, bk, flat, halo);
     if (pair) return bn == 128 ? kernel_ptr_bk<128, false, true>(bk, flat, halo)
                                : kernel_ptr_bk<256, false, true>(bk, flat, halo);
     if (swap) return kernel_ptr_bk<128, true, false>(bk, flat, halo);
@@ -78,6 +78,14 @@ static bool igemm_fused(const conv_plan *p) { return p->has_res || p->up > 1; }
 static bool igemm_fold(const conv_plan *p) {
     const bool prep = p->dtype == CONV_I8 || p->s.c_in % 16 != 0;
     return prep && p->s.k_w > 1 && p->s.k_w * p->s.c_in <= 16;
+}
+
+// Folded in the kernel: the elements of one input row that a bw-pixel tile
+// row reads, ((bw - 1) x stride + k_w) x Cin, plus up to 7 before them (the
+// box starts on a 16-byte unit), rounded up to whole 16-byte units.
+static int fold_inner(const conv_plan *p, int bw) {
+    const long long e = ((long long)(bw - 1) * p->stride + p->s.k_w) * p->s.c_in + 7;
+    return (int)((e + 7) / 8 * 8);
 }
 
 // Input channels the tensor-core kernel sees: Cin, or Cin (k_w x Cin when
@@ -118,9 +126,17 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
     g.wx = g.fold ? p->s.w + 2 * p->pad_w - p->s.k_w + 1 : p->s.w;
     // (a flat tile's pixels have no (oh, ow) structure for the upsample replicas)
     g.flat = (p->s.k_h == 1 && g.kw == 1 && S == 1 && p->pad_h == 0 && g.padw == 0 && p->up == 1) ? 1 : 0;
-    // int8 operands can be widened in the kernel (CVT variants) where their
-    // channel rows are whole 16-byte TMA units and nothing is folded or padded
-    const bool cvt_ok = p->dtype == CONV_I8 && cin == p->s.c_in && !igemm_fold(p) && !igemm_fused(p);
+    // The converter warpgroup (CVT variants) builds the bf16 operand in the
+    // kernel: int8 operands widened, where their channel rows are whole
+    // 16-byte TMA units and nothing is folded or padded (mode 1); or a bf16
+    // k_w-folded stem assembled from the plain NHWC rows, where an image row
+    // is a whole number of 16-byte units (mode 2).
+    const int cvt_mode =
+        igemm_fused(p) ? 0
+        : (p->dtype == CONV_I8 && cin == p->s.c_in && !g.fold) ? 1
+        : (p->dtype == CONV_BF16 && g.fold && !g.flat && (long long)p->s.w * p->s.c_in * 2 % 16 == 0) ? 2
+                                                                                                      : 0;
+    const bool cvt_ok = cvt_mode != 0;
     if (widen == 2 && !cvt_ok) return CONV_ERR_UNSUPPORTED;
 
     // Candidates: the tile layout (swapped, Cout <= 128, with 256-pixel
@@ -227,15 +243,16 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
                     // One epilogue per tile where each CTA gets at least two tiles
                     // (with fewer, slicing every tile's columns over the warpgroups
                     // finishes each tile sooner), or where forced.
-                    c.ept = !cvt && ept_ok && epi != 1 && (epi == 2 || c.units >= 2LL * p->num_sms) ? 1 : 0;
-                    if (cvt && epi == 2) continue;
+                    c.ept = (!cvt || cvt_mode == 2) && ept_ok && epi != 1 && (epi == 2 || c.units >= 2LL * p->num_sms)
+                                ? 1 : 0;
+                    if (cvt && cvt_mode == 1 && epi == 2) continue;
                     // In-kernel widening where each CTA gets at least four tiles
                     // (or where forced): every CTA widens the whole weight tensor
                     // before its first MMA, which a layer of about one tile per
                     // CTA pays in full (measured: int8 3x3 64->64 @96, 96 tiles,
                     // 16.1 us against 9.7 with the pre-pass; @160 batch 8, 1600
                     // tiles, 54.2 against 70.5).
-                    if (cvt && widen != 2 && c.units < 4LL * p->num_sms) continue;
+                    if (cvt && cvt_mode == 1 && widen != 2 && c.units < 4LL * p->num_sms) continue;
                     // Shared memory: ring stages, resident weights, epilogue
                     // staging.  A halo stage holds the box's (bh + k_h - 1) x bw
                     // pixel rows and, when bh x bw < P, the P - bh x bw rows the
@@ -262,10 +279,23 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
                     if (st > 8) st = 8;
                     if (cvt) {
                         // resident (widened) weights, and a raw region holding first the
-                        // raw int8 weights, then the raw ring of int8 activation boxes
+                        // raw int8 weights, then the raw ring of int8 activation boxes;
+                        // folded: first the raw bf16 weights (and a word of slack), then
+                        // the raw ring of image-row boxes, each box row the
+                        // ((bw - 1) x stride + k_w) x Cin elements under the tile from
+                        // the 16-byte unit at or before its first, at most 256
                         if (!c.wres) continue;
-                        c.raw_stage = (uint32_t)(((long long)box_rows * bk + 127) / 128 * 128);
-                        const long long wraw = wblocks * bnc * bk;
+                        long long wraw = wblocks * bnc * bk;
+                        if (cvt_mode == 2) {
+                            const int inner = fold_inner(p, c.bw);
+                            if (inner > 256) continue;
+                            const int rrows = halo ? hrows : c.bh;
+                            // (36 bytes of slack: the converter reads nine whole words per row)
+                            c.raw_stage = (uint32_t)(((long long)inner * rrows * 2 + 36 + 127) / 128 * 128);
+                            wraw = (long long)p->s.c_out * p->s.k_h * p->s.k_w * p->s.c_in * 2 + 36;
+                        } else {
+                            c.raw_stage = (uint32_t)(((long long)box_rows * bk + 127) / 128 * 128);
+                        }
                         for (; st >= 2; --st) {
                             const long long ring = st * (long long)c.raw_stage;
                             const long long region = ((ring > wraw ? ring : wraw) + 1023) / 1024 * 1024;
@@ -322,7 +352,8 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
     // plan-owned bf16 copies of x and w (channels padded to `cin`), unless the
     // kernel reads the operands as they are (bf16 with whole rows) or widens
     // them itself (CVT)
-    g.prep = (cin != p->s.c_in || (p->dtype == CONV_I8 && !g.cvt)) ? 1 : 0;
+    g.cvt = g.cvt ? cvt_mode : 0;
+    g.prep = !g.cvt && (cin != p->s.c_in || p->dtype == CONV_I8) ? 1 : 0;
     if (g.prep) {
         const size_t xb = (size_t)p->s.n * p->s.h * g.wx * cin * 2;
         const size_t wb = (size_t)p->s.c_out * p->s.k_h * g.kw * cin * 2;
@@ -352,7 +383,7 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
     if (g.smem < 116 * 1024) g.smem = 116 * 1024;
     if (!tensor_map_encoder()) return CONV_ERR_CUDA;
     void *kern = select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0, g.pair != 0, igemm_fused(p), g.halo != 0, g.ept != 0,
-                              g.cvt != 0);
+                              g.cvt);
     const int rc = conv_grant_smem(kern, p->device, g.smem);
     if (rc != CONV_OK) return rc;
     if (g.pair) {
@@ -377,7 +408,8 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
     snprintf(p->desc, sizeof(p->desc),
              "igemm_%s_tcgen05 %s%s %s BK=%d tile=%dx%d%s stages=%d%s out_bufs=%d%s tiles=%d grid=%d",
              p->dtype == CONV_I8 ? (g.fold ? "i8-as-bf16-kwfold" : (g.cvt ? "i8-widened-in-kernel" : "i8-as-bf16"))
-                                 : (g.fold ? "bf16-cpad-kwfold" : (g.prep ? "bf16-cpad" : "bf16")),
+                                 : (g.fold ? (g.cvt ? "bf16-kwfold-in-kernel" : "bf16-cpad-kwfold")
+                                           : (g.prep ? "bf16-cpad" : "bf16")),
              g.flat ? "flat" : "spatial",
              g.swap ? " swapped" : (g.pair ? " cta-pair" : ""),
              g.swap ? "M=128co N=256px"
@@ -405,10 +437,23 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
     CUresult rc;
     // CVT: the operands as they are, int8, unswizzled (the converter
     // warpgroup widens them into the swizzled bf16 layout)
-    const cuuint64_t es = g.cvt ? 1 : 2;
-    const CUtensorMapDataType op_type = g.cvt ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const cuuint64_t es = g.cvt == 1 ? 1 : 2;
+    const CUtensorMapDataType op_type = g.cvt == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const CUtensorMapSwizzle op_swz = g.cvt ? CU_TENSOR_MAP_SWIZZLE_NONE : swizzle_for(g.bk);
-    if (g.flat) {
+    const int inner = g.cvt == 2 ? fold_inner(p, g.bw) : 0;
+    if (g.cvt == 2) {
+        // folded in the kernel: x as [N][H][W x Cin] element rows; a box is
+        // `inner` elements of the tile's input rows (every stride-th row per
+        // tap, or the bh + k_h - 1 rows of a halo box)
+        const cuuint64_t row = (cuuint64_t)p->s.w * p->s.c_in;
+        const cuuint64_t dims[3] = {row, (cuuint64_t)p->s.h, (cuuint64_t)p->s.n};
+        const cuuint64_t strides[2] = {row * 2, (cuuint64_t)p->s.h * row * 2};
+        const cuuint32_t box[3] = {(cuuint32_t)inner,
+                                   g.halo ? (cuuint32_t)(g.bh + p->s.k_h - 1) : (cuuint32_t)(g.bh * S), 1};
+        const cuuint32_t estr[3] = {1, g.halo ? 1u : (cuuint32_t)S, 1};
+        rc = encode(&tmA, op_type, 3, const_cast<void *>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    op_swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else if (g.flat) {
         const cuuint64_t dims[2] = {(cuuint64_t)cin, (cuuint64_t)p->s.n * p->s.h * g.wx};
         const cuuint64_t strides[1] = {(cuuint64_t)cin * es};
         const cuuint32_t box[2] = {(cuuint32_t)g.bk, (cuuint32_t)(g.swap ? kBMSwap : kBM)};
@@ -427,7 +472,17 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
                     op_swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     if (rc != CUDA_SUCCESS) return CONV_ERR_CUDA;
-    {
+    if (g.cvt == 2) {
+        // (the converter reads the weights from global memory; a valid map of
+        // x's first 16 bytes stands in for the unused weight map)
+        const cuuint64_t dims[2] = {8, 1};
+        const cuuint64_t strides[1] = {16};
+        const cuuint32_t box[2] = {8, 1};
+        rc = encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims, strides, box, ones,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (rc != CUDA_SUCCESS) return CONV_ERR_CUDA;
+    } else {
         const cuuint64_t K = (cuuint64_t)p->s.k_h * g.kw * cin;
         const cuuint64_t dims[2] = {K, (cuuint64_t)p->s.c_out};
         const cuuint64_t strides[1] = {K * es};
@@ -480,8 +535,11 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
     a.tiles_m = g.tiles_m;
     a.M = (long long)p->s.n * p->s.h * g.wx;
     const int box_rows = g.flat ? (g.swap ? kBMSwap : kBM) : g.bw * (g.halo ? g.bh + p->s.k_h - 1 : g.bh);
-    a.a_bytes = (uint32_t)(box_rows * g.bk * (int)es);
+    a.a_bytes = g.cvt == 2 ? (uint32_t)(inner * (g.halo ? g.bh + p->s.k_h - 1 : g.bh) * 2)
+                           : (uint32_t)(box_rows * g.bk * (int)es);
     a.box_rows = box_rows;
+    a.fold_cin = p->s.c_in; a.fold_kw = p->s.k_w; a.fold_padw = p->pad_w; a.raw_inner = inner;
+    a.w_raw = static_cast<const __nv_bfloat16 *>(w);
     a.raw_stage = (uint32_t)g.raw_stage;
     a.raw_region = (uint32_t)g.raw_region;
     a.a_stage = (uint32_t)g.a_stage;
@@ -501,7 +559,7 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
     a.status = p->d_status;
 
     void *k = select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0, g.pair != 0, igemm_fused(p), g.halo != 0, g.ept != 0,
-                              g.cvt != 0);
+                              g.cvt);
     void *args[] = {&tmA, &tmB, &tmY, &a};
     const cudaError_t e = conv_launch(k, dim3(g.grid), dim3(cta_threads(g.bn, g.swap != 0, g.ept != 0, g.cvt != 0)), args, (size_t)g.smem, st,
                                       g.pair ? 2 : 1);

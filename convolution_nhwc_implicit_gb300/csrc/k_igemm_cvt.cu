@@ -1,31 +1,43 @@
-// The variants of the tcgen05 implicit-GEMM kernel that widen int8 operands
-// in the kernel (normal layout with N <= 128, resident weights, no output
-// options): a
-// translation unit of its own so that it compiles in parallel with the others.
+// The variants of the tcgen05 implicit-GEMM kernel with a converter
+// warpgroup (normal layout with N <= 128, resident weights, no output
+// options): int8 operands widened in the kernel, and the k_w-folded
+// small-channel bf16 stem assembled in the kernel.  A translation unit of
+// its own so that it compiles in parallel with the others.
 #include "k_igemm_kernel.cuh"
 
 namespace {
 
 template <int BN, int BK>
-void *cvt_ptr(bool flat, bool halo) {
+void *widen_ptr(bool flat, bool halo) {
     if (flat)
-        return reinterpret_cast<void *>(&igemm_bf16_kernel<BN, BK, true, false, false, false, false, false, true>);
+        return reinterpret_cast<void *>(&igemm_bf16_kernel<BN, BK, true, false, false, false, false, false, 1>);
     if (halo)
-        return reinterpret_cast<void *>(&igemm_bf16_kernel<BN, BK, false, false, false, false, true, false, true>);
-    return reinterpret_cast<void *>(&igemm_bf16_kernel<BN, BK, false, false, false, false, false, false, true>);
+        return reinterpret_cast<void *>(&igemm_bf16_kernel<BN, BK, false, false, false, false, true, false, 1>);
+    return reinterpret_cast<void *>(&igemm_bf16_kernel<BN, BK, false, false, false, false, false, false, 1>);
 }
 
 template <int BN>
-void *cvt_bk(int bk, bool flat, bool halo) {
+void *widen_bk(int bk, bool flat, bool halo) {
     switch (bk) {
-    case 64: return cvt_ptr<BN, 64>(flat, halo);
-    case 32: return cvt_ptr<BN, 32>(flat, halo);
-    default: return cvt_ptr<BN, 16>(flat, halo);
+    case 64: return widen_ptr<BN, 64>(flat, halo);
+    case 32: return widen_ptr<BN, 32>(flat, halo);
+    default: return widen_ptr<BN, 16>(flat, halo);
     }
+}
+
+// (the folded operand is one 16-channel K block per filter row: BK = 16, spatial)
+template <int BN>
+void *fold_ptr(bool halo, bool ept) {
+    if (halo)
+        return ept ? reinterpret_cast<void *>(&igemm_bf16_kernel<BN, 16, false, false, false, false, true, true, 2>)
+                   : reinterpret_cast<void *>(&igemm_bf16_kernel<BN, 16, false, false, false, false, true, false, 2>);
+    return ept ? reinterpret_cast<void *>(&igemm_bf16_kernel<BN, 16, false, false, false, false, false, true, 2>)
+               : reinterpret_cast<void *>(&igemm_bf16_kernel<BN, 16, false, false, false, false, false, false, 2>);
 }
 
 }  // namespace
 
-void *igemm_select_cvt(int bn, int bk, bool flat, bool halo) {
-    return bn == 128 ? cvt_bk<128>(bk, flat, halo) : cvt_bk<64>(bk, flat, halo);
+void *igemm_select_cvt(int mode, int bn, int bk, bool flat, bool halo, bool ept) {
+    if (mode == 2) return bn == 128 ? fold_ptr<128>(halo, ept) : fold_ptr<64>(halo, ept);
+    return bn == 128 ? widen_bk<128>(bk, flat, halo) : widen_bk<64>(bk, flat, halo);
 }

@@ -93,6 +93,10 @@ struct IgArgs {
     uint32_t raw_stage;
     int box_rows;
     uint32_t raw_region;  // bytes of the raw region (the raw weights, then the raw ring, share it)
+    // CVT == 2 (small-Cin bf16 layers folded in the kernel): the layer's own
+    // Cin, k_w and pad_w, the bf16 elements of a raw box row, and the weights
+    int fold_cin, fold_kw, fold_padw, raw_inner;
+    const __nv_bfloat16 *w_raw;
 };
 
 // The output tensor maps of the TMA-store epilogue: one per upsample
@@ -380,24 +384,35 @@ __device__ __forceinline__ void epilogue_swapped_bf16(const IgArgs &a, int tile,
 // store), four tiles' epilogues then run at once; and a layer with fewer
 // output channels than BN keeps every warpgroup busy.
 //
-// CVT (int8 layers, normal layout, single CTAs, resident weights): the int8
-// operands are widened to bf16 in the kernel instead of by a pre-pass (no
-// second launch, no bf16 copy in HBM).  TMA brings the raw int8 activation
-// boxes into a raw ring and, once, the raw int8 weights; a converter
-// warpgroup widens each raw stage into the stage's bf16 operand (an int8 is
-// exact in bf16), writing it in the swizzled K-major layout the MMA reads
-// (the 16-byte chunk index XOR the address bits above the row), then fences
-// the writes for the tensor cores and marks the stage full.  The widened
-// weights stay resident.
+// CVT == 1 (int8 layers, normal layout, single CTAs, resident weights): the
+// int8 operands are widened to bf16 in the kernel instead of by a pre-pass
+// (no second launch, no bf16 copy in HBM).  TMA brings the raw int8
+// activation boxes into a raw ring and, once, the raw int8 weights; a
+// converter warpgroup widens each raw stage into the stage's bf16 operand (an
+// int8 is exact in bf16), writing it in the swizzled K-major layout the MMA
+// reads (the 16-byte chunk index XOR the address bits above the row), then
+// fences the writes for the tensor cores and marks the stage full.  The
+// widened weights stay resident.
+// CVT == 2 (bf16 layers with k_w * Cin <= 16, the image stem; BK = 16): the
+// k_w taps are folded into 16 channels in the kernel instead of by a
+// pre-pass.  A raw box is a run of each input row's elements (W * Cin per
+// row, pixels contiguous) from an 8-element boundary at or before the tile's
+// first tap (TMA reads zeros outside the row and the image: the padding);
+// the converter writes, for each pixel of the stage, the k_w * Cin values
+// starting at its first tap and zeros up to 16, as one 32-byte operand row.
+// The raw weights arrive once by a bulk copy into the raw region, and the
+// converter writes the folded resident blocks from them (each (co, r) row's
+// k_w * Cin values, zero-padded) before the raw ring reuses that memory.
 template <int BN, int BK, bool FLAT, bool SWAP, bool PAIR, bool FUSED, bool HALO = false, bool EPT = false,
-          bool CVT = false>
+          int CVT = 0>
 __global__ void __launch_bounds__(cta_threads(BN, SWAP, EPT, CVT), 1)
 igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ YMaps tmY, const IgArgs a) {
     static_assert(!(PAIR && SWAP), "the CTA-pair mode uses the normal layout");
     static_assert(!(HALO && FLAT), "halo staging is for spatial tiles");
     static_assert(!EPT || (!SWAP && !PAIR && BN <= 128), "one epilogue per tile: normal layout, BN <= 128");
-    static_assert(!CVT || (!SWAP && !PAIR && !EPT && !FUSED), "in-kernel widening: plain normal layout");
+    static_assert(!CVT || (!SWAP && !PAIR && !FUSED && (CVT == 2 || !EPT)), "in-kernel widening: normal layout");
+    static_assert(CVT != 2 || (BK == 16 && !FLAT), "in-kernel fold: 16-channel rows of spatial tiles");
     constexpr int kPix = SWAP ? kBMSwap : kBM;  // pixel rows of a tile (per CTA)
     constexpr int kAcc = SWAP ? kBMSwap : BN;   // accumulator columns of a tile
     constexpr int kBRows = PAIR ? BN / 2 : BN;  // weight rows this CTA stages
@@ -452,7 +467,8 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
-            tc::mbar_init(full_bar(s), 1);
+            // (CVT: filled by the four converter warps, each for its own rows)
+            tc::mbar_init(full_bar(s), CVT ? 4 : 1);
             tc::mbar_init(empty_bar(s), 1);
         }
         for (int b = 0; b < kBufs; ++b) {
@@ -464,7 +480,7 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         if constexpr (CVT) {
             for (int s = 0; s < stages; ++s) {
                 tc::mbar_init(raw_full_bar(s), 1);
-                tc::mbar_init(raw_empty_bar(s), 1);
+                tc::mbar_init(raw_empty_bar(s), 4);
             }
             tc::mbar_init(wraw_bar, 1);
         }
@@ -503,7 +519,15 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             bool ok = true;
             // pair mode: both CTAs' loads complete on the even CTA's barriers
             const uint32_t full0 = PAIR ? tc::mapa_shared(full_bar(0), 0) : full_bar(0);
-            if (CVT && unit < a.num_tiles) {
+            if (CVT == 2 && unit < a.num_tiles) {
+                // the raw weights [Cout][k_h][k_w x Cin] into the raw region, as
+                // they are (one bulk copy); the converter folds them into the
+                // resident blocks, and only then may the raw ring be filled
+                const uint32_t wbytes = (uint32_t)(a.Cout * a.KH * a.fold_kw * a.fold_cin * 2);
+                tc::mbar_arrive_expect_tx(wraw_bar, wbytes);
+                tc::bulk_load(sRaw, a.w_raw, wbytes, wraw_bar);
+                ok = wait_bounded(wres_bar, 0u, abort_flag, a.status, KSTATUS_TIMEOUT_PRODUCER);
+            } else if (CVT == 1 && unit < a.num_tiles) {
                 // the raw int8 weights into the raw region, once; the converter
                 // widens them into the resident blocks, and only then may the
                 // raw ring (the same memory) be filled
@@ -563,7 +587,14 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         }
                         const uint32_t dR = sRaw + stage * a.raw_stage;
                         tc::mbar_arrive_expect_tx(raw_full_bar(stage), a.a_bytes);
-                        if (FLAT) {
+                        if (CVT == 2) {
+                            // the input rows' element runs from the 8-element boundary at
+                            // or before the tile's first tap (16-byte aligned start)
+                            const int v = (ow0 * a.stride - a.fold_padw) * a.fold_cin;
+                            const int x0 = v >= 0 ? (v & ~7) : -((-v + 7) & ~7);
+                            const int c2 = HALO ? oh0 - a.pad_h : oh0 * a.stride - a.pad_h + r;
+                            tc::tma_load_3d(dR, &tmA, raw_full_bar(stage), x0, c2, n);
+                        } else if (FLAT) {
                             tc::tma_load_2d(dR, &tmA, raw_full_bar(stage), cb * BK, m0);
                         } else {
                             const int c1 = ow0 * a.stride - a.pad_w + s, c2 = oh0 * a.stride - a.pad_h + r;
@@ -782,7 +813,62 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             return r;
         };
         bool ok = true;
-        if (CVT && unit < a.num_tiles) {
+        // CVT == 2: folded operand row m (16 bf16, two 16-byte chunks) from the
+        // k_w x Cin consecutive bf16 at element e of the shared buffer `src`,
+        // then zeros: nine 32-bit words from the one holding element e (the
+        // buffers have 36 bytes of slack after their last row), realigned by
+        // a funnel shift, the elements past k_w x Cin masked
+        const int kwc = CVT == 2 ? a.fold_kw * a.fold_cin : 0;
+        auto fold_load = [&](uint32_t src, int e, uint32_t (&w)[9]) {
+            const uint32_t wa = src + (uint32_t)(e & ~1) * 2u;
+#pragma unroll
+            for (int k = 0; k < 9; ++k)
+                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w[k]) : "r"(wa + 4u * k) : "memory");
+        };
+        // (output word i keeps its elements 2i, 2i + 1 below k_w x Cin)
+        uint32_t keep[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) keep[i] = 2 * i + 1 < kwc ? 0xffffffffu : (2 * i < kwc ? 0xffffu : 0u);
+        auto fold_store = [&](const uint32_t (&w)[9], int e, uint32_t dst, int m) {
+            const uint32_t sh = (uint32_t)(e & 1) * 16u;  // an odd first element: shift by one
+            uint32_t o[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[i] = __funnelshift_r(w[i], w[i + 1], sh) & keep[i];
+            const uint32_t sw = (uint32_t)((m * kRowBytes) >> 7) & (uint32_t)(kChunks - 1);
+            const uint32_t d = dst + (uint32_t)(m * kRowBytes);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d + ((0u ^ sw) << 4)), "r"(o[0]), "r"(o[1]),
+                         "r"(o[2]), "r"(o[3])
+                         : "memory");
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d + ((1u ^ sw) << 4)), "r"(o[4]), "r"(o[5]),
+                         "r"(o[6]), "r"(o[7])
+                         : "memory");
+        };
+        auto fold_row = [&](uint32_t src, int e, uint32_t dst, int m) {
+            uint32_t w[9];
+            fold_load(src, e, w);
+            fold_store(w, e, dst, m);
+        };
+        if (CVT == 2 && unit < a.num_tiles) {
+            // the folded weights: row co of K block r holds w[co][r][s][ci] at
+            // s * Cin + ci (zero past k_w x Cin and for co >= Cout)
+            ok = all_ok(ct != 0 || wait_bounded(wraw_bar, 0u, abort_flag, a.status, KSTATUS_TIMEOUT_EPILOGUE));
+            if (ok) {
+                (void)tc::mbar_try_wait(wraw_bar, 0u);  // (complete: each thread's own acquire of the bytes)
+                for (int idx = ct; idx < a.wblocks * kBRows; idx += 128) {
+                    const int kb = idx / kBRows, co = idx - kb * kBRows;
+                    if (co < a.Cout) {
+                        fold_row(sRaw, (co * a.KH + kb) * kwc, sB + (uint32_t)kb * kBStage, co);
+                    } else {
+                        const uint32_t d = sB + (uint32_t)kb * kBStage + (uint32_t)(co * kRowBytes);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(d), "r"(0u) : "memory");
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(d + 16u), "r"(0u) : "memory");
+                    }
+                }
+                tc::fence_proxy_async_smem();  // the folded weights visible to the tensor cores
+                tc::named_bar_sync(6, 128);
+                if (ct == 0) tc::mbar_arrive(wres_bar);
+            }
+        } else if (CVT == 1 && unit < a.num_tiles) {
             // the resident weights: every K block [kBRows x BK], widened once
             ok = all_ok(ct != 0 || wait_bounded(wraw_bar, 0u, abort_flag, a.status, KSTATUS_TIMEOUT_EPILOGUE));
             if (ok) {
@@ -794,23 +880,72 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 if (ct == 0) tc::mbar_arrive(wres_bar);
             }
         }
+        // CVT == 2: this thread's box rows m = ct + 128 i (at most three: a box
+        // has at most 128 + 2 bw <= 384 rows), pixel (m / bw, m % bw), whose taps
+        // start at element (m / bw) x raw_inner + (m % bw) x stride x Cin + e0
+        // of the raw stage; e0 = (tile column x bw x stride - pad_w) x Cin mod 8
+        // (the producer starts the box on the 8-element boundary at or below).
+        int roff[3] = {0, 0, 0};
+        int nrows = 0;
+        int tw = 0, nb = 0, dn = 0, dw = 0;
+        const int e_col = CVT == 2 ? a.bw * a.stride * a.fold_cin : 0, e_pad = CVT == 2 ? a.fold_padw * a.fold_cin : 0;
+        if constexpr (CVT == 2) {
+#pragma unroll
+            for (int i = 0; i < 3; ++i) {
+                const int m = ct + 128 * i;
+                if (m < a.box_rows) {
+                    roff[i] = (m / a.bw) * a.raw_inner + (m % a.bw) * a.stride * a.fold_cin;
+                    nrows = i + 1;
+                }
+            }
+            // the CTA's tiles tile = unit + k units: their N block and tile column,
+            // advanced without division
+            nb = unit % a.tiles_n;
+            tw = (unit / a.tiles_n) % a.tiles_w;
+            dn = units % a.tiles_n;
+            dw = (units / a.tiles_n) % a.tiles_w;
+        }
+        // The ring: each converter warp waits for the stage on its own (every
+        // lane, bounded), converts its own rows (those of its lanes' thread
+        // indices), and hands them on with one arrival per warp on the
+        // raw-empty and full barriers (four each), so that the warps run
+        // independently of one another.
+        const int cl = ct & 31;
         int stage = 0;
         uint32_t phase = 0;
         for (int tile = unit; tile < a.num_tiles && ok; tile += units) {
+            const int e0 = (tw * e_col - e_pad) & 7;
+            if constexpr (CVT == 2) {
+                nb += dn;
+                const int carry = nb >= a.tiles_n ? 1 : 0;
+                nb -= carry * a.tiles_n;
+                tw += dw + carry;
+                if (tw >= a.tiles_w) tw -= a.tiles_w;
+            }
             for (int kb = 0; kb < a.kblocks; ++kb) {
                 // raw stage landed, and its operand slot consumed by the MMAs
-                ok = all_ok(ct != 0 ||
-                            (wait_bounded(raw_full_bar(stage), phase, abort_flag, a.status, KSTATUS_TIMEOUT_EPILOGUE) &&
-                             wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, a.status, KSTATUS_TIMEOUT_EPILOGUE)));
+                // (each lane's own acquire of the TMA bytes and of the slot)
+                const bool got =
+                    wait_bounded(raw_full_bar(stage), phase, abort_flag, a.status, KSTATUS_TIMEOUT_EPILOGUE) &&
+                    wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, a.status, KSTATUS_TIMEOUT_EPILOGUE);
+                ok = __all_sync(0xffffffffu, got);
                 if (!ok) break;
-                // (both complete: each thread's own acquire of the TMA bytes and of
-                // the MMAs' release of the slot)
-                (void)tc::mbar_try_wait(raw_full_bar(stage), phase);
-                (void)tc::mbar_try_wait(empty_bar(stage), phase ^ 1u);
-                widen(sRaw + stage * a.raw_stage, sA + stage * aStage, a.box_rows);
+                if constexpr (CVT == 2) {
+                    // (every row's loads issued before the first row's stores)
+                    const uint32_t rw = sRaw + stage * a.raw_stage, dA = sA + stage * aStage;
+                    uint32_t w0[9], w1[9], w2[9];
+                    if (nrows > 0) fold_load(rw, roff[0] + e0, w0);
+                    if (nrows > 1) fold_load(rw, roff[1] + e0, w1);
+                    if (nrows > 2) fold_load(rw, roff[2] + e0, w2);
+                    if (nrows > 0) fold_store(w0, roff[0] + e0, dA, ct);
+                    if (nrows > 1) fold_store(w1, roff[1] + e0, dA, ct + 128);
+                    if (nrows > 2) fold_store(w2, roff[2] + e0, dA, ct + 256);
+                } else {
+                    widen(sRaw + stage * a.raw_stage, sA + stage * aStage, a.box_rows);
+                }
                 tc::fence_proxy_async_smem();
-                tc::named_bar_sync(6, 128);  // every converter thread's rows are written
-                if (ct == 0) {
+                __syncwarp();  // the warp's rows are written
+                if (cl == 0) {
                     tc::mbar_arrive(raw_empty_bar(stage));
                     tc::mbar_arrive(full_bar(stage));
                 }

@@ -125,15 +125,20 @@ typedef enum {
  *             conv_output_t options; CONV_ERR_UNSUPPORTED otherwise). */
 #define CONV_ALGO_EPI_SLICED 0x400
 #define CONV_ALGO_EPI_PER_TILE 0x800
-/* How int8 layers reach the tensor cores (which have no integer MMA on
- * sm_103a; an int8 value is exact in bf16), OR-ed in the same way (default:
- * in the kernel where it can, else the pre-pass):
- *   PREPASS   a pre-pass kernel writes bf16 copies of x and w into plan-owned
- *             buffers, which the tensor-core kernel reads;
- *   INKERNEL  the kernel loads the int8 tensors as they are and a converter
- *             warpgroup widens them in shared memory (normal layouts with
- *             N <= 128 whose weights stay resident, c_in % 16 == 0, no
- *             conv_output_t options; CONV_ERR_UNSUPPORTED otherwise). */
+/* How operands that the tensor cores cannot read as they are reach them,
+ * OR-ed in the same way (default: in the kernel where it can, else the
+ * pre-pass).  These are int8 layers (sm_103a has no integer MMA; an int8
+ * value is exact in bf16) and bf16 layers with k_w x c_in <= 16 (the image
+ * stem), whose k_w taps are folded into one 16-channel operand row:
+ *   PREPASS   a pre-pass kernel writes bf16 copies of x and w (widened,
+ *             channel-padded or folded) into plan-owned buffers, which the
+ *             tensor-core kernel reads;
+ *   INKERNEL  the kernel loads x as it is and a converter warpgroup builds
+ *             the bf16 operand in shared memory: int8 widened (c_in % 16 ==
+ *             0), or the folded rows assembled from the plain NHWC image rows
+ *             (bf16, w x c_in x 2 a multiple of 16 bytes).  Normal layouts
+ *             with N <= 128 whose weights stay resident, no conv_output_t
+ *             options; CONV_ERR_UNSUPPORTED otherwise. */
 #define CONV_ALGO_WIDEN_PREPASS 0x1000
 #define CONV_ALGO_WIDEN_INKERNEL 0x2000
 

@@ -184,6 +184,42 @@ def test_int8_widening_in_kernel_needs_whole_rows():
         make_plan(spec, d, "igemm+inkernel")
 
 
+# bf16 layers with k_w x Cin <= 16 whose image rows are whole 16-byte units:
+# the folded operand assembled in the kernel (converter warpgroup) from the
+# plain NHWC rows, forced, against the folding pre-pass; both must match the
+# oracle.  Ragged heights and widths, stride 2, padding wider than k_w / 2,
+# one input channel, k_h = 5 and 10.
+FOLD_INKERNEL = [
+    L("fold_stem_cin3_ragged_h", 2, 37, 48, 3, 32, 3, 3, 1, 1, 1),
+    L("fold_stem_cin3_s2", 1, 41, 64, 3, 32, 3, 3, 2, 1, 1, act="relu"),
+    L("fold_cin4_cout48", 1, 23, 20, 4, 48, 3, 3, 1, 1, 1, act="none"),
+    L("fold_cin5_s2_overpad_w", 1, 21, 16, 5, 24, 3, 3, 2, 1, 2, act="relu"),
+    L("fold_5x2_no_pad", 2, 11, 12, 8, 16, 5, 2, 1, 0, 0),
+    L("fold_cin1_10x4", 1, 49, 16, 1, 64, 10, 4, 2, 5, 1, act="none"),
+]
+
+
+@pytest.mark.parametrize("spec,layout", [
+    pytest.param(spec, f"{lay}+{w}", id=f"{spec.name}-{lay}+{w}")
+    for spec in FOLD_INKERNEL for lay in ("igemm_n64", "igemm_n128") for w in ("inkernel", "prepass")
+] + [pytest.param(spec, f"igemm_n64+{st}+{ep}+inkernel", id=f"{spec.name}-igemm_n64+{st}+{ep}+inkernel")
+     for spec in FOLD_INKERNEL for st in ("taps", "halo") for ep in ("ept", "sliced")
+     if st == "taps" or (spec.stride == 1 and spec.kh == 3)])
+def test_kw_fold_in_kernel(spec, layout):
+    plan = check(spec, layout, "igemm")
+    want = "bf16-kwfold-in-kernel" if "inkernel" in layout else "bf16-cpad-kwfold"
+    assert want in plan.describe(), plan.describe()
+    assert plan.launches == (1 if "inkernel" in layout else 2)
+
+
+def test_kw_fold_in_kernel_needs_whole_rows():
+    # 45 pixels x 3 channels x 2 bytes = 270: not a whole number of 16-byte units
+    spec = L("fold_row_270_bytes", 1, 18, 45, 3, 32, 3, 3, 1, 1, 1)
+    d = make_layer(spec, torch.Generator("cpu").manual_seed(0))
+    with pytest.raises(RuntimeError, match="UNSUPPORTED"):
+        make_plan(spec, d, "igemm+inkernel")
+
+
 # bf16 layers whose channel rows are too short for TMA: channels padded to 16.
 IGEMM_CPAD = [
     L("cpad_stem_cin3", 1, 37, 45, 3, 32, 3, 3, 1, 1, 1),
@@ -199,8 +235,10 @@ IGEMM_CPAD = [
 @pytest.mark.parametrize("spec,layout", with_layouts(IGEMM_CPAD))
 def test_igemm_channel_padding(spec, layout):
     plan = check_layout(spec, layout)
-    assert "cpad" in plan.describe()
-    assert ("kwfold" in plan.describe()) == (spec.kw > 1 and spec.kw * spec.cin <= 16)
+    folded = spec.kw > 1 and spec.kw * spec.cin <= 16
+    # (a folded layer whose image rows are whole 16-byte units is folded in the kernel)
+    assert "cpad" in plan.describe() or (folded and "kwfold-in-kernel" in plan.describe()), plan.describe()
+    assert ("kwfold" in plan.describe()) == folded
 
 
 def test_int8_plan_without_tensor_core_path_falls_to_dp4a():
