@@ -243,16 +243,7 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
                     // One epilogue per tile where each CTA gets at least two tiles
                     // (with fewer, slicing every tile's columns over the warpgroups
                     // finishes each tile sooner), or where forced.
-                    c.ept = (!cvt || cvt_mode == 2) && ept_ok && epi != 1 && (epi == 2 || c.units >= 2LL * p->num_sms)
-                                ? 1 : 0;
-                    if (cvt && cvt_mode == 1 && epi == 2) continue;
-                    // In-kernel widening where each CTA gets at least four tiles
-                    // (or where forced): every CTA widens the whole weight tensor
-                    // before its first MMA, which a layer of about one tile per
-                    // CTA pays in full (measured: int8 3x3 64->64 @96, 96 tiles,
-                    // 16.1 us against 9.7 with the pre-pass; @160 batch 8, 1600
-                    // tiles, 54.2 against 70.5).
-                    if (cvt && cvt_mode == 1 && widen != 2 && c.units < 4LL * p->num_sms) continue;
+                    c.ept = ept_ok && epi != 1 && (epi == 2 || c.units >= 2LL * p->num_sms) ? 1 : 0;
                     // Shared memory: ring stages, resident weights, epilogue
                     // staging.  A halo stage holds the box's (bh + k_h - 1) x bw
                     // pixel rows and, when bh x bw < P, the P - bh x bw rows the
@@ -264,6 +255,19 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
                     c.a_stage = (uint32_t)(((long long)a_rows * bk * 2 + 1023) / 1024 * 1024);
                     const long long ring_kb = halo ? (long long)g.kw * cblocks : wblocks;  // stages per tile
                     const long long wblock = (long long)bnc * bk * 2;
+                    // In-kernel widening where each CTA gets at least four tiles,
+                    // or where the weights are at most half the bytes of the CTA's
+                    // output pixels' input channels (or where forced): every CTA
+                    // widens the whole weight tensor before its first MMA, which a
+                    // layer of about one tile per CTA pays in full.  Measured
+                    // (warm): int8 3x3 64->64 @96, 72 tiles, weights 36 KB against
+                    // 8 KB: 14.5 us against 10.5 with the pre-pass; 1x1 32->64
+                    // @96, 2 KB against 4 KB: 7.6 against 10.0; 3x3 64->64 @160
+                    // batch 8, 1600 tiles: 51.9 against 70.0.
+                    if (cvt && cvt_mode == 1 && widen != 2 && c.units < 4LL * p->num_sms) {
+                        const long long per_cta = (c.units + p->num_sms - 1) / p->num_sms;
+                        if (2 * wblocks * bnc * bk > per_cta * P * cin) continue;
+                    }
                     const int one_buf = swap ? 4 * 16 * kTP : epi_groups(bn, false, c.ept != 0) * kBM * 64;
                     c.out_bufs = 1;
                     if (!swap && wblocks < 16 && (smem_cap - 2 * one_buf) / ((long long)c.a_stage + wblock) >= 4)

@@ -7,21 +7,21 @@
 
 namespace {
 
-template <int BN, int BK>
+template <int BN, int BK, bool EPT>
 void *widen_ptr(bool flat, bool halo) {
     if (flat)
-        return reinterpret_cast<void *>(&igemm_bf16_kernel<BN, BK, true, false, false, false, false, false, 1>);
+        return reinterpret_cast<void *>(&igemm_bf16_kernel<BN, BK, true, false, false, false, false, EPT, 1>);
     if (halo)
-        return reinterpret_cast<void *>(&igemm_bf16_kernel<BN, BK, false, false, false, false, true, false, 1>);
-    return reinterpret_cast<void *>(&igemm_bf16_kernel<BN, BK, false, false, false, false, false, false, 1>);
+        return reinterpret_cast<void *>(&igemm_bf16_kernel<BN, BK, false, false, false, false, true, EPT, 1>);
+    return reinterpret_cast<void *>(&igemm_bf16_kernel<BN, BK, false, false, false, false, false, EPT, 1>);
 }
 
 template <int BN>
-void *widen_bk(int bk, bool flat, bool halo) {
+void *widen_bk(int bk, bool flat, bool halo, bool ept) {
     switch (bk) {
-    case 64: return widen_ptr<BN, 64>(flat, halo);
-    case 32: return widen_ptr<BN, 32>(flat, halo);
-    default: return widen_ptr<BN, 16>(flat, halo);
+    case 64: return ept ? widen_ptr<BN, 64, true>(flat, halo) : widen_ptr<BN, 64, false>(flat, halo);
+    case 32: return ept ? widen_ptr<BN, 32, true>(flat, halo) : widen_ptr<BN, 32, false>(flat, halo);
+    default: return ept ? widen_ptr<BN, 16, true>(flat, halo) : widen_ptr<BN, 16, false>(flat, halo);
     }
 }
 
@@ -39,5 +39,5 @@ void *fold_ptr(bool halo, bool ept) {
 
 void *igemm_select_cvt(int mode, int bn, int bk, bool flat, bool halo, bool ept) {
     if (mode == 2) return bn == 128 ? fold_ptr<128>(halo, ept) : fold_ptr<64>(halo, ept);
-    return bn == 128 ? widen_bk<128>(bk, flat, halo) : widen_bk<64>(bk, flat, halo);
+    return bn == 128 ? widen_bk<128>(bk, flat, halo, ept) : widen_bk<64>(bk, flat, halo, ept);
 }

@@ -411,7 +411,7 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     static_assert(!(PAIR && SWAP), "the CTA-pair mode uses the normal layout");
     static_assert(!(HALO && FLAT), "halo staging is for spatial tiles");
     static_assert(!EPT || (!SWAP && !PAIR && BN <= 128), "one epilogue per tile: normal layout, BN <= 128");
-    static_assert(!CVT || (!SWAP && !PAIR && !FUSED && (CVT == 2 || !EPT)), "in-kernel widening: normal layout");
+    static_assert(!CVT || (!SWAP && !PAIR && !FUSED), "in-kernel widening: normal layout");
     static_assert(CVT != 2 || (BK == 16 && !FLAT), "in-kernel fold: 16-channel rows of spatial tiles");
     constexpr int kPix = SWAP ? kBMSwap : kBM;  // pixel rows of a tile (per CTA)
     constexpr int kAcc = SWAP ? kBMSwap : BN;   // accumulator columns of a tile
@@ -510,6 +510,45 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     // previous one's writes before the first global access
     pdl_trigger();
     pdl_wait();
+
+    // CVT == 1: int8 -> bf16 (exact) into the swizzled K-major operand, rows
+    // [0, rows) of BK bytes at src, items (row, 16-byte chunk) t, t + T, ...:
+    // chunk j of row r goes to chunk j ^ ((r * row bytes) >> 7 & (chunks - 1))
+    // of the row (the 128-, 64- or 32-byte swizzle of a 1024-aligned slot)
+    constexpr int kChunks = BK / 8;  // 16-byte bf16 chunks per row
+    auto widen_span = [&](uint32_t src, uint32_t dst, int rows, int t, int T) {
+        for (int idx = t; idx < rows * kChunks; idx += T) {
+            const int r = idx / kChunks, j = idx % kChunks;
+            uint32_t lo, hi;  // 8 int8 values
+            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(lo), "=r"(hi) : "r"(src + (uint32_t)(r * BK + j * 8)));
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t wd = e < 2 ? lo : hi;
+                const int sh = (e & 1) * 16;
+                const float f0 = (float)(int8_t)(wd >> sh), f1 = (float)(int8_t)(wd >> (sh + 8));
+                // bf16 of a small integer is its float's upper half, exactly
+                o[e] = (__float_as_uint(f0) >> 16) | (__float_as_uint(f1) & 0xffff0000u);
+            }
+            const uint32_t sw = (uint32_t)((r * kRowBytes) >> 7) & (uint32_t)(kChunks - 1);
+            const uint32_t d = dst + (uint32_t)(r * kRowBytes) + (((uint32_t)j ^ sw) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d), "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                         : "memory");
+        }
+    };
+    // CVT == 1: the resident weights (every K block, [kBRows x BK] each, the
+    // blocks contiguous in the raw region and in sB) are widened once by the
+    // converter and the epilogue warps together (the latter idle until the
+    // first accumulator), after which the converter marks them resident.
+    constexpr int kWidenThreads = 128 * (kGroups + 1);
+    auto widen_weights = [&]() {
+        const int t = (int)threadIdx.x - 64;  // epilogue warps, then the converter warpgroup
+        if (wait_bounded(wraw_bar, 0u, abort_flag, a.status, KSTATUS_TIMEOUT_EPILOGUE)) {
+            widen_span(sRaw, sB, a.wblocks * kBRows, t, kWidenThreads);
+            tc::fence_proxy_async_smem();  // the widened weights visible to the tensor cores
+        }
+        tc::named_bar_sync(7, kWidenThreads);  // (reached by every thread: the wait is bounded)
+    };
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -774,33 +813,8 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         }
     } else if (CVT && warp >= 2 + 4 * kGroups) {
         // ------------------------------------------------ converter (the last warpgroup)
-        // int8 -> bf16 (exact) into the swizzled K-major operand: a 16-byte
-        // chunk of 8 bf16 channels, chunk j of row r, goes to chunk
-        // j ^ ((r * row bytes) >> 7 & (chunks - 1)) of the row (the 128-, 64- or
-        // 32-byte swizzle of a 1024-aligned slot).
-        constexpr int kChunks = BK / 8;  // 16-byte bf16 chunks per row
         const int ct = threadIdx.x - (64 + 128 * kGroups);
-        auto widen = [&](uint32_t src, uint32_t dst, int rows) {
-            for (int idx = ct; idx < rows * kChunks; idx += 128) {
-                const int r = idx / kChunks, j = idx % kChunks;
-                uint32_t lo, hi;  // 8 int8 values
-                asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(lo), "=r"(hi) : "r"(src + (uint32_t)(r * BK + j * 8)));
-                uint32_t o[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const uint32_t wd = e < 2 ? lo : hi;
-                    const int sh = (e & 1) * 16;
-                    const float f0 = (float)(int8_t)(wd >> sh), f1 = (float)(int8_t)(wd >> (sh + 8));
-                    // bf16 of a small integer is its float's upper half, exactly
-                    o[e] = (__float_as_uint(f0) >> 16) | (__float_as_uint(f1) & 0xffff0000u);
-                }
-                const uint32_t sw = (uint32_t)((r * kRowBytes) >> 7) & (uint32_t)(kChunks - 1);
-                const uint32_t d = dst + (uint32_t)(r * kRowBytes) + (((uint32_t)j ^ sw) << 4);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d), "r"(o[0]), "r"(o[1]), "r"(o[2]),
-                             "r"(o[3])
-                             : "memory");
-            }
-        };
+        auto widen = [&](uint32_t src, uint32_t dst, int rows) { widen_span(src, dst, rows, ct, 128); };
         // One thread does the (bounded) waits and tells the others through
         // shared memory, so that the warpgroup gives up, if it must, as one
         // (a hardware named barrier has no time limit).
@@ -869,16 +883,9 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 if (ct == 0) tc::mbar_arrive(wres_bar);
             }
         } else if (CVT == 1 && unit < a.num_tiles) {
-            // the resident weights: every K block [kBRows x BK], widened once
-            ok = all_ok(ct != 0 || wait_bounded(wraw_bar, 0u, abort_flag, a.status, KSTATUS_TIMEOUT_EPILOGUE));
-            if (ok) {
-                (void)tc::mbar_try_wait(wraw_bar, 0u);  // (complete: each thread's own acquire of the TMA bytes)
-                for (int kb = 0; kb < a.wblocks; ++kb)
-                    widen(sRaw + (uint32_t)kb * kBRows * BK, sB + (uint32_t)kb * kBStage, kBRows);
-                tc::fence_proxy_async_smem();  // the widened weights visible to the tensor cores
-                tc::named_bar_sync(6, 128);
-                if (ct == 0) tc::mbar_arrive(wres_bar);
-            }
+            widen_weights();
+            ok = *abort_flag == 0;  // (a thread that gave up has raised it)
+            if (ok && ct == 0) tc::mbar_arrive(wres_bar);
         }
         // CVT == 2: this thread's box rows m = ct + 128 i (at most three: a box
         // has at most 128 + 2 bw <= 384 rows), pixel (m / bw, m % bw), whose taps
@@ -967,6 +974,7 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         int oc = 0;  // TMA stores this group has issued (selects the staging buffer)
         // pair mode: accumulator-empty arrivals go to the even CTA's barrier
         const uint32_t tempty0 = PAIR ? tc::mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
+        if (CVT == 1 && unit < a.num_tiles) widen_weights();
         // lt: the CTA's local tile index (EPT: this group's tiles, every 4th)
         const int lt0 = EPT ? grp : 0, lstep = EPT ? kGroups : 1;
         for (int tile = unit + lt0 * units, lt = lt0; tile < a.num_tiles; tile += lstep * units, lt += lstep) {

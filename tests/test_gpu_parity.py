@@ -169,7 +169,9 @@ I8_WIDEN = [s for s in IGEMM_I8 if s.name in ("i8_3x3_64to64_ragged", "i8_3x3_re
     for spec in I8_WIDEN for lay in ("igemm", "igemm_n64", "igemm_n128") for w in ("inkernel", "prepass")
     if not (w == "inkernel" and lay == "igemm_n128" and spec.kh > 1)
 ] + [pytest.param(spec, "igemm_n64+halo+inkernel", id=f"{spec.name}-igemm_n64+halo+inkernel")
-     for spec in I8_WIDEN if spec.stride == 1 and spec.kh == 3])
+     for spec in I8_WIDEN if spec.stride == 1 and spec.kh == 3
+] + [pytest.param(spec, f"igemm_n64+{ep}+inkernel", id=f"{spec.name}-igemm_n64+{ep}+inkernel")
+     for spec in I8_WIDEN for ep in ("ept", "sliced")])
 def test_igemm_int8_widening(spec, layout):
     plan = check(spec, layout, "igemm")
     want = "i8-widened-in-kernel" if "inkernel" in layout else "i8-as-bf16"
