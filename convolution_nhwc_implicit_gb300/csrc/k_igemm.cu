@@ -143,23 +143,26 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
     // tiles; normal with 128-pixel tiles and BN in {256, 128, 64}; the CTA
     // pair with 2 x 128-pixel tiles and BN in {256, 128}) x the staging
     // (per-tap boxes, or halo staging for stride-1 spatial layers with
-    // k_h = 3) x, in spatial mode, the tile's bh x bw shape.  The channel
-    // block BK is the largest of 64, 32, 16 dividing Cin (measured: smaller
-    // blocks never won, even where they let the weights stay resident)
-    // unless it leaves no room for two stages.
+    // k_h = 3) x, in spatial mode, the tile's bh x bw shape x the channel
+    // block BK: the largest of 64, 32, 16 dividing Cin and half of it (a
+    // smaller one only where neither leaves room for two stages).
     // Each candidate is scored by an estimate of its time, waves x (per-tile
-    // cost + a fixed cost), the per-tile cost (per SM) being the largest of
-    //   MMA issue   128 cycles per K = 16 step whatever N is (N = 256 is the
-    //               only full-rate width; measured),
-    //   TMA issue   ~2 cycles per staged operand row (a pixel's or an output
-    //               channel's BK channels), whatever its length,
-    //   ring latency  a freed stage is refilled ~2000 cycles later: with S
-    //               stages each stage's MMAs are spaced at least 2000 / (S - 1),
-    //   epilogue    accumulator lanes x columns (wasted lanes included)
-    //               x cycles per value / 128 lanes per cycle per SM,
+    // cost + a fixed cost), the per-tile cost (per SM) being the larger of
+    //   the ring  stages per tile x (per-stage time + ~200 cycles of barrier
+    //             round trip), a stage taking the longest of
+    //               its MMAs     128 cycles per K = 16 step whatever N is (N =
+    //                            256 is the only full-rate width; measured),
+    //               its TMA rows ~1.5 cycles per staged operand row (a pixel's
+    //                            or an output channel's BK channels),
+    //               the refill   a freed stage is refilled ~2000 cycles later:
+    //                            with S stages, 2000 / (S - 1) per stage,
+    //   the epilogue  accumulator lanes x columns (wasted lanes included)
+    //             x cycles per value / 128 lanes per cycle per SM,
     // with the epilogue costing ~16 cycles per value with Mish (two MUFU
-    // operations), ~10 for an int8 requantisation and ~6 otherwise.
-    const long long K = (long long)p->s.k_h * g.kw * cin;
+    // operations), ~10 for an int8 requantisation and ~6 otherwise.  The
+    // per-stage constants fit the batch-8 sweep's 3x3 layers (measured per
+    // stage: 256->256 @80 CTA pair per-tap BK 64, 6 stages, 730 cycles; halo
+    // BK 64, 2 stages, 2070; halo BK 32, 5 stages, 985 -- the fastest).
     const long long epi_c = p->dtype == CONV_I8 ? 10 : (p->act == CONV_ACT_MISH ? 16 : 6);
     const int smem_cap = 227 * 1024 - 1024 - 512;  // minus the alignment slack and the barriers
     const bool halo_ok = !g.flat && S == 1 && p->s.k_h == 3;  // (the halo variants' tap count)
@@ -186,9 +189,9 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
         if (epi == 2 && !ept_ok) continue;
         const int P = swap ? kBMSwap : kBM;
         const int bnc = swap ? 128 : (pair ? bn / 2 : bn);  // weight rows a CTA stages per K block
-        // (a smaller channel block only where the largest leaves no room for
-        // two ring stages of this layout and staging)
-        for (int bk = bk_max, fits = 0; bk >= 16 && !fits; bk /= 2) {
+        // (the largest channel block and half of it; smaller ones only where
+        // neither leaves room for two ring stages of this layout and staging)
+        for (int bk = bk_max, fits = 0; bk >= 16 && (2 * bk >= bk_max || !fits); bk /= 2) {
             const long long cblocks = cin / bk;
             const long long wblocks = (long long)p->s.k_h * g.kw * cblocks;
             for (int halo = 0; halo <= (halo_ok ? 1 : 0); ++halo) {
@@ -315,19 +318,18 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
                     // the estimate
                     const long long slots = pair ? p->num_sms / 2 : p->num_sms;
                     const long long waves = (c.units + slots - 1) / slots;
-                    const long long t_mma = K / 16 * 128;
                     c.rows = ring_kb * box_rows + (c.wres ? 0 : wblocks * bnc);  // staged rows per tile
-                    const long long t_tma = 2 * c.rows;
                     const long long t_epi = 128LL * (swap ? P : bn) * epi_c / 128;
-                    // a stage is refilled ~2000 cycles after its MMAs free it, which
-                    // the MMAs of the other stages must cover
+                    // a stage: its MMAs, its TMA rows, or the ring's refill latency
+                    // spread over the other stages, whichever is longest, plus a
+                    // fixed cost of the stage's barrier round trip
                     const long long m_stage = (long long)taps * (bk / 16) * 128;
+                    const long long rows_stage = box_rows + (c.wres ? 0 : (long long)taps * bnc);
                     long long per_stage = 2000 / (c.stages - 1);
                     if (per_stage < m_stage) per_stage = m_stage;
-                    const long long t_ring = ring_kb * per_stage;
-                    long long t_tile = t_mma > t_tma ? t_mma : t_tma;
-                    if (t_epi > t_tile) t_tile = t_epi;
-                    if (t_ring > t_tile) t_tile = t_ring;
+                    if (per_stage < 3 * rows_stage / 2) per_stage = 3 * rows_stage / 2;
+                    const long long t_ring = ring_kb * (per_stage + 200);
+                    const long long t_tile = t_ring > t_epi ? t_ring : t_epi;
                     const long long cost = waves * (t_tile + 500);
                     // ties: more work units (more SMs busy), then fewer staged
                     // rows, then the narrower N tile
