@@ -109,6 +109,34 @@ struct YMaps {
 // Waits for phase `parity` of `bar`, giving up after kWaitBudgetNs or when
 // another role of the CTA has given up.  Returns false on give-up.
 // CLUSTER: acquire at cluster scope (arrivals may come from the peer CTA).
+// The coordinates of a CTA's (or an epilogue group's) tiles tile0, tile0 +
+// step, ...: N block nb, M tile mt and, spatial, its tile column tw, tile row
+// th and image n, advanced by mixed-radix addition of the step's digits
+// (no division per tile).
+struct TileWalk {
+    int nb, mt, tw, th, n;
+    int sn, sm, sw, sh, snn;
+    __device__ __forceinline__ void init(const IgArgs &a, int tile0, int step) {
+        nb = tile0 % a.tiles_n; mt = tile0 / a.tiles_n;
+        tw = mt % a.tiles_w; th = (mt / a.tiles_w) % a.tiles_h; n = mt / (a.tiles_w * a.tiles_h);
+        sn = step % a.tiles_n; sm = step / a.tiles_n;
+        sw = sm % a.tiles_w; sh = (sm / a.tiles_w) % a.tiles_h; snn = sm / (a.tiles_w * a.tiles_h);
+    }
+    __device__ __forceinline__ void advance(const IgArgs &a) {
+        nb += sn;
+        const int c = nb >= a.tiles_n ? 1 : 0;
+        nb -= c * a.tiles_n;
+        mt += sm + c;
+        tw += sw + c;
+        const int c2 = tw >= a.tiles_w ? 1 : 0;
+        tw -= c2 * a.tiles_w;
+        th += sh + c2;
+        const int c3 = th >= a.tiles_h ? 1 : 0;
+        th -= c3 * a.tiles_h;
+        n += snn + c3;
+    }
+};
+
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                              int *status, int code) {
@@ -977,7 +1005,11 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         if (CVT == 1 && unit < a.num_tiles) widen_weights();
         // lt: the CTA's local tile index (EPT: this group's tiles, every 4th)
         const int lt0 = EPT ? grp : 0, lstep = EPT ? kGroups : 1;
-        for (int tile = unit + lt0 * units, lt = lt0; tile < a.num_tiles; tile += lstep * units, lt += lstep) {
+        // (single CTAs: the tiles' coordinates advanced without division)
+        TileWalk walk;
+        walk.init(a, unit + lt0 * units, lstep * units);
+        for (int tile = unit + lt0 * units, lt = lt0; tile < a.num_tiles;
+             tile += lstep * units, lt += lstep, walk.advance(a)) {
             const int buf = lt % kBufs;
             const uint32_t use = (uint32_t)(lt / kBufs);
             const bool got = wait_bounded(tfull_bar(buf), use & 1u, abort_flag, a.status,
@@ -1028,8 +1060,8 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             // one TMA tensor store per 32 columns.  The box is the tile's
             // bh x bw pixel rectangle (or 128 flat rows): rows past it are
             // never stored and pixels outside the image are clipped by TMA.
-            const int nb = tile % a.tiles_n;
-            const int mt = PAIR ? (tile / a.tiles_n) * 2 + (int)rank : tile / a.tiles_n;
+            const int nb = PAIR ? tile % a.tiles_n : walk.nb;
+            const int mt = PAIR ? (tile / a.tiles_n) * 2 + (int)rank : walk.mt;
             if (PAIR && mt >= a.tiles_m) {  // the empty half of the last pair tile
                 if constexpr (kChunked) release();
                 continue;
@@ -1037,12 +1069,16 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             int n = 0, oh0 = 0, ow0 = 0, m0 = 0;
             if (FLAT) {
                 m0 = mt * kPix;
-            } else {
+            } else if (PAIR) {
                 const int tw = mt % a.tiles_w;
                 const int t2 = mt / a.tiles_w;
                 oh0 = (t2 % a.tiles_h) * a.bh;
                 n = t2 / a.tiles_h;
                 ow0 = tw * a.bw;
+            } else {
+                oh0 = walk.th * a.bh;
+                n = walk.n;
+                ow0 = walk.tw * a.bw;
             }
             const uint32_t swz = (uint32_t)((row >> 1) & 3);
             // residual pixel of this thread's row (-1: none, or outside the image;
