@@ -56,6 +56,7 @@ constexpr int kHalo = 6;         // (13 - 1) / 2
 constexpr int kP = kTW + 2 * kHalo;  // row pitch (pixels) of the shared buffers
 constexpr int kR = kTH + 2 * kHalo;
 constexpr int kThreads = 256;
+constexpr int kImgPer = 12;  // whole-image kernel: elements per thread (2 x 12 x 256 x 16 B = 96 KB)
 
 struct SppArgs {
     int N, H, W, CV;       // CV: 16-byte channel vectors per pixel of x
@@ -170,38 +171,74 @@ __global__ void __launch_bounds__(kThreads) spp_image_kernel(const uint4 *__rest
     uint4 *B = sm + nel;
     const uint4 neg = make_uint4(VMax<T>::kNeg, VMax<T>::kNeg, VMax<T>::kNeg, VMax<T>::kNeg);
     const long long xbase = (long long)n * np;
+    // This thread's elements e = threadIdx.x + k * kThreads (k < kImgPer; the
+    // host keeps nel <= kImgPer * kThreads): pixel (h, w) and channel vector
+    // cv, found once.  A window clipped at the border equals the window whose
+    // indices are clamped into the image (max is idempotent), so each pass
+    // reads the five clamped neighbours with no branch.
+    int eh[kImgPer], ew[kImgPer], ec[kImgPer];
+#pragma unroll
+    for (int k = 0; k < kImgPer; ++k) {
+        const int e = threadIdx.x + k * kThreads;
+        const int p = e / a.cbv;
+        ec[k] = e - p * a.cbv;
+        eh[k] = p / a.W;
+        ew[k] = p - eh[k] * a.W;
+    }
     // x -> A (and to its own slice of y, if asked)
-    for (int e = threadIdx.x; e < nel; e += kThreads) {
-        const int cv = e % a.cbv, p = e / a.cbv;
+#pragma unroll
+    for (int k = 0; k < kImgPer; ++k) {
+        const int e = threadIdx.x + k * kThreads;
+        if (e >= nel) break;
+        const long long pix = xbase + eh[k] * a.W + ew[k];
         uint4 v = neg;
-        if (cv0 + cv < a.CV) {
-            v = __ldg(x + (xbase + p) * a.CV + cv0 + cv);
-            if (a.off[3] >= 0) y[(xbase + p) * a.Cy + a.off[3] + cv0 + cv] = v;
+        if (cv0 + ec[k] < a.CV) {
+            v = __ldg(x + pix * a.CV + cv0 + ec[k]);
+            if (a.off[3] >= 0) y[pix * a.Cy + a.off[3] + cv0 + ec[k]] = v;
         }
         A[e] = v;
     }
     __syncthreads();
+    const int rowstep = a.W * a.cbv;
     for (int level = 0; level < 3; ++level) {  // 5x5, 9x9, 13x13
         // along rows (A -> B), then along columns (B -> A): clipped 5-wide maxima
-        for (int dir = 0; dir < 2; ++dir) {
-            const uint4 *src = dir ? B : A;
-            uint4 *dst = dir ? A : B;
-            for (int e = threadIdx.x; e < nel; e += kThreads) {
-                const int cv = e % a.cbv, p = e / a.cbv;
-                const int h = p / a.W, w = p - h * a.W;
-                const int pos = dir ? h : w, len = dir ? a.H : a.W;
-                const int step = (dir ? a.W : 1) * a.cbv;
-                const int lo = pos < 2 ? -pos : -2, hi = pos + 2 >= len ? len - 1 - pos : 2;
-                uint4 m = src[e + lo * step];
-                for (int d = lo + 1; d <= hi; ++d) m = VMax<T>::max(m, src[e + d * step]);
-                dst[e] = m;
+#pragma unroll
+        for (int k = 0; k < kImgPer; ++k) {
+            const int e = threadIdx.x + k * kThreads;
+            if (e >= nel) break;
+            const int w = ew[k], b = e - w * a.cbv;  // b: the element at w = 0 of this row
+            uint4 m = A[e];
+#pragma unroll
+            for (int d = -2; d <= 2; ++d) {
+                if (d == 0) continue;
+                const int q = min(max(w + d, 0), a.W - 1);
+                m = VMax<T>::max(m, A[b + q * a.cbv]);
             }
-            __syncthreads();
+            B[e] = m;
         }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < kImgPer; ++k) {
+            const int e = threadIdx.x + k * kThreads;
+            if (e >= nel) break;
+            const int h = eh[k], b = e - h * rowstep;  // b: the element at h = 0 of this column
+            uint4 m = B[e];
+#pragma unroll
+            for (int d = -2; d <= 2; ++d) {
+                if (d == 0) continue;
+                const int q = min(max(h + d, 0), a.H - 1);
+                m = VMax<T>::max(m, B[b + q * rowstep]);
+            }
+            A[e] = m;
+        }
+        __syncthreads();
         if (a.off[level] >= 0) {
-            for (int e = threadIdx.x; e < nel; e += kThreads) {
-                const int cv = e % a.cbv, p = e / a.cbv;
-                if (cv0 + cv < a.CV) y[(xbase + p) * a.Cy + a.off[level] + cv0 + cv] = A[e];
+#pragma unroll
+            for (int k = 0; k < kImgPer; ++k) {
+                const int e = threadIdx.x + k * kThreads;
+                if (e >= nel) break;
+                if (cv0 + ec[k] < a.CV)
+                    y[(xbase + eh[k] * a.W + ew[k]) * a.Cy + a.off[level] + cv0 + ec[k]] = A[e];
             }
         }
         // (the next level's row pass overwrites B only: A stays readable here)
