@@ -152,7 +152,7 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
     //             round trip), a stage taking the longest of
     //               its MMAs     128 cycles per K = 16 step whatever N is (N =
     //                            256 is the only full-rate width; measured),
-    //               its TMA rows ~1.5 cycles per staged operand row (a pixel's
+    //               its TMA rows ~1.4 cycles per staged operand row (a pixel's
     //                            or an output channel's BK channels),
     //               the refill   a freed stage is refilled ~2000 cycles later:
     //                            with S stages, 2000 / (S - 1) per stage,
@@ -161,8 +161,10 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
     // with the epilogue costing ~16 cycles per value with Mish (two MUFU
     // operations), ~10 for an int8 requantisation and ~6 otherwise.  The
     // per-stage constants fit the batch-8 sweep's 3x3 layers (measured per
-    // stage: 256->256 @80 CTA pair per-tap BK 64, 6 stages, 730 cycles; halo
-    // BK 64, 2 stages, 2070; halo BK 32, 5 stages, 985 -- the fastest).
+    // stage: 256->256 @80 CTA pair per-tap BK 64, 6 stages, 730-800 cycles;
+    // halo BK 64, 2 stages, 2070; halo BK 32, 5 stages, 985 -- the fastest;
+    // 512->1024 @40 pair per-tap BK 64 713, halo BK 32 990 a stage, 72
+    // against 48 stages a tile: halo the faster by 7 %).
     const long long epi_c = p->dtype == CONV_I8 ? 10 : (p->act == CONV_ACT_MISH ? 16 : 6);
     const int smem_cap = 227 * 1024 - 1024 - 512;  // minus the alignment slack and the barriers
     const bool halo_ok = !g.flat && S == 1 && p->s.k_h == 3;  // (the halo variants' tap count)
@@ -327,7 +329,7 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
                     const long long rows_stage = box_rows + (c.wres ? 0 : (long long)taps * bnc);
                     long long per_stage = 2000 / (c.stages - 1);
                     if (per_stage < m_stage) per_stage = m_stage;
-                    if (per_stage < 3 * rows_stage / 2) per_stage = 3 * rows_stage / 2;
+                    if (per_stage < 7 * rows_stage / 5) per_stage = 7 * rows_stage / 5;
                     const long long t_ring = ring_kb * (per_stage + 200);
                     const long long t_tile = t_ring > t_epi ? t_ring : t_epi;
                     const long long cost = waves * (t_tile + 500);
