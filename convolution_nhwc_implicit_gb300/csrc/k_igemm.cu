@@ -205,19 +205,26 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
                 if (g.flat) {
                     shapes[nshapes][0] = P; shapes[nshapes][1] = 1; ++nshapes;
                 } else if (!halo) {
-                    long long bt = -1;
-                    int bw = P, bh = 1;
-                    for (int cw = 1; cw <= P && cw <= p->ow * 2; ++cw) {
-                        if (cw * S > 256) break;
-                        int ch = P / cw;
-                        if (ch > p->oh) ch = p->oh;
-                        while (ch * S > 256) --ch;
-                        if (ch < 1) continue;
-                        const long long t = (long long)((p->ow + cw - 1) / cw) * ((p->oh + ch - 1) / ch) * p->s.n;
-                        if (bt < 0 || t < bt || (t == bt && cw > bw)) { bt = t; bw = cw; bh = ch; }
-                        if (cw >= p->ow) break;
+                    // (the fewest tiles, then the widest; and, for the fold built in
+                    // the kernel, the same among the widths whose raw box rows fit
+                    // TMA's 256 elements)
+                    for (int pass = 0; pass < (cvt_mode == 2 ? 2 : 1); ++pass) {
+                        long long bt = -1;
+                        int bw = P, bh = 1;
+                        for (int cw = 1; cw <= P && cw <= p->ow * 2; ++cw) {
+                            if (cw * S > 256) break;
+                            if (pass == 1 && fold_inner(p, cw) > 256) break;
+                            int ch = P / cw;
+                            if (ch > p->oh) ch = p->oh;
+                            while (ch * S > 256) --ch;
+                            if (ch < 1) continue;
+                            const long long t = (long long)((p->ow + cw - 1) / cw) * ((p->oh + ch - 1) / ch) * p->s.n;
+                            if (bt < 0 || t < bt || (t == bt && cw > bw)) { bt = t; bw = cw; bh = ch; }
+                            if (cw >= p->ow) break;
+                        }
+                        if (bt < 0 || (pass == 1 && bw == shapes[0][0])) continue;
+                        shapes[nshapes][0] = bw; shapes[nshapes][1] = bh; ++nshapes;
                     }
-                    shapes[nshapes][0] = bw; shapes[nshapes][1] = bh; ++nshapes;
                 } else {
                     for (int cw = 8; cw <= P && cw <= 256 && nshapes < 40; cw += 8) {
                         int ch = P / cw;

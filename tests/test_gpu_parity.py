@@ -194,6 +194,8 @@ def test_int8_widening_in_kernel_needs_whole_rows():
 FOLD_INKERNEL = [
     L("fold_stem_cin3_ragged_h", 2, 37, 48, 3, 32, 3, 3, 1, 1, 1),
     L("fold_stem_cin3_s2", 1, 41, 64, 3, 32, 3, 3, 2, 1, 1, act="relu"),
+    # (128 output columns: the widest tile's raw rows would pass 256 elements)
+    L("fold_stem_s2_wide_rows", 1, 21, 256, 3, 32, 3, 3, 2, 1, 1),
     L("fold_cin4_cout48", 1, 23, 20, 4, 48, 3, 3, 1, 1, 1, act="none"),
     L("fold_cin5_s2_overpad_w", 1, 21, 16, 5, 24, 3, 3, 2, 1, 2, act="relu"),
     L("fold_5x2_no_pad", 2, 11, 12, 8, 16, 5, 2, 1, 0, 0),
