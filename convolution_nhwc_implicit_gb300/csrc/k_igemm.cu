@@ -296,7 +296,8 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
                     if (cvt) {
                         // resident (widened) weights, and a raw region holding first the
                         // raw int8 weights, then the raw ring of int8 activation boxes;
-                        // folded: first the raw bf16 weights (and a word of slack), then
+                        // folded: first the raw bf16 weights (and 36 bytes of slack for the
+                        // converter's whole-word reads), then
                         // the raw ring of image-row boxes, each box row the
                         // ((bw - 1) x stride + k_w) x Cin elements under the tile from
                         // the 16-byte unit at or before its first, at most 256

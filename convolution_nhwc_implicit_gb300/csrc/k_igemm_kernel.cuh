@@ -843,9 +843,10 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         // ------------------------------------------------ converter (the last warpgroup)
         const int ct = threadIdx.x - (64 + 128 * kGroups);
         auto widen = [&](uint32_t src, uint32_t dst, int rows) { widen_span(src, dst, rows, ct, 128); };
-        // One thread does the (bounded) waits and tells the others through
-        // shared memory, so that the warpgroup gives up, if it must, as one
-        // (a hardware named barrier has no time limit).
+        // (The folded weights' one-time wait:) one thread does the bounded wait
+        // and tells the others through shared memory, so that the warpgroup
+        // gives up, if it must, as one (a hardware named barrier has no time
+        // limit).
         volatile int *go = reinterpret_cast<volatile int *>(gmisc + 8);
         auto all_ok = [&](bool mine) {
             if (ct == 0) *go = mine ? 1 : 0;
