@@ -26,6 +26,17 @@ MUTANTS = {
     "requant_truncates": ("float r = nearbyintf(p);", "float r = truncf(p);"),
     "requant_rounds_half_away": ("float r = nearbyintf(p);", "float r = roundf(p);"),
     "no_saturation": ("if (r > 127.0f) r = 127.0f;", ""),
+    "requant_scale_w_only": ("M[co] = (float)((double)in_scale * (double)w_scales[co] /\n"
+                             "                        (double)out_scale);",
+                             "M[co] = (float)(double)w_scales[co];"),
+    "requant_scale_ratio_inverted": ("M[co] = (float)((double)in_scale * (double)w_scales[co] /\n"
+                                     "                        (double)out_scale);",
+                                     "M[co] = (float)((double)out_scale * (double)w_scales[co] /\n"
+                                     "                        (double)in_scale);"),
+    "requant_scale_first_channel_full": ("(int8_t)oracle_requant_one(v, M[co], relu);",
+                                         "(int8_t)oracle_requant_one(v, M[0], relu);"),
+    "requant_scale_first_channel": ("vals[i] = (int8_t)oracle_requant_one(v, M[p[3]], relu);",
+                                    "vals[i] = (int8_t)oracle_requant_one(v, M[0], relu);"),
     "ceil_output_dim": ("return span / stride + 1;", "return (span + stride - 1) / stride + 1;"),
     "hardmish": ("return v * tanh(softplus(v));",
                  "return v * fmin(fmax(v + 2.0, 0.0), 2.0) / 2.0;"),

@@ -295,6 +295,31 @@ def test_requant_tie_table():
         assert oracle.requant_one(v, M[0], relu=True) == qr, v
 
 
+def test_requant_scale_ratio_hand_cases():
+    # s_x != s_y: the multiplier is s_x * s_w / s_y, not s_w alone and not its
+    # reciprocal ratio; values worked by hand in the golden file.
+    rows = _read_rows("requant_scales.txt")
+    for _, sx, sy, sw, m in (r for r in rows if r[0] == "mult"):
+        M = oracle.requant_multipliers(float(sx), float(sy), [float(sw)])
+        assert M[0] == np.float32(float(m)), (sx, sy, sw)
+    for _, sx, sy, sw, v, q in (r for r in rows if r[0] == "q"):
+        M = oracle.requant_multipliers(float(sx), float(sy), [float(sw)])
+        assert oracle.requant_one(int(v), M[0]) == int(q), (sx, sy, sw, v)
+
+
+def test_requant_scale_ratio_whole_layer():
+    rows = {r[0]: [int(v) for v in r[1:]] for r in _read_rows("requant_scales.txt") if r[0].startswith("conv")}
+    x = np.arange(1, 10, dtype=np.int8).reshape(1, 3, 3, 1)
+    w = np.ones((2, 3, 3, 1), dtype=np.int8)
+    M = oracle.requant_multipliers(0.1, 0.05, [0.25, 0.125])
+    y = oracle.conv_i8(x, w, np.array([1, 0], dtype=np.int32), M, stride=1, pad_h=1, pad_w=1)
+    np.testing.assert_array_equal(y[..., 0].ravel(), rows["conv_ch0"])
+    np.testing.assert_array_equal(y[..., 1].ravel(), rows["conv_ch1"])
+    pts = np.array([[0, h, w_, c] for h in range(3) for w_ in range(3) for c in range(2)], dtype=np.int32)
+    vals = oracle.conv_i8_points(x, w, np.array([1, 0], dtype=np.int32), M, pts, 1, 1, 1)
+    np.testing.assert_array_equal(vals, y[0, pts[:, 1], pts[:, 2], pts[:, 3]])
+
+
 def test_requant_float_rounding_of_accumulator():
     # Above 2**24 the accumulator is first rounded to float (ties to even):
     # 2**24 + 1 -> 2**24, and 2**24 + 3 -> 2**24 + 4.  With M = 2**-17 these
