@@ -50,7 +50,7 @@ class LayerSpec:
     b_dist: tuple = ("normal", 0.01)  # ("normal", std) | ("int", lo, hi) | None
     in_scale: float = 0.05      # int8 only: activation scale s_x
     out_scale: float = 0.05     # int8 only: output scale s_y
-    ws_dist: tuple = ("uniform", 0.001, 0.01)  # int8 only: per-channel s_w
+    ws_dist: tuple = ("uniform", 0.001, 0.01)  # int8 only: per-channel s_w, or ("pow2", lo, hi)
 
 
 @dataclass
@@ -203,7 +203,12 @@ def make_layer(s: LayerSpec, g: torch.Generator) -> LayerData:
         b = _draw((s.cout,), s.b_dist, g, fan_in)
         b = b.to(torch.int32) if s.dtype == "i8" else b.to(torch.float32)
     ws = None
-    if s.dtype == "i8":
+    if s.dtype == "i8" and s.ws_dist[0] == "pow2":
+        # s_w = 2^e with integer e drawn uniformly from [lo, hi]: scales whose
+        # multipliers are exact in float, so that requantisation ties occur
+        e = torch.randint(s.ws_dist[1], s.ws_dist[2] + 1, (s.cout,), generator=g, dtype=torch.int64)
+        ws = torch.pow(2.0, e.to(torch.float64)).to(torch.float32)
+    elif s.dtype == "i8":
         lo, hi = s.ws_dist[1], s.ws_dist[2]
         ws = torch.rand((s.cout,), generator=g, dtype=torch.float32) * (hi - lo) + lo
     return LayerData(s, _cast(x, s.dtype), _cast(w, s.dtype), b, ws)

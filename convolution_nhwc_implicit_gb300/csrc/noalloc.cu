@@ -105,8 +105,13 @@ extern "C" int conv_run_i8_noalloc(const conv_shape_t *shape, int stride, int pa
         for (int i = 0; i < n; ++i)
             chunk.m[i] = (float)((double)quant->in_scale * (double)quant->w_scales[off + i] /
                                  (double)quant->out_scale);
-        fill_multipliers<<<(n + 255) / 256, 256, 0, st>>>(chunk, off, n);
-        if (cudaGetLastError() != cudaSuccess) return CONV_ERR_CUDA;
+        // The launch's own status (not cudaGetLastError, which would also
+        // return, and clear, an earlier error of unrelated caller work).
+        int o = off, cnt = n;
+        void *args[] = {&chunk, &o, &cnt};
+        if (cudaLaunchKernel((const void *)fill_multipliers, dim3((n + 255) / 256), dim3(256), args, 0, st) !=
+            cudaSuccess)
+            return CONV_ERR_CUDA;
     }
     return launch_direct(&p, x, w, bias, nullptr, y, st) == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
