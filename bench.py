@@ -80,7 +80,7 @@ def layer_bound(spec, peaks):
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """Samples nvidia-smi clocks / throttle reasons every 200 ms while running."""
+    """Samples nvidia-smi clocks / throttle reasons every 50 ms while running."""
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -111,7 +111,7 @@ class ClockSampler:
     def mark(self, which):
         setattr(self, which, time.time())
 
-    def stop(self):
+    def stop(self, window_s=None):
         if not self.proc:
             return None
         self.proc.terminate()
@@ -123,13 +123,16 @@ class ClockSampler:
             self.t.join(timeout=2)
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        # samples that arrived inside the timed region (+ one sampling period)
+        # samples of the main timed region (+ one sampling period), and of
+        # every GPU timing phase up to t_last
         t0, t1 = getattr(self, "t_start", 0.0), getattr(self, "t_end", 1e30) + 0.06
-        inside = [ln for ts, ln in self.lines if t0 <= ts <= t1]
-        where = "timed region"
-        if not inside and self.lines:
-            inside = [ln for _, ln in self.lines]
-            where = "whole run (timed region shorter than the sampling period)"
+        n_main = sum(1 for ts, _ in self.lines if t0 <= ts <= t1)
+        t_last = getattr(self, "t_last", 1e30) + 0.06
+        inside = [ln for ts, ln in self.lines if ts <= t_last]
+        where = ("warm-up, the timed step replays and every later GPU timing phase (per-layer, other "
+                 "layer sets, adjacent rows)")
+        if window_s is not None:
+            where += f": {window_s:.1f} s"
         for ln in inside:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
@@ -144,8 +147,9 @@ class ClockSampler:
                     reasons.add(name)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm), "window": where}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "sm_min_mhz": min(sm),
+                "reasons": sorted(reasons), "samples": len(sm), "samples_in_step_region": n_main,
+                "window": where}
 
 
 # ---------------------------------------------------------------- replicas
@@ -167,6 +171,207 @@ def job_tflops(flops_per_step, world, steps, ms):
     """Whole-job throughput: the work of every rank's `steps` steps over the
     slowest rank's time (ms)."""
     return flops_per_step * world * steps / (ms * 1e-3) / 1e12
+
+
+# ---------------------------------------------------------------- per-layer timing
+
+class GraphTimer:
+    """CUDA-graph timing helpers on one device, with an L2-flush buffer."""
+
+    def __init__(self, dev, flush):
+        self.dev, self.flush = dev, flush
+
+    def capture(self, fn, with_events=False):
+        """fn captured as a CUDA graph (optionally between two timing events,
+        external=True so each replay re-records them)."""
+        import torch
+        evs = None
+        if with_events:
+            evs = (torch.cuda.Event(enable_timing=True, external=True),
+                   torch.cuda.Event(enable_timing=True, external=True))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            st = torch.cuda.current_stream(self.dev)
+            if evs:
+                evs[0].record(st)
+            fn()
+            if evs:
+                evs[1].record(st)
+        return g, evs
+
+    def graph_us(self, fn, reps=5):
+        """Best of `reps` replays of fn captured between two events, in us."""
+        import torch
+        g, (ea, eb) = self.capture(fn, with_events=True)
+        best = None
+        for _ in range(reps):
+            g.replay()
+            torch.cuda.synchronize()
+            t = ea.elapsed_time(eb) * 1e3
+            best = t if best is None else min(best, t)
+        del g
+        return best
+
+    def launch_floor(self, cl, R=20):
+        """A layer of almost no work (depthwise 3x3 on one 8x8x8 bf16 image)
+        R times back to back in one graph, per launch."""
+        import torch
+        tiny = cl.Plan(1, 8, 8, 8, 8, 3, 3, 1, 1, 1, 8, "bf16", "none")
+        tx = torch.zeros(1, 8, 8, 8, dtype=torch.bfloat16, device=self.dev)
+        tw = torch.zeros(8, 3, 3, 1, dtype=torch.bfloat16, device=self.dev)
+        ty = torch.empty(1, 8, 8, 8, dtype=torch.bfloat16, device=self.dev)
+
+        def tiny_run():
+            st = torch.cuda.current_stream(self.dev)
+            for _ in range(R):
+                tiny.run(tx, tw, None, ty, st)
+        tiny_run()
+        torch.cuda.synchronize()
+        return self.graph_us(tiny_run) / R
+
+
+def measure_set(tm, plans, X, Wt, B, Y, pairs=50, R=20):
+    """Per-layer times of one layer set on the GPU, in us:
+      marginal_us  the layer's cost inside the step: the step's graph (the
+                   layers back to back, programmatic dependent launch between
+                   them) minus the same graph without that layer, each replay
+                   after an L2 flush, interleaved, mean of `pairs` replays;
+      evented_us   events recorded between consecutive layers of the step
+                   (they serialise the layers: reads high by the event cost);
+      cold_us / warm_us  the layer alone, R launches in one graph, cold as
+                   [flush, layer] x R minus [flush] x R, warm back to back,
+                   divided by R;
+      step_us      the whole step (mean of the same replays)."""
+    import torch
+    dev, flush = tm.dev, tm.flush
+    nl = len(plans)
+
+    def step_without(skip):
+        def f():
+            st = torch.cuda.current_stream(dev)
+            for i in range(nl):
+                if i != skip:
+                    plans[i].run(X[i], Wt[i], B[i], Y[i], st)
+        return f
+
+    stream = torch.cuda.current_stream(dev)
+    step_without(None)()
+    torch.cuda.synchronize()
+    graphs = [tm.capture(step_without(None))[0]]
+    if nl > 1:
+        graphs += [tm.capture(step_without(i))[0] for i in range(nl)]
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in graphs]
+          for _ in range(pairs)]
+    for k in range(pairs):
+        for j, g in enumerate(graphs):
+            flush.fill_((k + j) & 0xFF)
+            ev[k][j][0].record(stream)
+            g.replay()
+            ev[k][j][1].record(stream)
+    torch.cuda.synchronize()
+    t = np.array([[a.elapsed_time(b) * 1e3 for a, b in row] for row in ev])
+    del graphs
+    step_us = float(t[:, 0].mean())
+    marginal = [step_us] if nl == 1 else [step_us - float(t[:, 1 + i].mean()) for i in range(nl)]
+
+    # events between the layers
+    lev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(nl + 1)]
+
+    def evented_step():
+        st = torch.cuda.current_stream(dev)
+        for i in range(nl):
+            lev[i].record(st)
+            plans[i].run(X[i], Wt[i], B[i], Y[i], st)
+        lev[nl].record(st)
+    gl, _ = tm.capture(evented_step)
+    reps = 10
+    ev_us = np.zeros((reps, nl))
+    for k in range(reps):
+        flush.fill_(k & 0xFF)
+        gl.replay()
+        torch.cuda.synchronize()
+        for i in range(nl):
+            ev_us[k, i] = lev[i].elapsed_time(lev[i + 1]) * 1e3
+    del gl
+
+    def flushes():
+        for r in range(R):
+            flush.fill_(r & 0xFF)
+    t_flush = tm.graph_us(flushes)
+    cold, warm = [], []
+    for i in range(nl):
+        def c(i=i):
+            st = torch.cuda.current_stream(dev)
+            for r in range(R):
+                flush.fill_(r & 0xFF)
+                plans[i].run(X[i], Wt[i], B[i], Y[i], st)
+
+        def w(i=i):
+            st = torch.cuda.current_stream(dev)
+            for _ in range(R):
+                plans[i].run(X[i], Wt[i], B[i], Y[i], st)
+        cold.append((tm.graph_us(c) - t_flush) / R)
+        warm.append(tm.graph_us(w) / R)
+    return {"step_us": step_us, "marginal_us": marginal, "evented_us": list(ev_us.mean(axis=0)),
+            "cold_us": cold, "warm_us": warm}
+
+
+def rate_of(spec, us, peaks):
+    """(achieved, peak, unit, bound) of a layer that took `us`: against its
+    compute roof (TFLOP/s, TOPS for int8, FFMA TFLOP/s for fp32) or HBM
+    (GB/s), whichever its arithmetic intensity puts it under."""
+    from conv_workloads import alg_bytes
+    bound, _ = layer_bound(spec, peaks)
+    if bound != "hbm":
+        unit = "TOPS" if spec.dtype == "i8" else "TFLOP/s"
+        return flops_of(spec) / (us * 1e-6) / 1e12, compute_peak(spec, peaks)[0], unit, bound
+    return alg_bytes(spec) / (us * 1e-6) / 1e9, peaks["hbm_gbs"], "GB/s", bound
+
+
+def layer_row(spec, plan, meas, i, peaks):
+    from conv_workloads import alg_bytes
+    us = max(float(meas["marginal_us"][i]), 1e-3)
+    cold = float(meas["cold_us"][i])
+    ach, pk, unit, bound = rate_of(spec, us, peaks)
+    ach_c = rate_of(spec, cold, peaks)[0]
+    _, ai = layer_bound(spec, peaks)
+    ops = "tops" if spec.dtype == "i8" else "tflops"
+    return {
+        "layer": spec.name, "kernel": plan.describe(), "launches": plan.launches, "us": round(us, 2),
+        "us_evented": round(float(meas["evented_us"][i]), 2),
+        "us_alone_cold": round(cold, 2), "us_alone_warm": round(float(meas["warm_us"][i]), 2),
+        ops: round(flops_of(spec) / (us * 1e-6) / 1e12, 2), "gbs": round(alg_bytes(spec) / (us * 1e-6) / 1e9, 1),
+        "ai_flop_per_byte": round(ai, 1), "bound": bound,
+        "achieved": round(ach, 2), "peak": pk, "unit": unit, "frac": round(ach / pk, 4),
+        "frac_alone_cold": round(ach_c / pk, 4),
+    }
+
+
+def measure_layer_set(cl, dev, tm, cfg, peaks):
+    """One of the other layer sets, each layer planned as a user would plan
+    it, timed as the main set's layers are (measure_set)."""
+    import torch
+    from conv_workloads import generate
+    layers = generate(cfg)
+    plans, X, Wt, B, Y = [], [], [], [], []
+    for d in layers:
+        s = d.spec
+        quant = (s.in_scale, s.out_scale, d.w_scales.tolist()) if s.dtype == "i8" else None
+        p = cl.Plan(s.n, s.h, s.w, s.cin, s.cout, s.kh, s.kw, s.stride, s.pad_h, s.pad_w, s.groups,
+                    s.dtype, s.act, quant)
+        plans.append(p)
+        X.append(d.x.to(dev))
+        Wt.append(d.w.to(dev))
+        B.append(None if d.b is None else d.b.to(dev))
+        Y.append(torch.empty(p.output_shape, dtype=d.x.dtype, device=dev))
+    meas = measure_set(tm, plans, X, Wt, B, Y)
+    rows = [layer_row(d.spec, p, meas, i, peaks) for i, (d, p) in enumerate(zip(layers, plans))]
+    for p in plans:
+        p.check_device_status()
+    flops = sum(flops_of(d.spec) for d in layers)
+    ops = "TOPS" if all(d.spec.dtype == "i8" for d in layers) else "TFLOP/s"
+    return {"step_us": round(meas["step_us"], 2), "rate": round(flops / (meas["step_us"] * 1e-6) / 1e12, 3),
+            "unit": ops, "layers": rows}
 
 
 # ---------------------------------------------------------------- our arm
@@ -215,28 +420,12 @@ def run_ours(args, rank, world, device):
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20)
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
     nl = len(layers)
+    tm = GraphTimer(dev, flush)
 
     def step():
         st = torch.cuda.current_stream(dev)  # the capture stream while capturing
         for i in range(nl):
             plans[i].run(X[i], Wt[i], B[i], Y[i], st)
-
-    def capture(fn, with_events=False):
-        """fn captured as a CUDA graph (optionally between two timing events,
-        external=True so each replay re-records them)."""
-        evs = None
-        if with_events:
-            evs = (torch.cuda.Event(enable_timing=True, external=True),
-                   torch.cuda.Event(enable_timing=True, external=True))
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            st = torch.cuda.current_stream(dev)
-            if evs:
-                evs[0].record(st)
-            fn()
-            if evs:
-                evs[1].record(st)
-        return g, evs
 
     # The step (the layers back to back, nothing between them: consecutive
     # launches overlap through programmatic dependent launch) is captured as
@@ -244,11 +433,16 @@ def run_ours(args, rank, world, device):
     for _ in range(2):
         step()
     torch.cuda.synchronize()
-    graph, _ = capture(step)
+    graph, _ = tm.capture(step)
     torch.cuda.synchronize()
 
+    # Clocks are sampled from the first warm-up replay to the end of the last
+    # timed phase (the step, the per-layer figures, the other layer sets and
+    # the adjacent rows): the step's own timed region is a few milliseconds,
+    # shorter than the sampling period.
     clocks = ClockSampler(device)
     clocks.start()
+    t_sampling = time.perf_counter()
     for _ in range(args.warmup):
         flush.fill_(1)
         graph.replay()
@@ -269,83 +463,12 @@ def run_ours(args, rank, world, device):
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     clocks.mark("t_end")
-    clk = clocks.stop()
     step_ms = np.array([e0[k].elapsed_time(e1[k]) for k in range(args.steps)])
+    del graph
 
-    # Per-layer figures.  (1) In the step: the same step captured with an
-    # event between consecutive layers, replayed `steps` times with the same
-    # L2 flush before each replay; a layer's duration is the mean over the
-    # replays of the time between its two events (the events serialise the
-    # layers, so this graph is not the one `value` times).  (2) Alone: each
-    # layer R times in one graph, cold ([flush, layer] x R minus [flush] x R)
-    # and warm ([layer] x R back to back), divided by R: the timer's ~2 us
-    # tick then costs at most ~0.1 us per launch.
-    def evented_step():
-        st = torch.cuda.current_stream(dev)
-        for i in range(nl):
-            lev[i].record(st)
-            plans[i].run(X[i], Wt[i], B[i], Y[i], st)
-        lev[nl].record(st)
-
-    lev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(nl + 1)]
-    gl, _ = capture(evented_step)
-    per_layer = np.zeros((args.steps, nl))
-    for k in range(args.steps):
-        flush.fill_(k & 0xFF)
-        gl.replay()
-        torch.cuda.synchronize()
-        for i in range(nl):
-            per_layer[k, i] = lev[i].elapsed_time(lev[i + 1])
-    del gl
-
-    R = 20
-
-    def graph_time(fn, reps=5):
-        g, (ea, eb) = capture(fn, with_events=True)
-        best = None
-        for _ in range(reps):
-            g.replay()
-            torch.cuda.synchronize()
-            t = ea.elapsed_time(eb) * 1e3
-            best = t if best is None else min(best, t)
-        del g
-        return best
-
-    def flushes():
-        for r in range(R):
-            flush.fill_(r & 0xFF)
-
-    t_flush = graph_time(flushes)
-    alone_cold = np.zeros(nl)
-    alone_warm = np.zeros(nl)
-    for i in range(nl):
-        def cold(i=i):
-            st = torch.cuda.current_stream(dev)
-            for r in range(R):
-                flush.fill_(r & 0xFF)
-                plans[i].run(X[i], Wt[i], B[i], Y[i], st)
-
-        def warm(i=i):
-            st = torch.cuda.current_stream(dev)
-            for r in range(R):
-                plans[i].run(X[i], Wt[i], B[i], Y[i], st)
-        alone_cold[i] = (graph_time(cold) - t_flush) / R
-        alone_warm[i] = graph_time(warm) / R
-
-    # The per-launch floor: a layer of almost no work (depthwise 3x3 on one
-    # 8x8x8 bf16 image) 20 times back to back in one graph, per launch.
-    tiny = cl.Plan(1, 8, 8, 8, 8, 3, 3, 1, 1, 1, 8, "bf16", "none")
-    tx = torch.zeros(1, 8, 8, 8, dtype=torch.bfloat16, device=dev)
-    tw = torch.zeros(8, 3, 3, 1, dtype=torch.bfloat16, device=dev)
-    ty = torch.empty(1, 8, 8, 8, dtype=torch.bfloat16, device=dev)
-
-    def tiny_run():
-        st = torch.cuda.current_stream(dev)
-        for r in range(R):
-            tiny.run(tx, tw, None, ty, st)
-    tiny_run()
-    torch.cuda.synchronize()
-    launch_floor = graph_time(tiny_run) / R
+    meas = measure_set(tm, plans, X, Wt, B, Y)
+    layer_rows = [layer_row(d.spec, p, meas, i, peaks) for i, (d, p) in enumerate(zip(layers, plans))]
+    launch_floor = tm.launch_floor(cl)
     for p in plans:
         p.check_device_status()
     my_ms = max_over_ranks(float(step_ms.sum()), world, dev)
@@ -353,32 +476,25 @@ def run_ours(args, rank, world, device):
     ms_per_step = my_ms / args.steps
     value = job_tflops(total_flops, world, args.steps, my_ms)
 
-    # ---- per-layer figures and the dominant kernel's roofline
-    layer_rows = []
-    for i, d in enumerate(layers):
-        s = d.spec
-        us = float(per_layer[:, i].mean() * 1e3)
-        bound, ai = layer_bound(s, peaks)
-        fl = flops_of(s)
-        by = alg_bytes(s)
-        if bound != "hbm":
-            ach, pk, unit = fl / (us * 1e-6) / 1e12, compute_peak(s, peaks)[0], "TFLOP/s"
-        else:
-            ach, pk, unit = by / (us * 1e-6) / 1e9, peaks["hbm_gbs"], "GB/s"
-        layer_rows.append({
-            "layer": s.name, "kernel": plans[i].describe(), "us": round(us, 2),
-            "us_alone_cold": round(float(alone_cold[i]), 2), "us_alone_warm": round(float(alone_warm[i]), 2),
-            "tflops": round(fl / (us * 1e-6) / 1e12, 1), "gbs": round(by / (us * 1e-6) / 1e9, 1),
-            "ai_flop_per_byte": round(ai, 1), "bound": bound,
-            "achieved": round(ach, 1), "peak": pk, "unit": unit, "frac": round(ach / pk, 4),
-        })
-    dom = max(range(nl), key=lambda i: per_layer[:, i].mean())
+    # ---- the dominant kernel's roofline: the layer taking the most time in
+    # the step (its marginal time there: the step minus the step without it)
+    dom = max(range(nl), key=lambda i: meas["marginal_us"][i])
     dr = layer_rows[dom]
     traffic = _traffic_for(args.workload, layers[dom].spec.name, plans[dom].describe())
     roofline = {"bound": dr["bound"], "achieved": dr["achieved"], "peak": dr["peak"], "unit": dr["unit"],
                 "frac": dr["frac"], "traffic": traffic, "kernel": layers[dom].spec.name,
+                "duration_us": dr["us"], "duration": "marginal time in the step (CUDA events)",
                 "peak_source": {"tensor": f"{peaks_src} (bf16 burst)", "hbm": f"{peaks_src} (HBM copy)",
                                 "alu": "derived: SMs x 128 FP32 lanes x 2 x max SM clock"}[dr["bound"]]}
+
+    # ---- the other layer sets, each measured the same way (rank 0 only)
+    layer_sets = None
+    if rank == 0 and not args.only and not args.no_layer_sets:
+        layer_sets = {}
+        for cfg in CONFIGS:
+            if cfg == args.workload:
+                continue
+            layer_sets[cfg] = measure_layer_set(cl, dev, tm, cfg, peaks)
 
     # ---- int8 context: the tensor cores' int8 rate as torch exposes it (these
     # layers themselves run as exact bf16 MMAs, so their roof is the bf16 peak)
@@ -413,18 +529,24 @@ def run_ours(args, rank, world, device):
         "config": {"workload": args.workload, "layers": len(layers),
                    "batch_per_gpu": layers[0].spec.n, "l2": "flushed before every step (outside the events)",
                    "launch": "CUDA graph replay of the step, events around each replay; per-layer 'us': "
-                             "the step replayed again with events between its layers (mean over the steps); "
-                             "'us_alone_*': each layer 20x in its own graph",
+                             "the layer's marginal time in the step (the step graph minus the same graph "
+                             "without that layer, L2 flushed before each replay, mean of 50 pairs); "
+                             "'us_evented': events between the layers; 'us_alone_*': each layer 20x in its "
+                             "own graph",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roofline, "layers": layer_rows, "e2e": e2e,
         "peaks": {"bf16_tflops": peaks["bf16_tflops"], "hbm_gbs": peaks["hbm_gbs"],
                   "fp32_ffma_tflops": peaks["fp32_ffma_tflops"], "source": peaks_src,
                   "int8_probe": int8_probe},
+        "layer_sets": layer_sets,
         "next_rows": measure_next_rows(dev, peaks) if rank == 0 and not args.no_next_rows else None,
         "launch_floor_us": round(float(launch_floor), 2),
-        "gpu_launches": sum(p.launches for p in plans) * args.steps, "clocks": clk,
+        "gpu_launches": sum(p.launches for p in plans) * args.steps,
         "wall_s_timed_region": round(wall, 4),
     }
+    torch.cuda.synchronize()
+    clocks.mark("t_last")
+    out["clocks"] = clocks.stop(time.perf_counter() - t_sampling)
     return out
 
 
@@ -760,6 +882,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next-rows", action="store_true", help="skip timing the residual / concat / SPP rows")
+    ap.add_argument("--no-layer-sets", action="store_true", help="skip timing the other layer sets")
     ap.add_argument("--only", default="",
                     help="run only these layers of the set (comma-separated names; for profiler captures)")
     ap.add_argument("--profile-pass", action="store_true",
