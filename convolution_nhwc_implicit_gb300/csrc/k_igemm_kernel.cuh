@@ -267,20 +267,25 @@ __device__ __forceinline__ void epilogue_swapped(const IgArgs &a, int tile, uint
 // general epilogue's.
 // FUSED: the layer has a residual or writes upsample replicas (a separate
 // instantiation, so that the plain epilogue carries none of that code).
-template <int kCols, bool FUSED>
-__device__ __forceinline__ void epilogue_swapped_bf16(const IgArgs &a, int tile, uint32_t taddr, uint32_t tempty,
-                                                      int grp, int c_base, uint8_t *tbuf, int gt, int q, int lane) {
-    const int nb = tile % a.tiles_n;
-    const int mt = tile / a.tiles_n;
-    // this thread's channels (within the 128-channel block): 32q + 16h + 8j + lane/4
-    float fb[2][2];
+// The bias of the thread's channels (32q + 16h + 8j + lane/4 of the layer's
+// single 128-channel block), read once per CTA rather than per tile (a
+// global load's latency on every tile's critical path).
+__device__ __forceinline__ void swapped_bias(const IgArgs &a, int q, int lane, float (&fb)[2][2]) {
 #pragma unroll
     for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const int co = nb * 128 + 32 * q + 16 * h + 8 * j + (lane >> 2);
+            const int co = 32 * q + 16 * h + 8 * j + (lane >> 2);
             fb[h][j] = (a.bias && co < a.Cout) ? __ldg(reinterpret_cast<const float *>(a.bias) + co) : 0.0f;
         }
+}
+
+template <int kCols, bool FUSED>
+__device__ __forceinline__ void epilogue_swapped_bf16(const IgArgs &a, int tile, uint32_t taddr, uint32_t tempty,
+                                                      int grp, int c_base, uint8_t *tbuf, int gt, int q, int lane,
+                                                      const float (&fb)[2][2]) {
+    const int nb = tile % a.tiles_n;
+    const int mt = tile / a.tiles_n;
     // the slice in registers, then the TMEM buffer goes back to the MMA warp
     uint32_t acc[2][kCols / 8][4];  // [lane half][8-column group][fragment registers]
 #pragma unroll
@@ -311,6 +316,12 @@ __device__ __forceinline__ void epilogue_swapped_bf16(const IgArgs &a, int tile,
     const int wpx = gt >> 3;
     const int wco = nb * 128 + (gt & 7) * 16;
     const __nv_bfloat16 *res = FUSED ? reinterpret_cast<const __nv_bfloat16 *>(a.om.res) : nullptr;
+    // this thread's output pixel of every chunk, located up front (off the
+    // chunks' barrier-to-barrier path)
+    long long ybs[kCols / 16];
+    bool vals[kCols / 16];
+#pragma unroll
+    for (int i = 0; i < kCols / 16; ++i) swapped_pixel(a, m0, n, oh0, ow0, c_base + 16 * i + wpx, ybs[i], vals[i]);
 #pragma unroll
     for (int c = 0; c < kCols; c += 16) {
         // residual rows of this thread's four pixels of the chunk (pixels
@@ -349,14 +360,10 @@ __device__ __forceinline__ void epilogue_swapped_bf16(const IgArgs &a, int tile,
             tc::stmatrix_x4_trans(srow + (uint32_t)(16 * h * 2), fr[0], fr[1], fr[2], fr[3]);
         }
         tc::named_bar_sync(1 + grp, 128);
-        const int p = c_base + c + wpx;  // pixel index inside the tile
-        long long yb;
-        bool valid;
-        swapped_pixel(a, m0, n, oh0, ow0, p, yb, valid);
-        if (valid) {
+        if (vals[c / 16]) {
             const uint4 *src = reinterpret_cast<const uint4 *>(tbuf + wpx * kTP + (gt & 7) * 32);
             const uint4 v0 = src[0], v1 = src[1];
-            __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(a.y) + yb + wco;
+            __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(a.y) + ybs[c / 16] + wco;
             const int up = FUSED ? a.om.up : 1;
             for (int dy = 0; dy < up; ++dy)
                 for (int dx = 0; dx < up; ++dx) {
@@ -371,8 +378,12 @@ __device__ __forceinline__ void epilogue_swapped_bf16(const IgArgs &a, int tile,
 // SWAP = false: MMA M = 128 pixels, N = BN output channels (D[pixel][co]).
 // SWAP = true (layers with Cout <= 128): the operands trade places, MMA M =
 // 128 output channels (weights as A), N = 256 pixels (activations as B),
-// D[co][pixel]; every MMA then has N = 256, the only width at which tcgen05
-// reaches its peak rate (the issue cost of an MMA does not shrink with N).
+// D[co][pixel]; every MMA then has N = 256.  Measured on GB300 (one thread
+// issuing back to back, M = 128, K = 16): 48 / 64 / 128 cycles for N = 64 /
+// 128 / 256.  Up to N = 128 that is the time to read the operands from shared
+// memory at 128 bytes a cycle ((128 + N) rows of 32 bytes); at N = 256 it is
+// the tensor core's own rate, with a quarter of the shared-memory bandwidth
+// left over for the TMA writes and the epilogue.
 //
 // PAIR (normal layout only): a cluster of two CTAs on two SMs computes a
 // 256-pixel x BN tile with tcgen05's CTA-pair MMA (M = 256).  Each CTA stages
@@ -1006,6 +1017,9 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         if (CVT == 1 && unit < a.num_tiles) widen_weights();
         // lt: the CTA's local tile index (EPT: this group's tiles, every 4th)
         const int lt0 = EPT ? grp : 0, lstep = EPT ? kGroups : 1;
+        // swapped bf16 layers: this thread's bias values, read once
+        float swb[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+        if (SWAP && !a.out_i8) swapped_bias(a, q, lane, swb);
         // (single CTAs: the tiles' coordinates advanced without division)
         TileWalk walk;
         walk.init(a, unit + lt0 * units, lstep * units);
@@ -1026,7 +1040,7 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                                    threadIdx.x - 64 - grp * 128);
                 else
                     epilogue_swapped_bf16<kCols, FUSED>(a, tile, ta, tempty_bar(buf), grp, c_base, tb,
-                                                        threadIdx.x - 64 - grp * 128, q, lane);
+                                                        threadIdx.x - 64 - grp * 128, q, lane, swb);
                 continue;
             }
             // Plain layers pull this thread's whole accumulator slice out of
