@@ -150,8 +150,14 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
     // cost + a fixed cost), the per-tile cost (per SM) being the larger of
     //   the ring  stages per tile x (per-stage time + ~200 cycles of barrier
     //             round trip), a stage taking the longest of
-    //               its MMAs     128 cycles per K = 16 step whatever N is (N =
-    //                            256 is the only full-rate width; measured),
+    //               its MMAs     128 cycles per K = 16 step whatever N is (an
+    //                            M = 128 MMA alone takes 48 / 64 / 128 cycles for
+    //                            N = 64 / 128 / 256, below N = 256 the time to read
+    //                            its operands from shared memory at 128 bytes a
+    //                            cycle; beside the TMA writes and the epilogue,
+    //                            which share that bandwidth, N <= 128 tiles ran no
+    //                            faster per output than N = 256 in every layer
+    //                            measured, which this flat charge models),
     //               its TMA rows ~1.4 cycles per staged operand row (a pixel's
     //                            or an output channel's BK channels),
     //               the refill   a freed stage is refilled ~2000 cycles later:
