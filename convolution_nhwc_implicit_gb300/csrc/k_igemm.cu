@@ -287,7 +287,10 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
                         if (2 * wblocks * bnc * bk > per_cta * P * cin) continue;
                     }
                     const int one_buf = swap ? 4 * 16 * kTP : epi_groups(bn, false, c.ept != 0) * kBM * 64;
-                    c.out_bufs = 1;
+                    // swapped plain bf16 layers whose 16-pixel chunks lie in one row
+                    // write out by TMA stores from two staging buffers per group
+                    const bool swap_tma = swap && !igemm_fused(p) && p->dtype == CONV_BF16 && (g.flat || c.bw % 16 == 0);
+                    c.out_bufs = swap_tma ? 2 : 1;
                     if (!swap && wblocks < 16 && (smem_cap - 2 * one_buf) / ((long long)c.a_stage + wblock) >= 4)
                         c.out_bufs = 2;
                     const long long out_bytes = (long long)one_buf * c.out_bufs;
@@ -335,7 +338,11 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
                     const long long slots = pair ? p->num_sms / 2 : p->num_sms;
                     const long long waves = (c.units + slots - 1) / slots;
                     c.rows = ring_kb * box_rows + (c.wres ? 0 : wblocks * bnc);  // staged rows per tile
-                    const long long t_epi = 128LL * (swap ? P : bn) * epi_c / 128;
+                    // (the staged swapped write-out -- shared-memory loads, global
+                    // stores and their address arithmetic in the epilogue threads --
+                    // adds ~650 cycles per 16-pixel chunk, measured; the TMA
+                    // write-out moves that to the TMA engine)
+                    const long long t_epi = 128LL * (swap ? P : bn) * epi_c / 128 + (swap && c.out_bufs == 1 ? 2600 : 0);
                     // a stage: its MMAs, its TMA rows, or the ring's refill latency
                     // spread over the other stages, whichever is longest, plus a
                     // fixed cost of the stage's barrier round trip
@@ -347,15 +354,21 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
                     const long long t_ring = ring_kb * (per_stage + 200);
                     const long long t_tile = t_ring > t_epi ? t_ring : t_epi;
                     const long long cost = waves * (t_tile + 500);
-                    // ties: more work units (more SMs busy), then fewer staged
-                    // rows, then the narrower N tile
+                    // ties: the TMA write-out of the swapped layout (measured faster
+                    // than the staged one at equal estimates: 64->128 @160 batch 8,
+                    // 8x32 tiles 24.7 us warm against 29.8 for 10x24 staged), more
+                    // work units (more SMs busy), then fewer staged rows, then the
+                    // narrower N tile
                     Cand &best = bests[cvt];
                     long long &best_cost = best_costs[cvt];
+                    const int tma_c = swap && c.out_bufs == 2, tma_b = best.swap && best.out_bufs == 2;
                     const bool better =
                         best_cost < 0 || cost < best_cost ||
                         (cost == best_cost &&
-                         (c.units > best.units ||
-                          (c.units == best.units && (c.rows < best.rows || (c.rows == best.rows && bn < best.bn)))));
+                         (tma_c > tma_b ||
+                          (tma_c == tma_b &&
+                           (c.units > best.units ||
+                            (c.units == best.units && (c.rows < best.rows || (c.rows == best.rows && bn < best.bn)))))));
                     if (better) {
                         best_cost = cost;
                         best = c;
@@ -531,7 +544,25 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
         for (int rp = 0; rp < up * up; ++rp) {
             const int dy = rp / up, dx = rp % up;
             char *base = static_cast<char *>(y) + ((cuuint64_t)p->y_coff + ((cuuint64_t)dy * OWy + dx) * Cy) * es;
-            if (g.flat) {  // (up == 1)
+            if (g.swap && g.out_bufs == 2) {
+                // swapped TMA write-out: [16 pixels][64 channels] boxes, 128-byte swizzle
+                if (g.flat) {
+                    const cuuint64_t dims[2] = {(cuuint64_t)p->s.c_out, (cuuint64_t)p->s.n * p->oh * p->ow};
+                    const cuuint64_t strides[1] = {Cy * es};
+                    const cuuint32_t box[2] = {64, 16};
+                    rc = encode(&tmY.m[rp], dt, 2, base, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                } else {
+                    const cuuint64_t dims[4] = {(cuuint64_t)p->s.c_out, (cuuint64_t)p->ow, (cuuint64_t)p->oh,
+                                                (cuuint64_t)p->s.n};
+                    const cuuint64_t strides[3] = {Cy * es, OWy * Cy * es, OHy * OWy * Cy * es};
+                    const cuuint32_t box[4] = {64, 16, 1, 1};
+                    rc = encode(&tmY.m[rp], dt, 4, base, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                }
+            } else if (g.flat) {  // (up == 1)
                 const cuuint64_t dims[2] = {(cuuint64_t)p->s.c_out, (cuuint64_t)p->s.n * p->oh * p->ow};
                 const cuuint64_t strides[1] = {Cy * es};
                 const cuuint32_t box[2] = {box_n, (cuuint32_t)(g.swap ? kBMSwap : kBM)};

@@ -375,6 +375,99 @@ __device__ __forceinline__ void epilogue_swapped_bf16(const IgArgs &a, int tile,
     }
 }
 
+// Swapped-mode bf16 epilogue whose write-out is a TMA tensor store (plain
+// layers whose tile width is a multiple of 16, or flat tiles: a 16-pixel
+// chunk is then one row segment of y).  The fragments are transposed by
+// stmatrix as in epilogue_swapped_bf16, but into two 128-byte-swizzled
+// [16 pixels][64 channels] boxes, the layout of the store's tensor map
+// (chunk j of row r at chunk j ^ (r mod 8): the eight rows of a fragment on
+// distinct banks), double-buffered per warpgroup; the group's first thread
+// then issues the stores and the group goes on to the next chunk while the
+// TMA engine reads the buffer.  The threads' own shared-memory loads, global
+// stores and address arithmetic of the write-out disappear.
+template <int kCols>
+__device__ __forceinline__ void epilogue_swapped_tma(const IgArgs &a, const CUtensorMap *tmY, int mt, uint32_t taddr,
+                                                     uint32_t tempty, int grp, int c_base, uint32_t sbuf0, int q,
+                                                     int lane, bool issuer, int &oc, const float (&fb)[2][2]) {
+    uint32_t acc[2][kCols / 8][4];  // [lane half][8-column group][fragment registers]
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int g = 0; g < kCols / 8; ++g)
+            tc::tmem_ld_16x256(taddr + ((uint32_t)(16 * h) << 16) + (uint32_t)(8 * g), acc[h][g]);
+    tc::tmem_ld_wait();
+    tc::fence_before_sync();
+    tc::mbar_arrive(tempty);
+
+    int n = 0, oh0 = 0, ow0 = 0;
+    long long m0 = 0;
+    if (a.flat) {
+        m0 = (long long)mt * kBMSwap;
+    } else {
+        const int tw = mt % a.tiles_w;
+        const int t2 = mt / a.tiles_w;
+        oh0 = (t2 % a.tiles_h) * a.bh;
+        n = t2 / a.tiles_h;
+        ow0 = tw * a.bw;
+    }
+    // the chunk's tile row and first column (16-pixel chunks stay in one row)
+    int dh = a.flat ? 0 : c_base / a.bw;
+    int dw = a.flat ? 0 : c_base - dh * a.bw;
+    // stmatrix row address of this thread in a buffer: matrix m = lane / 8
+    // (pixels 8 (m / 2) + 0..7, channels 32q + 16h + 8 (m % 2) + 0..7), row
+    // lane % 8: pixel r, 16-byte chunk 4q + 2h + m % 2 of its 256-byte row,
+    // i.e. box q / 2, swizzled chunk (4 (q % 2) + 2h + m % 2) ^ (r % 8)
+    const int r = 8 * (lane >> 4) + (lane & 7);
+    const uint32_t roff = (uint32_t)((q >> 1) * 2048 + r * 128);
+    uint32_t coff[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+        coff[h] = roff + ((uint32_t)((4 * (q & 1) + 2 * h + ((lane >> 3) & 1)) ^ (r & 7)) << 4);
+    const bool two_boxes = a.Cout > 64;
+#pragma unroll
+    for (int c = 0; c < kCols; c += 16) {
+        const uint32_t sb = sbuf0 + (uint32_t)(oc & 1) * 4096u;
+        // the store that last read this buffer (two chunks ago) has read it
+        if (issuer) tc::bulk_wait_read1();
+        tc::named_bar_sync(1 + grp, 128);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t fr[4];
+#pragma unroll
+            for (int gg = 0; gg < 2; ++gg) {
+                const uint32_t(&rv)[4] = acc[h][c / 8 + gg];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float2 v = activate2_fast(
+                        make_float2(__uint_as_float(rv[2 * j]) + fb[h][j], __uint_as_float(rv[2 * j + 1]) + fb[h][j]),
+                        a.act);
+                    __nv_bfloat162 b2 = __floats2bfloat162_rn(v.x, v.y);
+                    fr[2 * gg + j] = *reinterpret_cast<uint32_t *>(&b2);
+                }
+            }
+            tc::stmatrix_x4_trans(sb + coff[h], fr[0], fr[1], fr[2], fr[3]);
+        }
+        tc::fence_proxy_async_smem();  // the staged values visible to the TMA engine
+        tc::named_bar_sync(1 + grp, 128);
+        if (issuer) {
+            if (a.flat) {
+                const int row0 = (int)(m0 + c_base + c);
+                tc::tma_store_2d(tmY, sb, 0, row0);
+                if (two_boxes) tc::tma_store_2d(tmY, sb + 2048u, 64, row0);
+            } else if (dh < a.bh) {  // (rows past the tile belong to the next tile)
+                tc::tma_store_4d(tmY, sb, 0, ow0 + dw, oh0 + dh, n);
+                if (two_boxes) tc::tma_store_4d(tmY, sb + 2048u, 64, ow0 + dw, oh0 + dh, n);
+            }
+            tc::bulk_commit();
+        }
+        ++oc;
+        if (!a.flat) {
+            dw += 16;
+            if (dw >= a.bw) { dw -= a.bw; ++dh; }
+        }
+    }
+}
+
 // SWAP = false: MMA M = 128 pixels, N = BN output channels (D[pixel][co]).
 // SWAP = true (layers with Cout <= 128): the operands trade places, MMA M =
 // 128 output channels (weights as A), N = 256 pixels (activations as B),
@@ -1035,6 +1128,13 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             if constexpr (SWAP) {
                 const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kAcc + c_base);
                 uint8_t *tb = gbase + (sOut - base) + grp * a.out_bufs * kOutStage;
+                if constexpr (!FUSED) {
+                    if (a.out_bufs == 2) {  // plain bf16, 16-pixel chunks in one row: TMA-store write-out
+                        epilogue_swapped_tma<kCols>(a, &tmY.m[0], tile, ta, tempty_bar(buf), grp, c_base,
+                                                    sOut + (uint32_t)(grp * 2) * 4096u, q, lane, issuer, oc, swb);
+                        continue;
+                    }
+                }
                 if (a.out_i8)
                     epilogue_swapped<kCols, FUSED>(a, tile, ta, tempty_bar(buf), row, grp, c_base, tb,
                                                    threadIdx.x - 64 - grp * 128);
