@@ -84,3 +84,31 @@ def test_traffic_is_reported_only_for_the_captured_kernel():
         assert got == e["bytes_per_launch"]
     else:
         assert got is None
+
+
+def test_rate_units_per_roof():
+    # int8 layers on the tensor roof are reported in TOPS, bf16 in TFLOP/s,
+    # memory-bound layers in GB/s against the HBM peak
+    vww = {s.name: s for s in CONFIGS["vww_int8"]}
+    ach, pk, unit, bound = bench.rate_of(vww["conv3x3_64to64_96"], 10.0, PEAKS)
+    assert (unit, bound, pk) == ("TOPS", "tensor", PEAKS["bf16_tflops"])
+    assert ach == pytest.approx(bench.flops_of(vww["conv3x3_64to64_96"]) / 10e-6 / 1e12)
+    dw = next(s for s in CONFIGS["sweep_b8_bf16"] if s.name == "dw3x3_512_40")
+    ach, pk, unit, bound = bench.rate_of(dw, 8.0, PEAKS)
+    assert (unit, bound, pk) == ("GB/s", "hbm", PEAKS["hbm_gbs"])
+    assert ach == pytest.approx(alg_bytes(dw) / 8e-6 / 1e9)
+
+
+def test_layer_row_takes_its_fraction_from_the_time_in_the_step():
+    class FakePlan:
+        launches = 1
+
+        def describe(self):
+            return "fake"
+    spec = next(s for s in CONFIGS["sweep_b8_bf16"] if s.name == "conv3x3_512to1024_40")
+    meas = {"marginal_us": [70.0], "evented_us": [75.0], "cold_us": [72.0], "warm_us": [69.0]}
+    row = bench.layer_row(spec, FakePlan(), meas, 0, PEAKS)
+    assert row["us"] == 70.0 and row["us_alone_cold"] == 72.0
+    assert row["frac"] == pytest.approx(bench.flops_of(spec) / 70e-6 / 1e12 / PEAKS["bf16_tflops"], rel=1e-3)
+    assert row["frac_alone_cold"] < row["frac"]
+    assert row["unit"] == "TFLOP/s" and row["bound"] == "tensor"
