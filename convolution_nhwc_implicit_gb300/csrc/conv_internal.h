@@ -32,6 +32,7 @@ struct IgemmGeom {
     int halo;      // 1: halo staging (a stage holds the tile's input rows for all k_h taps of one column shift)
     int a_stage;   // bytes of the activation part of a ring stage
     int ept;       // 1: one epilogue per tile (each warpgroup drains whole tiles, four TMEM accumulators)
+    int bias_smem; // 1: the bias (and int8 multipliers) copied into shared memory once per CTA
     int cvt;       // 1: int8 operands widened to bf16 in the kernel (converter warpgroup), no pre-pass
     int raw_stage; // cvt: bytes of a raw int8 activation stage
     int raw_region;  // cvt: bytes of the raw region (raw weights, then the raw ring)

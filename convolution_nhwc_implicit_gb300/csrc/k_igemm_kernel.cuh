@@ -82,6 +82,8 @@ struct IgArgs {
     int out_i8;          // 1: int8 output, requantised with mult[co]
     const float *mult;   // int8: requantisation multipliers M[co]
     int out_bufs;        // normal mode: output staging buffers per epilogue group (1 or 2)
+    int bias_smem;       // 1: the epilogue warps copy the bias (and the int8 multipliers)
+                         //    into shared memory once per CTA and read them from there
     int wres;            // 1: the layer's whole weight tensor (one N block; in pair mode this
                          //    CTA's half of it) is loaded once per CTA and stays in shared
                          //    memory; the ring then holds activations only
@@ -588,6 +590,9 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const uint32_t wraw_bar = sBar + 8u * (4 * stages + 9);
     uint8_t *gmisc = gbase + (sBar - base) + 8u * (CVT ? 4 * stages + 10 : 2 * stages + 9);
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(gmisc);
+    // the bias copy (fp32 or int32 [Cout]) and, int8, the multipliers [Cout]
+    const uint32_t sBias = (sBar + 8u * (CVT ? 4 * stages + 10 : 2 * stages + 9) + 16u + 15u) & ~15u;
+    const uint32_t sMult = sBias + (uint32_t)((a.Cout * 4 + 15) & ~15);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gmisc + 4);
 
     const int warp = threadIdx.x >> 5;
@@ -1098,6 +1103,23 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         // run of four consecutive warps covers the 128 accumulator rows; warp
         // group g (warps 2 + 4g .. 5 + 4g) drains columns [g * kCols, (g+1) * kCols)
         // (EPT: all columns of every 4th tile, from accumulator g).
+        // The bias (and the int8 multipliers), once per CTA into shared
+        // memory: the epilogue of each tile then reads them there instead of
+        // waiting on global loads (~0.5 us on a layer of one tile per CTA).
+        if (a.bias_smem) {
+            const int et = (int)threadIdx.x - 64;
+            for (int i = et; i < a.Cout; i += 128 * kGroups) {
+                if (a.bias) {
+                    const uint32_t bv = __ldg(reinterpret_cast<const uint32_t *>(a.bias) + i);
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(sBias + 4u * (uint32_t)i), "r"(bv) : "memory");
+                }
+                if (a.out_i8) {
+                    const uint32_t mv = __float_as_uint(__ldg(a.mult + i));
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(sMult + 4u * (uint32_t)i), "r"(mv) : "memory");
+                }
+            }
+            tc::named_bar_sync(5, 128 * kGroups);
+        }
         const int q = warp & 3;
         const int grp = (warp - 2) >> 2;
         const int row = q * 32 + lane;
@@ -1241,8 +1263,18 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     for (int e = 0; e < 32; ++e) {
                         const int cc = co + e;
                         long long v = (long long)__float2int_rn(__uint_as_float(av[e]));
-                        if (a.bias) v += (long long)__ldg(reinterpret_cast<const int32_t *>(a.bias) + cc);
-                        const int q = requant_i8(v, __ldg(a.mult + cc), a.act);
+                        float mlt;
+                        if (a.bias_smem) {
+                            int32_t bi = 0;
+                            if (a.bias)
+                                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(bi) : "r"(sBias + 4u * (uint32_t)cc));
+                            v += (long long)bi;
+                            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(mlt) : "r"(sMult + 4u * (uint32_t)cc));
+                        } else {
+                            if (a.bias) v += (long long)__ldg(reinterpret_cast<const int32_t *>(a.bias) + cc);
+                            mlt = __ldg(a.mult + cc);
+                        }
+                        const int q = requant_i8(v, mlt, a.act);
                         if ((e & 3) == 0) pk[e >> 2] = 0u;
                         pk[e >> 2] |= ((uint32_t)(q & 0xff)) << (8 * (e & 3));
                     }
@@ -1260,9 +1292,18 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 #pragma unroll
                         for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(av[8 * j + e]);
                         if (a.bias && co + 8 * j < a.Cout) {  // Cout % 8 == 0: 8 columns all in or all out
-                            const float *fb = reinterpret_cast<const float *>(a.bias) + co + 8 * j;
-                            const float4 b0 = __ldg(reinterpret_cast<const float4 *>(fb));
-                            const float4 b1 = __ldg(reinterpret_cast<const float4 *>(fb) + 1);
+                            float4 b0, b1;
+                            if (a.bias_smem) {
+                                const uint32_t sb = sBias + 4u * (uint32_t)(co + 8 * j);
+                                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                             : "=f"(b0.x), "=f"(b0.y), "=f"(b0.z), "=f"(b0.w) : "r"(sb));
+                                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                             : "=f"(b1.x), "=f"(b1.y), "=f"(b1.z), "=f"(b1.w) : "r"(sb + 16u));
+                            } else {
+                                const float *fb = reinterpret_cast<const float *>(a.bias) + co + 8 * j;
+                                b0 = __ldg(reinterpret_cast<const float4 *>(fb));
+                                b1 = __ldg(reinterpret_cast<const float4 *>(fb) + 1);
+                            }
                             v[0] += b0.x; v[1] += b0.y; v[2] += b0.z; v[3] += b0.w;
                             v[4] += b1.x; v[5] += b1.y; v[6] += b1.z; v[7] += b1.w;
                         }

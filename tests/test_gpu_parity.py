@@ -448,3 +448,23 @@ def test_repeated_runs_are_deterministic():
     y1, _ = run_gpu(spec, d, plan=plan)
     y2, _ = run_gpu(spec, d, plan=plan)
     assert torch.equal(y1, y2)
+
+
+# The swapped layout's two write-outs: TMA tensor stores from swizzled staging
+# (plain bf16 layers whose tile width is a multiple of 16, and flat tiles:
+# "out_bufs=2") and the staged transpose written by the threads (other
+# widths, int8, output options: "out_bufs=1").  Ragged widths and heights put
+# part of the last tiles outside the image (clipped stores).
+SWAP_WRITE_OUT = [
+    (L("swap_tma_ragged", 2, 21, 45, 64, 128, 3, 3, 1, 1, 1), "out_bufs=2"),
+    (L("swap_tma_cout64", 1, 17, 33, 32, 64, 3, 3, 1, 1, 1, act="relu"), "out_bufs=2"),
+    (L("swap_tma_flat", 2, 15, 17, 64, 96, 1, 1, act="none"), "out_bufs=2"),
+    (L("swap_staged_w8", 3, 19, 8, 64, 128, 3, 3, 1, 1, 1), "out_bufs=1"),
+    (L("swap_staged_i8", 1, 21, 45, 64, 64, 3, 3, 1, 1, 1, dtype="i8"), "out_bufs=1"),
+]
+
+
+@pytest.mark.parametrize("spec,want", SWAP_WRITE_OUT, ids=[s.name for s, _ in SWAP_WRITE_OUT])
+def test_swapped_write_out_paths(spec, want):
+    plan = check(spec, "igemm_swapped", "igemm")
+    assert "swapped" in plan.describe() and want in plan.describe(), plan.describe()
