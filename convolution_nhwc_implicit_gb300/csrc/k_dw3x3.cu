@@ -307,6 +307,19 @@ __global__ void __launch_bounds__(CBV * TW / 2, (CBV * TW / 2) <= 128 ? 4 : 2)
 dw3x3_bf16_rows_kernel(const __grid_constant__ CUtensorMap tmX, const __nv_bfloat16 *__restrict__ w,
                        const DwArgs a) {
     pdl_trigger();  // see conv_launch
+    // Before waiting for the previous kernel: the halos of this CTA's first
+    // tiles into L2 (while that kernel's last CTAs run on other SMs)
+    if (threadIdx.x == 0) {
+        tc::tma_prefetch_desc(&tmX);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {  // (the two halo buffers' first tiles)
+            const int t = (int)blockIdx.x + j * (int)gridDim.x;
+            if (t < a.tiles_total) {
+                const DwTile d = tile_of(a, t);
+                tc::tma_prefetch_l2_4d(&tmX, d.tcb * CBV * 4, d.ow0 - a.pad_w, d.oh0 - a.pad_h, d.n);
+            }
+        }
+    }
     pdl_wait();
     constexpr int kWin = TW + 2, kHin = TH + 2;
     constexpr uint32_t kPix = CBV * 8;  // bytes of one halo pixel: CBV vectors of 4 bf16

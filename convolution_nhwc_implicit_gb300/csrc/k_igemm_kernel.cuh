@@ -646,6 +646,42 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     // set-up done: let the next kernel be scheduled, and wait for the
     // previous one's writes before the first global access
     pdl_trigger();
+    // Before that wait, the operand boxes of this CTA's first ring stages go
+    // into L2 (when the previous kernel's last CTAs still run on other SMs,
+    // its tail hides their latency).  L2 is where global writes land, so this
+    // cannot serve stale bytes to the loads after the wait.
+    if (!CVT && threadIdx.x == 0 && unit < a.num_tiles) {
+        const int tile = unit;
+        const int nb = tile % a.tiles_n;
+        const int mt = PAIR ? (tile / a.tiles_n) * 2 + (int)rank : tile / a.tiles_n;
+        int n = 0, oh0 = 0, ow0 = 0;
+        if (!FLAT) {
+            const int tw = mt % a.tiles_w;
+            const int t2 = mt / a.tiles_w;
+            oh0 = (t2 % a.tiles_h) * a.bh;
+            n = t2 / a.tiles_h;
+            ow0 = tw * a.bw;
+        }
+        const int kpre = a.kblocks < stages ? a.kblocks : stages;
+        int r = 0, s = 0, cb = 0;
+        for (int kb = 0; kb < kpre; ++kb) {
+            if (FLAT) {
+                tc::tma_prefetch_l2_2d(&tmA, cb * BK, mt * kPix);
+            } else if (HALO) {
+                tc::tma_prefetch_l2_4d(&tmA, cb * BK, ow0 - a.pad_w + s, oh0 - a.pad_h, n);
+            } else {
+                tc::tma_prefetch_l2_4d(&tmA, cb * BK, ow0 * a.stride - a.pad_w + s, oh0 * a.stride - a.pad_h + r, n);
+            }
+            if (!wres) {
+                const int kx = ((HALO ? 0 : r) * a.KW + s) * a.Cin + cb * BK;
+                tc::tma_prefetch_l2_2d(&tmB, kx, nb * BN + (PAIR ? (int)rank * kBRows : 0));
+            }
+            if (++cb == a.cblocks) {
+                cb = 0;
+                if (++s == a.KW) { s = 0; if (!HALO) ++r; }
+            }
+        }
+    }
     pdl_wait();
 
     // CVT == 1: int8 -> bf16 (exact) into the swizzled K-major operand, rows

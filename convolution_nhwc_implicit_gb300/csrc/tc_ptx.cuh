@@ -113,6 +113,23 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *tm,
         : "memory");
 }
 
+// Prefetch of a tensor box into L2 (no shared memory, no barrier).  L2 is
+// where global writes land, so a prefetch issued before the previous kernel
+// on the stream has finished writing the same bytes cannot leave stale data
+// behind for later loads.
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap *tm, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *tm, int c0, int c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(tm)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 // Loads into this CTA's shared memory whose completion is counted on an
 // mbarrier of either CTA of a CTA pair (`bar`: shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *tm, uint32_t bar, int c0,
