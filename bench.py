@@ -235,7 +235,9 @@ def measure_set(tm, plans, X, Wt, B, Y, pairs=50, R=20):
       marginal_us  the layer's cost inside the step: the step's graph (the
                    layers back to back, programmatic dependent launch between
                    them) minus the same graph without that layer, each replay
-                   after an L2 flush, interleaved, mean of `pairs` replays;
+                   after an L2 flush, interleaved, mean of `pairs` replays (a
+                   set of one layer: the graph of the layer twice minus the
+                   graph of it once);
       evented_us   events recorded between consecutive layers of the step
                    (they serialise the layers: reads high by the event cost);
       cold_us / warm_us  the layer alone, R launches in one graph, cold as
@@ -254,12 +256,19 @@ def measure_set(tm, plans, X, Wt, B, Y, pairs=50, R=20):
                     plans[i].run(X[i], Wt[i], B[i], Y[i], st)
         return f
 
+    def twice():  # (a set of one layer: the graph of the layer run twice)
+        st = torch.cuda.current_stream(dev)
+        for _ in range(2):
+            plans[0].run(X[0], Wt[0], B[0], Y[0], st)
+
     stream = torch.cuda.current_stream(dev)
     step_without(None)()
     torch.cuda.synchronize()
     graphs = [tm.capture(step_without(None))[0]]
     if nl > 1:
         graphs += [tm.capture(step_without(i))[0] for i in range(nl)]
+    else:
+        graphs.append(tm.capture(twice)[0])
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in graphs]
           for _ in range(pairs)]
     for k in range(pairs):
@@ -272,7 +281,10 @@ def measure_set(tm, plans, X, Wt, B, Y, pairs=50, R=20):
     t = np.array([[a.elapsed_time(b) * 1e3 for a, b in row] for row in ev])
     del graphs
     step_us = float(t[:, 0].mean())
-    marginal = [step_us] if nl == 1 else [step_us - float(t[:, 1 + i].mean()) for i in range(nl)]
+    # a layer's cost in the step; for a set of one layer, what a second copy
+    # of it adds to the graph (the graph's own launch cost is not the layer's)
+    marginal = ([float(t[:, 1].mean()) - step_us] if nl == 1
+                else [step_us - float(t[:, 1 + i].mean()) for i in range(nl)])
 
     # events between the layers
     lev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(nl + 1)]
