@@ -700,6 +700,10 @@ int dw3x3_configure(conv_plan *p) {
     int th = kMaxTh;
     if (th > p->oh) th = p->oh;
     while ((th - 1) * S + 3 > 256) --th;
+    // Small layers: fewer output rows per tile (a shorter serial walk per
+    // thread) until there is a tile per SM.
+    const long long col_tiles = (long long)((p->ow + best_tw - 1) / best_tw) * ((cvt + cbv - 1) / cbv) * p->s.n;
+    while (th > 1 && col_tiles * ((p->oh + th - 1) / th) < (long long)p->num_sms) th = (th + 1) / 2;
     DwGeom &g = p->dw;
     g.tw = best_tw;
     g.th = th;
