@@ -150,86 +150,83 @@ __global__ void __launch_bounds__(kThreads) spp_kernel(const uint4 *__restrict__
     store_tile(A, 0, y, a, n, h0, w0, cv0, 2);
 }
 
-// Whole-image variant, for images whose H x W x cbv vectors fit in shared
-// memory twice: a CTA owns one image and cbv channel vectors, so nothing is
-// loaded or pooled twice (the tiled kernel above re-reads a 6-pixel halo
-// around every 8x8 tile).  Windows are clipped to the image instead of
-// padded with -inf: a 5-wide max over the clipped window of 5-wide maxima
-// over clipped windows is the 9-wide max over the clipped window, exactly as
-// with padding, so the cascade is unchanged.
+// Whole-image variant, for images whose (H + 4) x (W + 4) x cbv vectors fit
+// in shared memory twice: a CTA owns one image and cbv channel vectors, so
+// nothing is loaded or pooled twice (the tiled kernel above re-reads a
+// 6-pixel halo around every 8x8 tile).  Both buffers carry a 2-pixel border
+// of minus infinity that no pass writes, so every 5-wide max reads its five
+// neighbours at fixed offsets: a window clipped at the image's edge is the
+// padded window, and a 5-wide max of 5-wide maxima over padded windows is the
+// 9-wide max over the padded window, so the cascade is unchanged.
 template <typename T>
-__global__ void __launch_bounds__(kThreads) spp_image_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ y,
-                                                             const SppArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) spp_image_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ y,
+                                                                const SppArgs a) {
     pdl_trigger();  // see conv_launch
     pdl_wait();
     extern __shared__ __align__(16) uint4 sm[];
     const int n = blockIdx.x;
     const int cv0 = blockIdx.y * a.cbv;
     const int np = a.H * a.W;
-    const int nel = np * a.cbv;
+    const int nel = np * a.cbv;                          // interior elements
+    const int pitch = (a.W + 4) * a.cbv;                 // vectors per padded row
+    const int npad = (a.H + 4) * pitch;                  // vectors per padded buffer
     uint4 *A = sm;
-    uint4 *B = sm + nel;
+    uint4 *B = sm + npad;
     const uint4 neg = make_uint4(VMax<T>::kNeg, VMax<T>::kNeg, VMax<T>::kNeg, VMax<T>::kNeg);
     const long long xbase = (long long)n * np;
-    // This thread's elements e = threadIdx.x + k * kThreads (k < kImgPer; the
-    // host keeps nel <= kImgPer * kThreads): pixel (h, w) and channel vector
-    // cv, found once.  A window clipped at the border equals the window whose
-    // indices are clamped into the image (max is idempotent), so each pass
-    // reads the five clamped neighbours with no branch.
-    int eh[kImgPer], ew[kImgPer], ec[kImgPer];
+    // This thread's interior elements e = threadIdx.x + k * kThreads (k <
+    // kImgPer; the host keeps nel <= kImgPer * kThreads): their buffer index
+    // and their pixel, found once.
+    int eb[kImgPer], ep[kImgPer];
 #pragma unroll
     for (int k = 0; k < kImgPer; ++k) {
         const int e = threadIdx.x + k * kThreads;
-        const int p = e / a.cbv;
-        ec[k] = e - p * a.cbv;
-        eh[k] = p / a.W;
-        ew[k] = p - eh[k] * a.W;
+        const int p = e / a.cbv, cv = e - p * a.cbv;
+        const int h = p / a.W, w = p - h * a.W;
+        ep[k] = p;
+        eb[k] = (h + 2) * pitch + (w + 2) * a.cbv + cv;
+    }
+    // the borders of both buffers: minus infinity
+    for (int i = threadIdx.x; i < npad; i += kThreads) {
+        const int r = i / pitch, c = i - r * pitch;
+        if (r < 2 || r >= a.H + 2 || c < 2 * a.cbv || c >= (a.W + 2) * a.cbv) {
+            A[i] = neg;
+            B[i] = neg;
+        }
     }
     // x -> A (and to its own slice of y, if asked)
 #pragma unroll
     for (int k = 0; k < kImgPer; ++k) {
         const int e = threadIdx.x + k * kThreads;
         if (e >= nel) break;
-        const long long pix = xbase + eh[k] * a.W + ew[k];
+        const int cv = e - ep[k] * a.cbv;
+        const long long pix = xbase + ep[k];
         uint4 v = neg;
-        if (cv0 + ec[k] < a.CV) {
-            v = __ldg(x + pix * a.CV + cv0 + ec[k]);
-            if (a.off[3] >= 0) y[pix * a.Cy + a.off[3] + cv0 + ec[k]] = v;
+        if (cv0 + cv < a.CV) {
+            v = __ldg(x + pix * a.CV + cv0 + cv);
+            if (a.off[3] >= 0) y[pix * a.Cy + a.off[3] + cv0 + cv] = v;
         }
-        A[e] = v;
+        A[eb[k]] = v;
     }
     __syncthreads();
-    const int rowstep = a.W * a.cbv;
     for (int level = 0; level < 3; ++level) {  // 5x5, 9x9, 13x13
-        // along rows (A -> B), then along columns (B -> A): clipped 5-wide maxima
+        // along rows (A -> B), then along columns (B -> A)
 #pragma unroll
         for (int k = 0; k < kImgPer; ++k) {
             const int e = threadIdx.x + k * kThreads;
             if (e >= nel) break;
-            const int w = ew[k], b = e - w * a.cbv;  // b: the element at w = 0 of this row
-            uint4 m = A[e];
-#pragma unroll
-            for (int d = -2; d <= 2; ++d) {
-                if (d == 0) continue;
-                const int q = min(max(w + d, 0), a.W - 1);
-                m = VMax<T>::max(m, A[b + q * a.cbv]);
-            }
-            B[e] = m;
+            const uint4 *s = A + eb[k];
+            uint4 m = VMax<T>::max(VMax<T>::max(s[-2 * a.cbv], s[-a.cbv]), VMax<T>::max(s[a.cbv], s[2 * a.cbv]));
+            B[eb[k]] = VMax<T>::max(m, s[0]);
         }
         __syncthreads();
 #pragma unroll
         for (int k = 0; k < kImgPer; ++k) {
             const int e = threadIdx.x + k * kThreads;
             if (e >= nel) break;
-            const int h = eh[k], b = e - h * rowstep;  // b: the element at h = 0 of this column
-            uint4 m = B[e];
-#pragma unroll
-            for (int d = -2; d <= 2; ++d) {
-                if (d == 0) continue;
-                const int q = min(max(h + d, 0), a.H - 1);
-                m = VMax<T>::max(m, B[b + q * rowstep]);
-            }
-            A[e] = m;
+            const uint4 *s = B + eb[k];
+            uint4 m = VMax<T>::max(VMax<T>::max(s[-2 * pitch], s[-pitch]), VMax<T>::max(s[pitch], s[2 * pitch]));
+            A[eb[k]] = VMax<T>::max(m, s[0]);
         }
         __syncthreads();
         if (a.off[level] >= 0) {
@@ -237,8 +234,8 @@ __global__ void __launch_bounds__(kThreads) spp_image_kernel(const uint4 *__rest
             for (int k = 0; k < kImgPer; ++k) {
                 const int e = threadIdx.x + k * kThreads;
                 if (e >= nel) break;
-                if (cv0 + ec[k] < a.CV)
-                    y[(xbase + eh[k] * a.W + ew[k]) * a.Cy + a.off[level] + cv0 + ec[k]] = A[e];
+                const int cv = e - ep[k] * a.cbv;
+                if (cv0 + cv < a.CV) y[(xbase + ep[k]) * a.Cy + a.off[level] + cv0 + cv] = A[eb[k]];
             }
         }
         // (the next level's row pass overwrites B only: A stays readable here)
@@ -281,10 +278,11 @@ extern "C" int conv_spp_run(int32_t n, int32_t h, int32_t w, int32_t c, conv_dty
     if (cudaGetDevice(&dev) != cudaSuccess) return CONV_ERR_CUDA;
     int num_sms = 0;
     if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return CONV_ERR_CUDA;
-    // Whole images when two copies of an image's channel block fit in 96 KB:
-    // the fewest channel vectors per CTA that still give every SM two CTAs.
+    // Whole images when two padded copies of an image's channel block fit in
+    // 96 KB: the fewest channel vectors per CTA that still give every SM two
+    // CTAs.
     {
-        const long long px = (long long)h * w;
+        const long long px = (long long)(h + 4) * (w + 4);
         int cbv = 0;
         for (int v = 1; v <= a.CV && v <= 16; v *= 2) {
             if (a.CV % v != 0 || 2 * px * v * 16 > 96 * 1024) break;

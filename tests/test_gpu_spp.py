@@ -13,6 +13,8 @@ pytestmark = pytest.mark.gpu
 CASES = [
     # (name, n, h, w, c, dtype, y_channels, off5, off9, off13, off_x)
     ("yolov4_m640_20x20x512", 1, 20, 20, 512, "bf16", 2048, 0, 512, 1024, 1536),
+    ("yolov4_m640_b8", 8, 20, 20, 512, "bf16", 2048, 0, 512, 1024, 1536),
+    ("whole_image_51x51_c8", 1, 51, 51, 8, "bf16", 32, 8, 16, 24, 0),  # ~10 elements a thread
     ("yolov4_320_10x10x512_darknet_order", 1, 10, 10, 512, "bf16", 2048, 1024, 512, 0, 1536),
     ("ragged_f32_b2", 2, 7, 11, 24, "f32", 112, 8, 36, 64, 88),
     ("i8_13x9x48_no_copy", 1, 13, 9, 48, "i8", 192, 16, 80, 144, -1),
