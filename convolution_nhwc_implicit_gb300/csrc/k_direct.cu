@@ -178,21 +178,35 @@ __global__ void __launch_bounds__(kDThreads)
 direct_conv_smem(DirectArgs a, int chunks_per_group, const T *__restrict__ x, const T *__restrict__ w,
                  const float *__restrict__ bias, T *__restrict__ y) {
     pdl_trigger();  // see conv_launch
-    pdl_wait();
     extern __shared__ __align__(16) float wsm[];  // [K][CT]
     const int K = a.KH * a.KW * a.cin_g;
     const int g = blockIdx.y / chunks_per_group;
     const int cc = blockIdx.y - g * chunks_per_group;
     const int co0 = g * a.cout_g + cc * CT;
     const int nco = min(CT, a.cout_g - cc * CT);
+    // Before waiting for the previous kernel: this chunk's weight rows (nco
+    // rows of K contiguous elements) into L2, 128 bytes a thread-step.  L2 is
+    // where global writes land, so this cannot serve stale bytes to the loads
+    // after the wait.
+    {
+        const char *wb = reinterpret_cast<const char *>(w + (long long)co0 * K);
+        const long long nbytes = (long long)nco * K * sizeof(T);
+        for (long long o = (long long)threadIdx.x * 128; o < nbytes; o += 128LL * kDThreads)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(wb + o));
+    }
+    pdl_wait();
     // Stage this chunk's weights as [K][CT]: consecutive threads write
     // consecutive channels of one k (no bank conflicts); the strided global
-    // reads hit the same few lines of w for all threads of a warp.
-    for (int i = threadIdx.x; i < K * CT; i += kDThreads) {
-        const int k = i / CT, j = i - k * CT;
-        wsm[i] = j < nco ? Elem<T>::to_f(__ldg(w + (long long)(co0 + j) * K + k)) : 0.0f;
-    }
-    __syncthreads();
+    // reads hit the same few lines of w for all threads of a warp.  Done once
+    // the first batch of input loads (below) is in flight, so that the two
+    // latencies overlap.
+    auto stage_weights = [&]() {
+        for (int i = threadIdx.x; i < K * CT; i += kDThreads) {
+            const int k = i / CT, j = i - k * CT;
+            wsm[i] = j < nco ? Elem<T>::to_f(__ldg(w + (long long)(co0 + j) * K + k)) : 0.0f;
+        }
+        __syncthreads();
+    };
 
     const int g0 = g * a.cin_g;
     // fp32 rows that start on 16-byte boundaries: vector loads of the channels
@@ -218,60 +232,87 @@ direct_conv_smem(DirectArgs a, int chunks_per_group, const T *__restrict__ x, co
 #pragma unroll
         for (int j = 0; j < CT; ++j) acc[i][j] = 0.0f;
 
-    for (int r = 0; r < a.KH; ++r) {
-        for (int s = 0; s < a.KW; ++s) {
-            const T *xp[PT];
-            bool ok[PT];
+    auto fma_k = [&](const float (&xv)[PT], const float *wr) {
+#pragma unroll
+        for (int j = 0; j < CT; j += 4) {
+            const float4 w4 = *reinterpret_cast<const float4 *>(wr + j);
 #pragma unroll
             for (int i = 0; i < PT; ++i) {
-                const int ih = ihb[i] + r, iw = iwb[i] + s;
-                ok[i] = pv[i] && ih >= 0 && ih < a.H && iw >= 0 && iw < a.W;  // zero padding
-                xp[i] = x + (((long long)nn[i] * a.H + (ok[i] ? ih : 0)) * a.W + (ok[i] ? iw : 0)) * a.Cin + g0;
+                acc[i][j] = __fmaf_rn(xv[i], w4.x, acc[i][j]);
+                acc[i][j + 1] = __fmaf_rn(xv[i], w4.y, acc[i][j + 1]);
+                acc[i][j + 2] = __fmaf_rn(xv[i], w4.z, acc[i][j + 2]);
+                acc[i][j + 3] = __fmaf_rn(xv[i], w4.w, acc[i][j + 3]);
             }
-            const float *wrow = wsm + (r * a.KW + s) * a.cin_g * CT;
-            auto fma_ci = [&](const float (&xv)[PT], const float *wr) {
+        }
+    };
+    // The reduction index k = (r, s, ci) walks K in order (the staged
+    // weights' row order) in batches whose input loads are all issued before
+    // the batch's FMAs: the loads' latency is paid once per batch, not once
+    // per tap.  fp32 rows that start on 16-byte boundaries load 4 channels
+    // at a time (NB chunks a batch), others one value at a time (8 a batch).
+    // (r, s, ci) advance incrementally: no division per value.
+    int r = 0, s = 0, ci = 0;
+    auto advance = [&](int step) {
+        ci += step;
+        if (ci == a.cin_g) {
+            ci = 0;
+            if (++s == a.KW) { s = 0; ++r; }
+        }
+    };
+    auto src = [&](int i, bool &ok) {
+        const int ih = ihb[i] + r, iw = iwb[i] + s;
+        ok = pv[i] && ih >= 0 && ih < a.H && iw >= 0 && iw < a.W;  // zero padding
+        return x + (((long long)nn[i] * a.H + (ok ? ih : 0)) * a.W + (ok ? iw : 0)) * a.Cin + g0 + ci;
+    };
+    if (vec4) {
+        constexpr int NB = PT == 1 ? 8 : 4;  // 4-channel chunks in flight per pixel
+        for (int k0 = 0; k0 < K; k0 += 4 * NB) {
+            float4 q[NB][PT];
 #pragma unroll
-                for (int j = 0; j < CT; j += 4) {
-                    const float4 w4 = *reinterpret_cast<const float4 *>(wr + j);
+            for (int b = 0; b < NB; ++b) {
+                const bool live = k0 + 4 * b < K;
 #pragma unroll
-                    for (int i = 0; i < PT; ++i) {
-                        acc[i][j] = __fmaf_rn(xv[i], w4.x, acc[i][j]);
-                        acc[i][j + 1] = __fmaf_rn(xv[i], w4.y, acc[i][j + 1]);
-                        acc[i][j + 2] = __fmaf_rn(xv[i], w4.z, acc[i][j + 2]);
-                        acc[i][j + 3] = __fmaf_rn(xv[i], w4.w, acc[i][j + 3]);
-                    }
+                for (int i = 0; i < PT; ++i) {
+                    bool ok = false;
+                    const T *xp = live ? src(i, ok) : x;
+                    q[b][i] = live && ok ? __ldg(reinterpret_cast<const float4 *>(xp)) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-            };
-            int ci = 0;
-            if (vec4) {
-                // fp32 channels in 16-byte chunks, two chunks in flight per pixel:
-                // the input loads no longer serialise on their latency
-                for (; ci + 8 <= a.cin_g; ci += 8) {
-                    float4 q0[PT], q1[PT];
+                if (live) advance(4);
+            }
+            if (k0 == 0) stage_weights();  // (every thread: K is the same for all)
 #pragma unroll
-                    for (int i = 0; i < PT; ++i) {
-                        const float4 *p4 = reinterpret_cast<const float4 *>(xp[i] + ci);
-                        q0[i] = ok[i] ? __ldg(p4) : make_float4(0.f, 0.f, 0.f, 0.f);
-                        q1[i] = ok[i] ? __ldg(p4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
+            for (int b = 0; b < NB; ++b) {
+                if (k0 + 4 * b >= K) break;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        float xv[PT];
+                for (int e = 0; e < 4; ++e) {
+                    float xv[PT];
 #pragma unroll
-                        for (int i = 0; i < PT; ++i) {
-                            const float4 &q = e < 4 ? q0[i] : q1[i];
-                            const int k = e & 3;
-                            xv[i] = k == 0 ? q.x : (k == 1 ? q.y : (k == 2 ? q.z : q.w));
-                        }
-                        fma_ci(xv, wrow + (ci + e) * CT);
-                    }
+                    for (int i = 0; i < PT; ++i)
+                        xv[i] = e == 0 ? q[b][i].x : (e == 1 ? q[b][i].y : (e == 2 ? q[b][i].z : q[b][i].w));
+                    fma_k(xv, wsm + (k0 + 4 * b + e) * CT);
                 }
             }
-            for (; ci < a.cin_g; ++ci) {
-                float xv[PT];
+        }
+    } else {
+        constexpr int NB = 8;  // values in flight per pixel
+        for (int k0 = 0; k0 < K; k0 += NB) {
+            float v[NB][PT];
 #pragma unroll
-                for (int i = 0; i < PT; ++i) xv[i] = ok[i] ? Elem<T>::to_f(__ldg(xp[i] + ci)) : 0.0f;
-                fma_ci(xv, wrow + ci * CT);
+            for (int b = 0; b < NB; ++b) {
+                const bool live = k0 + b < K;
+#pragma unroll
+                for (int i = 0; i < PT; ++i) {
+                    bool ok = false;
+                    const T *xp = live ? src(i, ok) : x;
+                    v[b][i] = live && ok ? Elem<T>::to_f(__ldg(xp)) : 0.0f;
+                }
+                if (live) advance(1);
+            }
+            if (k0 == 0) stage_weights();  // (every thread: K is the same for all)
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                if (k0 + b >= K) break;
+                fma_k(v[b], wsm + (k0 + b) * CT);
             }
         }
     }
