@@ -295,7 +295,7 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
                     }
                     const int one_buf = swap ? 4 * 16 * kTP : epi_groups(bn, false, c.ept != 0) * kBM * 64;
                     // swapped plain bf16 layers whose 16-pixel chunks lie in one row
-                    // write out by TMA stores from two staging buffers per group
+                    // write out by TMA stores from two staging buffers per warp
                     const bool swap_tma = swap && !igemm_fused(p) && p->dtype == CONV_BF16 && (g.flat || c.bw % 16 == 0);
                     c.out_bufs = swap_tma ? 2 : 1;
                     if (!swap && wblocks < 16 && (smem_cap - 2 * one_buf) / ((long long)c.a_stage + wblock) >= 4)
@@ -554,21 +554,22 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
             const int dy = rp / up, dx = rp % up;
             char *base = static_cast<char *>(y) + ((cuuint64_t)p->y_coff + ((cuuint64_t)dy * OWy + dx) * Cy) * es;
             if (g.swap && g.out_bufs == 2) {
-                // swapped TMA write-out: [16 pixels][64 channels] boxes, 128-byte swizzle
+                // swapped TMA write-out: [16 pixels][32 channels] boxes, one per
+                // warp, 64-byte swizzle
                 if (g.flat) {
                     const cuuint64_t dims[2] = {(cuuint64_t)p->s.c_out, (cuuint64_t)p->s.n * p->oh * p->ow};
                     const cuuint64_t strides[1] = {Cy * es};
-                    const cuuint32_t box[2] = {64, 16};
+                    const cuuint32_t box[2] = {32, 16};
                     rc = encode(&tmY.m[rp], dt, 2, base, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
                 } else {
                     const cuuint64_t dims[4] = {(cuuint64_t)p->s.c_out, (cuuint64_t)p->ow, (cuuint64_t)p->oh,
                                                 (cuuint64_t)p->s.n};
                     const cuuint64_t strides[3] = {Cy * es, OWy * Cy * es, OHy * OWy * Cy * es};
-                    const cuuint32_t box[4] = {64, 16, 1, 1};
+                    const cuuint32_t box[4] = {32, 16, 1, 1};
                     rc = encode(&tmY.m[rp], dt, 4, base, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
                 }
             } else if (g.flat) {  // (up == 1)

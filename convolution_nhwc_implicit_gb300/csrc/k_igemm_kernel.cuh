@@ -379,18 +379,20 @@ __device__ __forceinline__ void epilogue_swapped_bf16(const IgArgs &a, int tile,
 
 // Swapped-mode bf16 epilogue whose write-out is a TMA tensor store (plain
 // layers whose tile width is a multiple of 16, or flat tiles: a 16-pixel
-// chunk is then one row segment of y).  The fragments are transposed by
-// stmatrix as in epilogue_swapped_bf16, but into two 128-byte-swizzled
-// [16 pixels][64 channels] boxes, the layout of the store's tensor map
-// (chunk j of row r at chunk j ^ (r mod 8): the eight rows of a fragment on
-// distinct banks), double-buffered per warpgroup; the group's first thread
-// then issues the stores and the group goes on to the next chunk while the
-// TMA engine reads the buffer.  The threads' own shared-memory loads, global
-// stores and address arithmetic of the write-out disappear.
+// chunk is then one row segment of y).  Each warp owns 32 of the 128
+// accumulator rows (channels 32q .. 32q + 31) and writes them out on its own:
+// its fragments are transposed by stmatrix as in epilogue_swapped_bf16, but
+// into a 64-byte-swizzled [16 pixels][32 channels] box, the layout of the
+// store's tensor map (chunk j of row r at chunk j ^ ((r / 2) mod 4): the rows
+// of an 8 x 8 fragment on distinct banks), double-buffered per warp; the
+// warp's lane 0 then issues the store and the warp goes on to the next chunk
+// while the TMA engine reads the buffer.  No barrier couples the warps of a
+// group, and the threads' own shared-memory loads, global stores and address
+// arithmetic of the write-out disappear.
 template <int kCols>
 __device__ __forceinline__ void epilogue_swapped_tma(const IgArgs &a, const CUtensorMap *tmY, int mt, uint32_t taddr,
-                                                     uint32_t tempty, int grp, int c_base, uint32_t sbuf0, int q,
-                                                     int lane, bool issuer, int &oc, const float (&fb)[2][2]) {
+                                                     uint32_t tempty, int c_base, uint32_t wbuf, int q, int lane,
+                                                     int &oc, const float (&fb)[2][2]) {
     uint32_t acc[2][kCols / 8][4];  // [lane half][8-column group][fragment registers]
 #pragma unroll
     for (int h = 0; h < 2; ++h)
@@ -417,21 +419,20 @@ __device__ __forceinline__ void epilogue_swapped_tma(const IgArgs &a, const CUte
     int dw = a.flat ? 0 : c_base - dh * a.bw;
     // stmatrix row address of this thread in a buffer: matrix m = lane / 8
     // (pixels 8 (m / 2) + 0..7, channels 32q + 16h + 8 (m % 2) + 0..7), row
-    // lane % 8: pixel r, 16-byte chunk 4q + 2h + m % 2 of its 256-byte row,
-    // i.e. box q / 2, swizzled chunk (4 (q % 2) + 2h + m % 2) ^ (r % 8)
+    // lane % 8: pixel r, 16-byte chunk 2h + m % 2 of its 64-byte row,
+    // swizzled: chunk (2h + m % 2) ^ ((r / 2) mod 4)
     const int r = 8 * (lane >> 4) + (lane & 7);
-    const uint32_t roff = (uint32_t)((q >> 1) * 2048 + r * 128);
     uint32_t coff[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h)
-        coff[h] = roff + ((uint32_t)((4 * (q & 1) + 2 * h + ((lane >> 3) & 1)) ^ (r & 7)) << 4);
-    const bool two_boxes = a.Cout > 64;
+        coff[h] = (uint32_t)(r * 64) + ((uint32_t)((2 * h + ((lane >> 3) & 1)) ^ ((r >> 1) & 3)) << 4);
+    const bool mine = 32 * q < a.Cout;  // (rows past Cout are never stored)
 #pragma unroll
     for (int c = 0; c < kCols; c += 16) {
-        const uint32_t sb = sbuf0 + (uint32_t)(oc & 1) * 4096u;
+        const uint32_t sb = wbuf + (uint32_t)(oc & 1) * 1024u;
         // the store that last read this buffer (two chunks ago) has read it
-        if (issuer) tc::bulk_wait_read1();
-        tc::named_bar_sync(1 + grp, 128);
+        if (lane == 0) tc::bulk_wait_read1();
+        __syncwarp();
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             uint32_t fr[4];
@@ -450,15 +451,13 @@ __device__ __forceinline__ void epilogue_swapped_tma(const IgArgs &a, const CUte
             tc::stmatrix_x4_trans(sb + coff[h], fr[0], fr[1], fr[2], fr[3]);
         }
         tc::fence_proxy_async_smem();  // the staged values visible to the TMA engine
-        tc::named_bar_sync(1 + grp, 128);
-        if (issuer) {
-            if (a.flat) {
-                const int row0 = (int)(m0 + c_base + c);
-                tc::tma_store_2d(tmY, sb, 0, row0);
-                if (two_boxes) tc::tma_store_2d(tmY, sb + 2048u, 64, row0);
-            } else if (dh < a.bh) {  // (rows past the tile belong to the next tile)
-                tc::tma_store_4d(tmY, sb, 0, ow0 + dw, oh0 + dh, n);
-                if (two_boxes) tc::tma_store_4d(tmY, sb + 2048u, 64, ow0 + dw, oh0 + dh, n);
+        __syncwarp();
+        if (lane == 0) {
+            if (mine) {
+                if (a.flat)
+                    tc::tma_store_2d(tmY, sb, 32 * q, (int)(m0 + c_base + c));
+                else if (dh < a.bh)  // (rows past the tile belong to the next tile)
+                    tc::tma_store_4d(tmY, sb, 32 * q, ow0 + dw, oh0 + dh, n);
             }
             tc::bulk_commit();
         }
@@ -1188,8 +1187,9 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 uint8_t *tb = gbase + (sOut - base) + grp * a.out_bufs * kOutStage;
                 if constexpr (!FUSED) {
                     if (a.out_bufs == 2) {  // plain bf16, 16-pixel chunks in one row: TMA-store write-out
-                        epilogue_swapped_tma<kCols>(a, &tmY.m[0], tile, ta, tempty_bar(buf), grp, c_base,
-                                                    sOut + (uint32_t)(grp * 2) * 4096u, q, lane, issuer, oc, swb);
+                        epilogue_swapped_tma<kCols>(a, &tmY.m[0], tile, ta, tempty_bar(buf), c_base,
+                                                    sOut + (uint32_t)(grp * 2) * 4096u + (uint32_t)q * 2048u, q,
+                                                    lane, oc, swb);
                         continue;
                     }
                 }
@@ -1385,8 +1385,9 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             }
         }
         // The staging buffers must outlive the stores' reads of them; the
-        // global writes themselves complete before the grid does.
-        if (issuer) tc::bulk_wait_read0();
+        // global writes themselves complete before the grid does.  (The
+        // swapped TMA write-out stores from every warp's lane 0.)
+        if (issuer || (SWAP && a.out_bufs == 2 && lane == 0)) tc::bulk_wait_read0();
     }
 
     // Warps 0 and 1 ran their loops on lane 0 only: reconverge each warp
