@@ -9,17 +9,17 @@
 // of one image.  Its input halo, ((th-1)S+3) x ((tw-1)S+3) pixels x cb
 // channels, arrives in shared memory as ONE TMA box: coordinates outside the
 // image read as zeros, which is the zero padding, and the whole halo is in
-// flight at once.  A thread owns one 16-byte channel vector (4 fp32, 8 bf16
-// or 16 int8 channels) at one output column and walks down the th rows,
-// keeping the three halo rows under its window in registers (one new row of
-// three 16-byte shared-memory loads per output row at stride 1).  Consecutive
-// threads take consecutive channel vectors, so shared-memory reads and the
-// global stores are contiguous.  The thread's 9 x 16 bytes of weights are
-// nine 16-byte loads (OHWI [C][3][3] keeps a channel's taps together) and
-// stay in registers, packed: bf16 products use fma.rn.f32.bf16 (bf16
-// operands, fp32 accumulation) so nothing is unpacked.  The bias seeds the
-// accumulator; activation and the int8 requantisation run before the single
-// 16-byte store.
+// flight at once.  A thread owns one channel vector (4 fp32, 4 bf16 or 16
+// int8 channels) at one output column and walks down the th rows, keeping
+// the three halo rows under its window in registers (one new row of three
+// shared-memory loads per output row at stride 1).  Consecutive threads take
+// consecutive channel vectors, so shared-memory reads and the global stores
+// are contiguous.  The thread's weights (OHWI [C][3][3] keeps a channel's
+// taps together) stay in registers; bf16 values are widened to fp32 (exact)
+// and products are paired fp32 FMAs, int8 products exact int32.  The bias
+// seeds the accumulator; activation and the int8 requantisation run before
+// the single vector store.  bf16 stride-1 layers run the rolling-row kernel
+// below instead.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
