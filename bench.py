@@ -511,7 +511,7 @@ def run_ours(args, rank, world, device):
     # ---- int8 context: the tensor cores' int8 rate as torch exposes it (these
     # layers themselves run as exact bf16 MMAs, so their roof is the bf16 peak)
     int8_probe = None
-    if any(d.spec.dtype == "i8" for d in layers):
+    if any(d.spec.dtype == "i8" for d in layers) or "vww_int8" in (layer_sets or {}):
         try:
             a8 = torch.randint(-128, 128, (8192, 8192), dtype=torch.int8, device=dev)
             b8 = torch.randint(-128, 128, (8192, 8192), dtype=torch.int8, device=dev).t()
