@@ -770,22 +770,31 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     }
                 }
             }
+            // (single CTAs: the tiles' coordinates advanced without division,
+            // which would sit in this thread's per-tile latency chain)
+            TileWalk pwalk;
+            if (!PAIR) pwalk.init(a, unit, units);
             for (int tile = unit; tile < a.num_tiles && ok; tile += units) {
-                const int nb = tile % a.tiles_n;
+                const int nb = PAIR ? tile % a.tiles_n : pwalk.nb;
                 // pair mode: this CTA's pixel tile (past tiles_m: an empty
                 // half, loaded as zeros from outside the tensor, never stored)
-                const int mt = PAIR ? (tile / a.tiles_n) * 2 + (int)rank : tile / a.tiles_n;
+                const int mt = PAIR ? (tile / a.tiles_n) * 2 + (int)rank : pwalk.mt;
                 int n = 0, oh0 = 0, ow0 = 0;
                 int m0 = 0;
                 if (FLAT) {
                     m0 = mt * kPix;
-                } else {
+                } else if (PAIR) {
                     const int tw = mt % a.tiles_w;
                     const int t2 = mt / a.tiles_w;
                     oh0 = (t2 % a.tiles_h) * a.bh;
                     n = t2 / a.tiles_h;
                     ow0 = tw * a.bw;
+                } else {
+                    oh0 = pwalk.th * a.bh;
+                    n = pwalk.n;
+                    ow0 = pwalk.tw * a.bw;
                 }
+                if (!PAIR) pwalk.advance(a);
                 if constexpr (CVT) {
                     // raw int8 activation boxes into the raw ring (per-tap or halo
                     // boxes, in the K block order of the plain variants)
