@@ -268,6 +268,26 @@ def test_depthwise(spec):
     check(spec, "depthwise", "depthwise")
 
 
+# The general depthwise kernel walks 8 output rows a tile on layers with a
+# tile per SM or more, and fewer (4, 2, 1) on smaller ones: both regimes, in
+# each type (bf16 here at stride 2: stride 1 runs the rolling-row kernel).
+DW_TH = [
+    (L("dw_i8_160_th8", 1, 160, 160, 64, 64, 3, 3, 1, 1, 1, groups=64, dtype="i8", act="relu"), 8),
+    (L("dw_f32_96_th8", 2, 96, 96, 32, 32, 3, 3, 1, 1, 1, groups=32, dtype="f32", act="relu"), 8),
+    (L("dw_bf16_s2_192_th8", 1, 192, 192, 64, 64, 3, 3, 2, 1, 1, groups=64, act="mish"), 8),
+    (L("dw_i8_24_small", 1, 24, 24, 32, 32, 3, 3, 1, 1, 1, groups=32, dtype="i8"), 1),
+]
+
+
+@pytest.mark.parametrize("spec,th", DW_TH, ids=[s.name for s, _ in DW_TH])
+def test_depthwise_tile_rows(spec, th):
+    plan = check(spec, "depthwise", "depthwise")
+    if th == 8:
+        assert "tile=8x" in plan.describe(), plan.describe()
+    else:
+        assert "tile=8x" not in plan.describe(), plan.describe()
+
+
 # bf16 stride 1 runs on the rolling-row kernel: ragged row and column tiles,
 # each padding and activation, channel counts from one 8-channel block up.
 DW_ROWS = [
