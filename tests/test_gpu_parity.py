@@ -328,6 +328,21 @@ def test_direct(spec):
     check(spec, "direct", "direct")
 
 
+# Layers with enough pixels that each thread takes two (PT = 2): 16-byte
+# channel chunks in flight per batch (a partial last batch: K = 72 is 18
+# chunks) and, grouped with 4 channels a group, single values (K = 36).
+DIRECT_PT2 = [
+    L("direct_pt2_f32_3x3", 1, 640, 640, 8, 16, 3, 3, 1, 1, 1, dtype="f32", act="relu"),
+    L("direct_pt2_f32_grouped", 1, 640, 640, 8, 16, 3, 3, 1, 1, 1, groups=2, dtype="f32", act="mish"),
+]
+
+
+@pytest.mark.parametrize("spec", DIRECT_PT2, ids=lambda s: s.name)
+def test_direct_two_pixels_a_thread(spec):
+    plan = check(spec, "direct", "direct")
+    assert "px/thread=2" in plan.describe(), plan.describe()
+
+
 def test_pointwise_paths_agree():
     """A 1x1 layer through the tcgen05 GEMM and through the direct kernel."""
     spec = L("pw_both", 1, 20, 20, 128, 64, 1, 1)
