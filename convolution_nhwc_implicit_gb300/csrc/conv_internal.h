@@ -34,6 +34,7 @@ struct IgemmGeom {
     int ept;       // 1: one epilogue per tile (each warpgroup drains whole tiles, four TMEM accumulators)
     int bias_smem; // 1: the bias (and int8 multipliers) copied into shared memory once per CTA
     int cvt;       // 1: int8 operands widened to bf16 in the kernel (converter warpgroup), no pre-pass
+    int mb;        // M blocks of 128 pixels a tile (2: the in-kernel stem fold, two blocks stacked)
     int raw_stage; // cvt: bytes of a raw int8 activation stage
     int raw_region;  // cvt: bytes of the raw region (raw weights, then the raw ring)
     int stages;    // shared-memory pipeline depth
@@ -140,7 +141,7 @@ void *igemm_select_fused(int bn, int bk, bool flat, bool swap, bool pair, bool h
 void *igemm_select_ept(int bn, int bk, bool flat, bool halo);
 // The variant that widens int8 operands in the kernel (normal layout,
 // resident weights, no output options), compiled in its own translation unit.
-void *igemm_select_cvt(int mode, int bn, int bk, bool flat, bool halo, bool ept);
+void *igemm_select_cvt(int mode, int bn, int bk, bool flat, bool halo, bool ept, int mb);
 // Fills p->ig and sets kernel attributes; CONV_* status.  layout 0 picks
 // the tile layout by estimated time; 1..6 force swapped, N256, N128, N64,
 // CTA pair (N = 256), CTA pair (N = 128).  staging 0 picks per-tap or halo

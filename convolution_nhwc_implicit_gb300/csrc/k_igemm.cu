@@ -50,9 +50,10 @@ void *kernel_ptr_bk(int bk, bool flat, bool halo) {
     }
 }
 
-void *select_kernel(int bn, int bk, bool flat, bool swap, bool pair, bool fused, bool halo, bool ept, int cvt) {
+void *select_kernel(int bn, int bk, bool flat, bool swap, bool pair, bool fused, bool halo, bool ept, int cvt,
+                    int mb) {
     if (fused) return igemm_select_fused(bn, bk, flat, swap, pair, halo);
-    if (cvt) return igemm_select_cvt(cvt, bn, bk, flat, halo, ept);
+    if (cvt) return igemm_select_cvt(cvt, bn, bk, flat, halo, ept, mb);
     if (ept) return igemm_select_ept(bn, bk, flat, halo);
     if (pair) return bn == 128 ? kernel_ptr_bk<128, false, true>(bk, flat, halo)
                                : kernel_ptr_bk<256, false, true>(bk, flat, halo);
@@ -183,7 +184,7 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
     if (staging == 2 && !halo_ok) return CONV_ERR_UNSUPPORTED;
     if (epi == 2 && igemm_fused(p)) return CONV_ERR_UNSUPPORTED;  // (no output options per tile)
     struct Cand {
-        int swap, pair, bn, bk, halo, ept, cvt, bw, bh, tw, th, wres, stages, out_bufs;
+        int swap, pair, bn, bk, halo, ept, cvt, bw, bh, tw, th, wres, stages, out_bufs, mb;
         long long tiles_m, tiles_n, units, rows;
         uint32_t a_stage, raw_stage, raw_region;
     };
@@ -213,7 +214,7 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
                 if ((staging == 1 && halo) || (staging == 2 && !halo)) continue;
                 // tile shapes: flat (one); per-tap spatial (the fewest tiles,
                 // then the widest); halo (bw a multiple of 8, bh x bw <= P)
-                int shapes[40][2];
+                int shapes[40][3];  // bw, bh, M blocks a tile
                 int nshapes = 0;
                 if (g.flat) {
                     shapes[nshapes][0] = P; shapes[nshapes][1] = 1; ++nshapes;
@@ -236,15 +237,28 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
                             if (cw >= p->ow) break;
                         }
                         if (bt < 0 || (pass == 1 && bw == shapes[0][0])) continue;
-                        shapes[nshapes][0] = bw; shapes[nshapes][1] = bh; ++nshapes;
+                        shapes[nshapes][0] = bw; shapes[nshapes][1] = bh; shapes[nshapes][2] = 1; ++nshapes;
                     }
                 } else {
                     for (int cw = 8; cw <= P && cw <= 256 && nshapes < 40; cw += 8) {
                         int ch = P / cw;
                         if (ch > p->oh) ch = p->oh;
                         if (ch + p->s.k_h - 1 > 256) continue;
-                        shapes[nshapes][0] = cw; shapes[nshapes][1] = ch; ++nshapes;
+                        shapes[nshapes][0] = cw; shapes[nshapes][1] = ch; shapes[nshapes][2] = 1; ++nshapes;
                         if (cw >= p->ow) break;  // wider tiles only waste more columns
+                    }
+                    // The stem fold built in the kernel (N = 64): also tiles of two
+                    // 128-pixel M blocks stacked (bh = 2 x 128 / bw), so that the
+                    // roles' fixed costs per tile are paid once per 256 pixels; the
+                    // converter reaches at most 384 box rows
+                    if (cvt_mode == 2 && !swap && !pair && bn == 64) {
+                        for (int i = 0, n1 = nshapes; i < n1 && nshapes < 40; ++i) {
+                            const int cw = shapes[i][0], ch = 2 * shapes[i][1];
+                            if (shapes[i][1] * cw != kBM || ch > p->oh || ch + p->s.k_h - 1 > 256 ||
+                                (ch + p->s.k_h - 1) * cw > 384)
+                                continue;
+                            shapes[nshapes][0] = cw; shapes[nshapes][1] = ch; shapes[nshapes][2] = 2; ++nshapes;
+                        }
                     }
                 }
                 for (int ci = 0; ci < 2 * nshapes; ++ci) {
@@ -253,7 +267,8 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
                     if (!cvt && widen == 2) continue;
                     Cand c{};
                     c.swap = swap; c.pair = pair; c.bn = bn; c.bk = bk; c.halo = halo; c.cvt = cvt;
-                    c.bw = shapes[si][0]; c.bh = shapes[si][1];
+                    c.bw = shapes[si][0]; c.bh = shapes[si][1]; c.mb = shapes[si][2];
+                    if (c.mb == 2 && !cvt) continue;  // (two M blocks: the in-kernel fold only)
                     if (g.flat) {
                         const long long M = (long long)p->s.n * p->s.h * g.wx;
                         c.tiles_m = (M + P - 1) / P;
@@ -269,13 +284,14 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
                     // (with fewer, slicing every tile's columns over the warpgroups
                     // finishes each tile sooner), or where forced.
                     c.ept = ept_ok && epi != 1 && (epi == 2 || c.units >= 2LL * p->num_sms) ? 1 : 0;
+                    if (c.mb == 2 && !c.ept) continue;  // (two M blocks: an epilogue per tile)
                     // Shared memory: ring stages, resident weights, epilogue
                     // staging.  A halo stage holds the box's (bh + k_h - 1) x bw
                     // pixel rows and, when bh x bw < P, the P - bh x bw rows the
                     // last tap's MMAs read past them (stale, never stored).
                     const int hrows = c.bh + p->s.k_h - 1;
                     const int box_rows = halo ? hrows * c.bw : P;  // pixel rows TMA writes per stage
-                    const int read_rows = halo ? (p->s.k_h - 1) * c.bw + P : P;
+                    const int read_rows = halo ? (p->s.k_h - 1) * c.bw + c.mb * P : P;
                     const int a_rows = box_rows > read_rows ? box_rows : read_rows;
                     c.a_stage = (uint32_t)(((long long)a_rows * bk * 2 + 1023) / 1024 * 1024);
                     const long long ring_kb = halo ? (long long)g.kw * cblocks : wblocks;  // stages per tile
@@ -349,11 +365,11 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
                     // stores and their address arithmetic in the epilogue threads --
                     // adds ~650 cycles per 16-pixel chunk, measured; the TMA
                     // write-out moves that to the TMA engine)
-                    const long long t_epi = 128LL * (swap ? P : bn) * epi_c / 128 + (swap && c.out_bufs == 1 ? 2600 : 0);
+                    const long long t_epi = 128LL * (swap ? P : bn) * c.mb * epi_c / 128 + (swap && c.out_bufs == 1 ? 2600 : 0);
                     // a stage: its MMAs, its TMA rows, or the ring's refill latency
                     // spread over the other stages, whichever is longest, plus a
                     // fixed cost of the stage's barrier round trip
-                    const long long m_stage = (long long)taps * (bk / 16) * 128;
+                    const long long m_stage = (long long)taps * (bk / 16) * 128 * c.mb;
                     const long long rows_stage = box_rows + (c.wres ? 0 : (long long)taps * bnc);
                     long long per_stage = 2000 / (c.stages - 1);
                     if (per_stage < m_stage) per_stage = m_stage;
@@ -389,6 +405,7 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
     const Cand &best = bests[track];
     g.swap = best.swap; g.pair = best.pair; g.bn = best.bn; g.bk = best.bk; g.halo = best.halo; g.ept = best.ept;
     g.cvt = best.cvt;
+    g.mb = best.mb;
     g.raw_stage = (int)best.raw_stage;
     g.raw_region = (int)best.raw_region;
     // plan-owned bf16 copies of x and w (channels padded to `cin`), unless the
@@ -427,7 +444,7 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
     if (g.smem < 116 * 1024) g.smem = 116 * 1024;
     if (!tensor_map_encoder()) return CONV_ERR_CUDA;
     void *kern = select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0, g.pair != 0, igemm_fused(p), g.halo != 0, g.ept != 0,
-                              g.cvt);
+                              g.cvt, g.mb);
     const int rc = conv_grant_smem(kern, p->device, g.smem);
     if (rc != CONV_OK) return rc;
     if (g.pair) {
@@ -450,7 +467,7 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
         g.grid = g.num_tiles < p->num_sms ? g.num_tiles : p->num_sms;
     }
     snprintf(p->desc, sizeof(p->desc),
-             "igemm_%s_tcgen05 %s%s %s BK=%d tile=%dx%d%s stages=%d%s out_bufs=%d%s tiles=%d grid=%d",
+             "igemm_%s_tcgen05 %s%s %s BK=%d tile=%dx%d%s%s stages=%d%s out_bufs=%d%s tiles=%d grid=%d",
              p->dtype == CONV_I8 ? (g.fold ? "i8-as-bf16-kwfold" : (g.cvt ? "i8-widened-in-kernel" : "i8-as-bf16"))
                                  : (g.fold ? (g.cvt ? "bf16-kwfold-in-kernel" : "bf16-cpad-kwfold")
                                            : (g.prep ? "bf16-cpad" : "bf16")),
@@ -459,7 +476,8 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
              g.swap ? "M=128co N=256px"
                     : (g.pair ? (g.bn == 256 ? "M=256px N=256co" : "M=256px N=128co")
                               : (g.bn == 256 ? "M=128px N=256co" : (g.bn == 128 ? "M=128px N=128co" : "M=128px N=64co"))),
-             g.bk, g.bh, g.bw, g.halo ? " halo" : "", g.stages, g.wres ? " resident-weights" : "", g.out_bufs,
+             g.bk, g.bh, g.bw, g.mb == 2 ? " (2 M blocks)" : "", g.halo ? " halo" : "", g.stages,
+             g.wres ? " resident-weights" : "", g.out_bufs,
              g.ept ? " epi=tile" : "", g.num_tiles, g.grid);
     return CONV_OK;
 }
@@ -582,7 +600,8 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
                 const cuuint64_t dims[4] = {(cuuint64_t)p->s.c_out, (cuuint64_t)p->ow, (cuuint64_t)p->oh,
                                             (cuuint64_t)p->s.n};
                 const cuuint64_t strides[3] = {up * Cy * es, up * OWy * Cy * es, OHy * OWy * Cy * es};
-                const cuuint32_t box[4] = {box_n, (cuuint32_t)g.bw, (cuuint32_t)g.bh, 1};
+                // (two M blocks a tile: one store per block, its bh / 2 rows)
+                const cuuint32_t box[4] = {box_n, (cuuint32_t)g.bw, (cuuint32_t)(g.bh / g.mb), 1};
                 rc = encode(&tmY.m[rp], dt, 4, base, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
             }
@@ -623,7 +642,7 @@ int launch_igemm(const conv_plan *p, const void *x, const void *w, const void *b
     a.status = p->d_status;
 
     void *k = select_kernel(g.bn, g.bk, g.flat != 0, g.swap != 0, g.pair != 0, igemm_fused(p), g.halo != 0, g.ept != 0,
-                              g.cvt);
+                              g.cvt, g.mb);
     void *args[] = {&tmA, &tmB, &tmY, &a};
     const cudaError_t e = conv_launch(k, dim3(g.grid), dim3(cta_threads(g.bn, g.swap != 0, g.ept != 0, g.cvt != 0)), args, (size_t)g.smem, st,
                                       g.pair ? 2 : 1);

@@ -37,7 +37,11 @@ void *fold_ptr(bool halo, bool ept) {
 
 }  // namespace
 
-void *igemm_select_cvt(int mode, int bn, int bk, bool flat, bool halo, bool ept) {
+void *igemm_select_cvt(int mode, int bn, int bk, bool flat, bool halo, bool ept, int mb) {
+    if (mode == 2 && mb == 2)  // (two M blocks a tile: N = 64, halo staging, an epilogue per tile)
+        return bn == 64 && halo && ept
+                   ? reinterpret_cast<void *>(&igemm_bf16_kernel<64, 16, false, false, false, false, true, true, 2, 2>)
+                   : nullptr;
     if (mode == 2) return bn == 128 ? fold_ptr<128>(halo, ept) : fold_ptr<64>(halo, ept);
     return bn == 128 ? widen_bk<128>(bk, flat, halo, ept) : widen_bk<64>(bk, flat, halo, ept);
 }

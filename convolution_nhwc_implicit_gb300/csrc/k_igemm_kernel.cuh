@@ -537,7 +537,7 @@ __device__ __forceinline__ void epilogue_swapped_tma(const IgArgs &a, const CUte
 // converter writes the folded resident blocks from them (each (co, r) row's
 // k_w * Cin values, zero-padded) before the raw ring reuses that memory.
 template <int BN, int BK, bool FLAT, bool SWAP, bool PAIR, bool FUSED, bool HALO = false, bool EPT = false,
-          int CVT = 0>
+          int CVT = 0, int MB = 1>
 __global__ void __launch_bounds__(cta_threads(BN, SWAP, EPT, CVT), 1)
 igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ YMaps tmY, const IgArgs a) {
@@ -546,8 +546,12 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     static_assert(!EPT || (!SWAP && !PAIR && BN <= 128), "one epilogue per tile: normal layout, BN <= 128");
     static_assert(!CVT || (!SWAP && !PAIR && !FUSED), "in-kernel widening: normal layout");
     static_assert(CVT != 2 || (BK == 16 && !FLAT), "in-kernel fold: 16-channel rows of spatial tiles");
+    static_assert(MB == 1 || (CVT == 2 && HALO && EPT && MB == 2 && 4 * MB * BN <= 512),
+                  "two M blocks a tile: the in-kernel stem fold, halo staging, an epilogue per tile");
     constexpr int kPix = SWAP ? kBMSwap : kBM;  // pixel rows of a tile (per CTA)
-    constexpr int kAcc = SWAP ? kBMSwap : BN;   // accumulator columns of a tile
+    // accumulator columns of a tile (MB = 2: the tile's two 128-pixel M blocks,
+    // its top and bottom bh / 2 rows, side by side)
+    constexpr int kAcc = SWAP ? kBMSwap : MB * BN;
     constexpr int kBRows = PAIR ? BN / 2 : BN;  // weight rows this CTA stages
     constexpr uint32_t kRowBytes = BK * 2;
     constexpr uint32_t kBStage = kBRows * BK * 2;  // one weight K block (this CTA's part)
@@ -944,8 +948,14 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                     tc::mma_bf16_pair(d, pd, wd, kIdesc, accum);
                                 else if (SWAP)
                                     tc::mma_bf16(d, wd, pd, kIdesc, accum);
-                                else
-                                    tc::mma_bf16(d, pd, wd, kIdesc, accum);
+                                else {
+                                    // (MB = 2: block j's pixel rows start 128 rows further
+                                    // into the box, its accumulator BN columns further)
+#pragma unroll
+                                    for (int j = 0; j < MB; ++j)
+                                        tc::mma_bf16(d + (uint32_t)(j * BN), pd + (uint64_t)(j * kBM * kRowBytes / 16), wd,
+                                                     kIdesc, accum);
+                                }
                             }
                         }
                         if (++cb == a.cblocks) { cb = 0; ++s; }
@@ -1219,7 +1229,7 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             constexpr bool kChunked = FUSED || EPT;
             constexpr int kAccRegs = kChunked ? 32 : kCols;
             uint32_t acc[kAccRegs];
-            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c_base);
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kAcc + c_base);
             auto release = [&]() {
                 tc::fence_before_sync();
                 if constexpr (PAIR) {
@@ -1277,7 +1287,9 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             }
 #pragma unroll
             for (int c = 0; c < kCols; c += 32) {
-                const int co = nb * BN + c_base + c;
+                // (MB = 2: columns [j BN, (j + 1) BN) are M block j, rows j bh / 2 ..)
+                const int jb = MB == 1 ? 0 : c / BN;
+                const int co = nb * BN + c_base + (MB == 1 ? c : c - jb * BN);
                 const bool live = co < a.Cout;  // the same for the whole group
                 if constexpr (kChunked) {
                     if (live) {
@@ -1380,16 +1392,17 @@ igemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
                 tc::fence_proxy_async_smem();  // staged values visible to the TMA engine
                 tc::named_bar_sync(1 + grp, 128);
-                if (issuer) {
+                // (MB = 2: a bottom block wholly below the image stores nothing)
+                if (issuer && (MB == 1 || oh0 + jb * (a.bh / MB) < a.OH)) {
                     const int reps = FUSED ? a.om.up * a.om.up : 1;
                     for (int rp = 0; rp < reps; ++rp) {  // one store per upsample replica
                         if (FLAT)
                             tc::tma_store_2d(&tmY.m[rp], sbuf, co, m0);
                         else
-                            tc::tma_store_4d(&tmY.m[rp], sbuf, co, ow0, oh0, n);
+                            tc::tma_store_4d(&tmY.m[rp], sbuf, co, ow0, oh0 + jb * (a.bh / MB), n);
                     }
-                    tc::bulk_commit();
                 }
+                if (issuer) tc::bulk_commit();
                 ++oc;
             }
         }

@@ -216,6 +216,22 @@ def test_kw_fold_in_kernel(spec, layout):
     assert plan.launches == (1 if "inkernel" in layout else 2)
 
 
+# The in-kernel fold with tiles of two stacked 128-pixel M blocks (N = 64,
+# halo staging, an epilogue per tile; chosen on layers with at least two tiles
+# per SM): ragged heights put a tile's bottom block partly or wholly below the
+# image (the latter stores nothing), and stride 1 only (halo staging).
+FOLD_MB2 = [
+    L("fold_mb2_bottom_block_outside", 1, 584, 256, 3, 32, 3, 3, 1, 1, 1),
+    L("fold_mb2_b2_half_tile_row", 2, 304, 304, 3, 32, 3, 3, 1, 1, 1, act="relu"),
+]
+
+
+@pytest.mark.parametrize("spec", FOLD_MB2, ids=lambda s: s.name)
+def test_kw_fold_two_m_blocks(spec):
+    plan = check(spec, "auto", "igemm")
+    assert "kwfold-in-kernel" in plan.describe() and "(2 M blocks)" in plan.describe(), plan.describe()
+
+
 def test_kw_fold_in_kernel_needs_whole_rows():
     # 45 pixels x 3 channels x 2 bytes = 270: not a whole number of 16-byte units
     spec = L("fold_row_270_bytes", 1, 18, 45, 3, 32, 3, 3, 1, 1, 1)
