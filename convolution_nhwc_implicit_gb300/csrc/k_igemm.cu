@@ -214,10 +214,10 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
                 if ((staging == 1 && halo) || (staging == 2 && !halo)) continue;
                 // tile shapes: flat (one); per-tap spatial (the fewest tiles,
                 // then the widest); halo (bw a multiple of 8, bh x bw <= P)
-                int shapes[40][3];  // bw, bh, M blocks a tile
+                int shapes[40][3] = {};  // bw, bh, M blocks a tile
                 int nshapes = 0;
                 if (g.flat) {
-                    shapes[nshapes][0] = P; shapes[nshapes][1] = 1; ++nshapes;
+                    shapes[nshapes][0] = P; shapes[nshapes][1] = 1; shapes[nshapes][2] = 1; ++nshapes;
                 } else if (!halo) {
                     // (the fewest tiles, then the widest; and, for the fold built in
                     // the kernel, the same among the widths whose raw box rows fit
@@ -267,7 +267,7 @@ int igemm_configure(conv_plan *p, int layout, int staging, int epi, int widen) {
                     if (!cvt && widen == 2) continue;
                     Cand c{};
                     c.swap = swap; c.pair = pair; c.bn = bn; c.bk = bk; c.halo = halo; c.cvt = cvt;
-                    c.bw = shapes[si][0]; c.bh = shapes[si][1]; c.mb = shapes[si][2];
+                    c.bw = shapes[si][0]; c.bh = shapes[si][1]; c.mb = shapes[si][2] == 2 ? 2 : 1;
                     if (c.mb == 2 && !cvt) continue;  // (two M blocks: the in-kernel fold only)
                     if (g.flat) {
                         const long long M = (long long)p->s.n * p->s.h * g.wx;
