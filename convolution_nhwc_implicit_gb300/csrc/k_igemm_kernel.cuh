@@ -536,6 +536,15 @@ __device__ __forceinline__ void epilogue_swapped_tma(const IgArgs &a, const CUte
 // The raw weights arrive once by a bulk copy into the raw region, and the
 // converter writes the folded resident blocks from them (each (co, r) row's
 // k_w * Cin values, zero-padded) before the raw ring reuses that memory.
+//
+// MB == 2 (CVT == 2 with halo staging and an epilogue per tile, BN = 64): a
+// tile is two 128-pixel M blocks stacked (its top and bottom bh / 2 rows),
+// so the producer, the converter and the ring handshakes run once per 256
+// pixels.  Each tap's MMA is issued for both blocks — the second reads the
+// box's pixel rows from 128 rows further — into two BN-column accumulators
+// side by side, and the epilogue stores them as two boxes of bh / 2 rows.
+// The per-tile fixed costs of these roles, not their arithmetic, paced the
+// one-block stem.
 template <int BN, int BK, bool FLAT, bool SWAP, bool PAIR, bool FUSED, bool HALO = false, bool EPT = false,
           int CVT = 0, int MB = 1>
 __global__ void __launch_bounds__(cta_threads(BN, SWAP, EPT, CVT), 1)
